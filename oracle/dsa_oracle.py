@@ -1,0 +1,265 @@
+"""Plain, slow CPU oracle of the DeepSeek Sparse Attention decode hot path.
+
+TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the CPU
+baseline of the benchmark; the CUDA path never imports it.
+
+Everything is float64 unless a page fixes a precision.  Page citations name
+the page and its section:
+
+* [V4-TileLang] "NPU DeepSeek-V4 TileLang算子开发实践" (TileLang-Ascend
+  DeepSeek-V4 operators): sections Sparse Flash Attention (steps 1-8),
+  Int8 General Matrix Multiplication (steps 1-4), Activation Quantization
+  (steps 1-4).
+* [V3.2-PyPTO] "NPU DeepSeek-V3.2-Exp PyPTO 融合算子开发优化实践" (PyPTO
+  fused operators): sections Indexer Prolog (the Indexer Q, Indexer Cache
+  and Indexer Weight formulas and the quantisation strategy paragraph),
+  Deepseek Indexer Attention, Lightning Indexer.
+
+Readings taken where the pages are silent or garbled are stated at each
+function.  Pins: tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+__all__ = [
+    "bf16_bits_to_f64", "sylvester_hadamard", "hadamard_rows", "dynamic_quant",
+    "int8_gemm_dequant", "rope", "layer_norm", "indexer_prolog",
+    "indexer_dots", "indexer_scores_token", "topk_indices",
+    "sparse_attention_token", "sparse_attention", "logical_rows",
+]
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Decode raw bf16 bit patterns (uint16) to float64 exactly."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(F64)
+
+
+# ----------------------------------------------------------------------------
+# Hadamard transform  [V3.2-PyPTO §Indexer Prolog: "the Hadamard transform is
+# a right-multiplication by hadamard_q / hadamard_k"]
+# ----------------------------------------------------------------------------
+def sylvester_hadamard(n: int) -> np.ndarray:
+    """Unscaled Sylvester Hadamard matrix of order n (a power of two):
+    H_1 = [1], H_2m = [[H_m, H_m], [H_m, -H_m]] (natural order).
+    Reading: the pages give no order or scale; Sylvester natural order with
+    a 1/sqrt(n) scale (orthonormal) is used."""
+    assert n >= 1 and n & (n - 1) == 0
+    h = np.ones((1, 1), dtype=F64)
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def hadamard_rows(x: np.ndarray) -> np.ndarray:
+    """x @ (H_n / sqrt(n)) over the last axis, as an explicit matrix product."""
+    n = x.shape[-1]
+    return np.asarray(x, dtype=F64) @ (sylvester_hadamard(n) / np.sqrt(n))
+
+
+# ----------------------------------------------------------------------------
+# DynamicQuant  [V4-TileLang §Activation Quantization steps 1-3;
+# V3.2-PyPTO §Indexer Prolog: per-token-head int8, FP16 dequant factors]
+# ----------------------------------------------------------------------------
+def dynamic_quant(x: np.ndarray):
+    """Symmetric int8 quantisation of each row (last axis).
+
+    Steps as the Activation Quantization section orders them, in fp32 as it
+    states: (1) take |x| in fp32 and its row maximum; (2) scale = max / 127
+    (round_scale=False); (3) y = round(clamp(x / scale, -127, 127)).
+    Readings: the scale is stored as FP16 (V3.2-PyPTO) and the division uses
+    that stored FP16 value, so that code * scale is exactly the dequantised
+    value a consumer sees; rounding is half-to-even; a row whose stored
+    scale is 0 gets all-zero codes.
+    Returns (codes int8, scale fp16)."""
+    x32 = np.asarray(x, dtype=F64).astype(np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s32 = amax / np.float32(127.0)
+    s16 = s32.astype(np.float16)
+    sdiv = s16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = x32 / sdiv
+    y = np.clip(y, np.float32(-127.0), np.float32(127.0))
+    codes = np.where(sdiv > 0, np.rint(y), np.float32(0.0))
+    return codes.astype(np.int8), s16
+
+
+# ----------------------------------------------------------------------------
+# Int8 GEMM + dequant  [V4-TileLang §Int8 GEMM steps 1-3]
+# ----------------------------------------------------------------------------
+def int8_gemm_dequant(a: np.ndarray, a_scale: np.ndarray, b: np.ndarray,
+                      b_scale: np.ndarray) -> np.ndarray:
+    """C[i, j] = (sum_k a[i,k] * b[j,k]) * a_scale[i] * b_scale[j].
+
+    a int8 [M, K] with a_scale [M]; b int8 [N, K] (K-major, as the page's
+    b_int8 [N, K]) with b_scale [N].  The integer sum is exact (a float64
+    matmul of int8 values is exact: every partial sum is an integer far
+    below 2^53); the dequant is float64 (reading: the fused prolog keeps full
+    precision up to the quantiser, no fp16 output cast)."""
+    acc = np.asarray(a, dtype=F64) @ np.asarray(b, dtype=F64).T
+    return acc * np.asarray(a_scale, dtype=F64)[:, None] * np.asarray(b_scale, dtype=F64)[None, :]
+
+
+# ----------------------------------------------------------------------------
+# RoPE  [V3.2-PyPTO §Indexer Prolog, Indexer Q and Indexer Cache formulas]
+# ----------------------------------------------------------------------------
+def rope(x: np.ndarray, pos: np.ndarray, cos_tab: np.ndarray, sin_tab: np.ndarray,
+         d_rope: int, interleaved: bool = False) -> np.ndarray:
+    """Rotate dims [0, d_rope) of x [T, ..., d] by angle(pos[t], i).
+
+    Readings (the pages give none of these): the first d_rope dims rotate,
+    the rest pass through; pairs are (i, i + d_rope/2) ("half split"), or
+    (2i, 2i+1) when interleaved; cos/sin come from the given tables
+    [max_pos, d_rope/2]; pair (a, b) maps to (a cos - b sin, b cos + a sin)."""
+    x = np.asarray(x, dtype=F64)
+    out = x.copy()
+    half = d_rope // 2
+    pos = np.asarray(pos, dtype=np.int64)
+    extra = (1,) * (x.ndim - 2)
+    c = np.asarray(cos_tab, dtype=F64)[pos].reshape((x.shape[0],) + extra + (half,))
+    s = np.asarray(sin_tab, dtype=F64)[pos].reshape((x.shape[0],) + extra + (half,))
+    i = np.arange(half)
+    ia, ib = (2 * i, 2 * i + 1) if interleaved else (i, i + half)
+    xa, xb = x[..., ia], x[..., ib]
+    out[..., ia] = xa * c - xb * s
+    out[..., ib] = xb * c + xa * s
+    return out
+
+
+def layer_norm(x: np.ndarray, gamma, beta, eps: float) -> np.ndarray:
+    """LayerNorm over the last axis [V3.2-PyPTO §Indexer Prolog, Indexer Cache
+    formula].  Reading: biased variance, eps inside the square root, affine
+    gamma/beta."""
+    x = np.asarray(x, dtype=F64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * np.asarray(gamma, F64) + np.asarray(beta, F64)
+
+
+# ----------------------------------------------------------------------------
+# Indexer Prolog  [V3.2-PyPTO §Indexer Prolog, the three formulas]
+# ----------------------------------------------------------------------------
+def indexer_prolog(p, k_cache=None, k_scale_cache=None):
+    """The three independent streams of the Indexer Prolog.
+
+      q, q_scale = DynamicQuant(Hadamard(RoPE(DeQuant(q_lora . w_qb))))
+      k, k_scale = DynamicQuant(Hadamard(RoPE(LayerNorm(x . w_k))))
+      weight     = (x . w_proj) * w_scale
+
+    ``p`` carries the fields of workloads.PrologInputs (plain arrays).  q is
+    quantised per (token, head), k per token.  When caches are given, row
+    slot[t] >= 0 receives k[t] / k_scale[t].  Returns a dict with q [T,H,D]
+    int8, q_scale [T,H] fp16, k [T,D] int8, k_scale [T] fp16 and, if w_proj
+    is given, w [T,H] fp32 (reading: fp32 output, not the page's FP16)."""
+    T, H, D = p.T, p.H_I, p.d_I
+    qf = int8_gemm_dequant(p.q_lora, p.q_lora_scale, p.w_qb, p.w_qb_scale).reshape(T, H, D)
+    qr = rope(qf, p.pos, p.rope_cos, p.rope_sin, p.d_rope, bool(p.rope_interleaved))
+    q, q_scale = dynamic_quant(hadamard_rows(qr))
+
+    x = bf16_bits_to_f64(p.x)
+    kf = x @ bf16_bits_to_f64(p.w_k).T
+    kn = layer_norm(kf, p.ln_gamma, p.ln_beta, p.ln_eps)
+    kr = rope(kn[:, None, :], p.pos, p.rope_cos, p.rope_sin, p.d_rope,
+              bool(p.rope_interleaved))[:, 0, :]
+    k, k_scale = dynamic_quant(hadamard_rows(kr))
+
+    out = {"q": q, "q_scale": q_scale, "k": k, "k_scale": k_scale,
+           "q_prequant": hadamard_rows(qr), "k_prequant": hadamard_rows(kr)}
+    if p.w_proj is not None:
+        out["w"] = ((x @ bf16_bits_to_f64(p.w_proj).T) * float(p.w_scale)).astype(np.float32)
+    if k_cache is not None:
+        for t in range(T):
+            if p.slot[t] >= 0:
+                k_cache[p.slot[t]] = k[t]
+                k_scale_cache[p.slot[t]] = k_scale[t]
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Lightning Indexer  [V3.2-PyPTO §Lightning Indexer: int8 q against the C8
+# key cache, then a per-query TopK; §Indexer Prolog for the scale types]
+# ----------------------------------------------------------------------------
+def logical_rows(inp, b: int, n: int) -> np.ndarray:
+    """Physical cache rows of keys 0..n-1 of sequence b (contiguous
+    [B, max_L, .] or paged through block_table[b, s // block_size])."""
+    s = np.arange(n, dtype=np.int64)
+    if inp.block_table is None:
+        return b * inp.max_L + s
+    blk = inp.block_table[b, s // inp.block_size].astype(np.int64)
+    return blk * inp.block_size + s % inp.block_size
+
+
+def indexer_dots(q_tok: np.ndarray, keys: np.ndarray) -> np.ndarray:
+    """Exact int64 dots [H, n] = q_tok[h] . keys[s] (int8 x int8)."""
+    d = np.asarray(q_tok, dtype=F64) @ np.asarray(keys, dtype=F64).T
+    return d.astype(np.int64)
+
+
+def indexer_scores_token(q_tok, q_scale_tok, w_tok, keys, key_scale, pos_t: int):
+    """I[s] = ks[s] * sum_h w[h] * qs[h] * ReLU(q[h] . K[s]) for s <= pos_t,
+    -inf for s > pos_t.
+
+    Reading: the score is sum_h w[h] * ReLU(q_h . k_s) on the dequantised
+    operands; as both scales are non-negative, ReLU(qs*ks*dot) =
+    qs*ks*ReLU(dot), which is the factorisation written here."""
+    dots = indexer_dots(q_tok, keys).astype(F64)
+    coef = np.asarray(w_tok, F64) * np.asarray(q_scale_tok, F64)
+    I = np.asarray(key_scale, F64) * (coef[:, None] * np.maximum(dots, 0.0)).sum(axis=0)
+    I[np.arange(keys.shape[0]) > pos_t] = -np.inf
+    return I
+
+
+def topk_indices(scores: np.ndarray, n_valid: int, k: int) -> np.ndarray:
+    """Indices of the k largest scores among positions [0, n_valid), by a
+    full sort (score descending, then index ascending); if fewer than k are
+    valid, all valid positions then -1 (the unused-slot marker of
+    [V4-TileLang §Sparse Flash Attention step 2])."""
+    s = np.asarray(scores, dtype=F64)[:n_valid]
+    order = np.lexsort((np.arange(n_valid), -s))
+    sel = order[:k]
+    out = np.full(k, -1, dtype=np.int64)
+    out[:sel.size] = sel
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Sparse Flash Attention  [V4-TileLang §Sparse Flash Attention steps 2-6, 8]
+# ----------------------------------------------------------------------------
+def sparse_attention_token(q_tok: np.ndarray, rows: np.ndarray, scale: float, d_v: int):
+    """Softmax attention of q_tok [H, d_qk] over the selected latent rows
+    [n, d_qk] (value = first d_v dims).  Returns (out [H, d_v], lse [H]),
+    lse = natural log of sum_j exp(scale * q.k_j).  No rows: out 0, lse -inf.
+    Reading: the online softmax of the page computes exactly this; the
+    attention sink (step 7) is not applied."""
+    q = np.asarray(q_tok, dtype=F64)
+    H = q.shape[0]
+    if rows.shape[0] == 0:
+        return np.zeros((H, d_v)), np.full(H, -np.inf)
+    kv = np.asarray(rows, dtype=F64)
+    S = scale * (q @ kv.T)
+    m = S.max(axis=1, keepdims=True)
+    p = np.exp(S - m)
+    l = p.sum(axis=1, keepdims=True)
+    out = (p @ kv[:, :d_v]) / l
+    return out, (m + np.log(l))[:, 0]
+
+
+def sparse_attention(inp, topk_idx: np.ndarray, tokens=None):
+    """Sparse attention for the given tokens of a workloads.DecodeInputs-like
+    object; index -1 selects nothing.  Returns (out [n_tok, H, d_v], lse)."""
+    if tokens is None:
+        tokens = range(inp.T)
+    outs, lses = [], []
+    for t in tokens:
+        idx = np.asarray(topk_idx[t], dtype=np.int64)
+        idx = idx[idx >= 0]
+        b = int(inp.seq_of_token[t])
+        phys = np.asarray(inp.physical_row(b, idx)) if idx.size else np.zeros(0, np.int64)
+        rows = bf16_bits_to_f64(inp.kv_cache[phys])
+        o, l = sparse_attention_token(bf16_bits_to_f64(inp.q_attn[t]), rows, inp.scale, inp.d_v)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)

@@ -1,0 +1,350 @@
+"""Pins of the CPU oracle to facts outside itself: closed forms, library
+routines, brute force and a hand-worked case.  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.special
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+# ---------------------------------------------------------------- Hadamard
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 64, 128, 256])
+def test_hadamard_is_sylvester_and_orthogonal(n):
+    H = O.sylvester_hadamard(n)
+    np.testing.assert_array_equal(H, scipy.linalg.hadamard(n))  # Sylvester natural order
+    np.testing.assert_array_equal(H @ H, n * np.eye(n))         # H.H = n.I (H symmetric)
+
+
+def _fwht(v):
+    """Independent recursive fast Walsh-Hadamard butterfly (natural order)."""
+    v = list(v)
+    if len(v) == 1:
+        return v
+    h = len(v) // 2
+    a, b = _fwht(v[:h]), _fwht(v[h:])
+    return [x + y for x, y in zip(a, b)] + [x - y for x, y in zip(a, b)]
+
+
+def test_hadamard_rows_matches_butterfly_and_keeps_norm():
+    x = rng.standard_normal((3, 128))
+    y = O.hadamard_rows(x)
+    ref = np.array([_fwht(r) for r in x]) / math.sqrt(128)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-12)
+    e0 = np.zeros(128); e0[0] = 1
+    np.testing.assert_allclose(O.hadamard_rows(e0), np.full(128, 1 / math.sqrt(128)), atol=1e-15)
+
+
+# ---------------------------------------------------------- DynamicQuant
+def test_quant_argmax_maps_to_127_and_error_bound():
+    x = rng.standard_normal((50, 128)) * rng.uniform(0.01, 10, size=(50, 1))
+    c, s = O.dynamic_quant(x)
+    assert c.dtype == np.int8 and s.dtype == np.float16
+    am = np.argmax(np.abs(x), axis=1)
+    np.testing.assert_array_equal(np.abs(c[np.arange(50), am]), 127)
+    np.testing.assert_array_equal(np.sign(c[np.arange(50), am]), np.sign(x[np.arange(50), am]))
+    sf = s.astype(np.float64)[:, None]
+    err = np.abs(c * sf - x)
+    # half a step, plus the clamp of |x| <= amax against 127*fp16(amax/127)
+    assert (err <= sf * 0.5 + np.abs(x).max(1, keepdims=True) * 2.0 ** -10).all()
+    assert np.abs(c).max() <= 127
+
+
+def test_quant_zero_row_and_exact_grid():
+    c, s = O.dynamic_quant(np.zeros((2, 64)))
+    assert (c == 0).all() and (s == 0).all()
+    s16 = np.float16(0.0371)
+    codes = rng.integers(-127, 128, size=128)
+    codes[5] = -127
+    x = codes.astype(np.float64) * float(s16)
+    c, s = O.dynamic_quant(x[None])
+    assert s[0] == s16
+    np.testing.assert_array_equal(c[0], codes)
+
+
+def test_quant_rounds_half_to_even():
+    # scale 1.0 exactly (amax 127): x / scale lands on .5 ties
+    x = np.array([127.0, 2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5] + [0.0] * 8)
+    c, s = O.dynamic_quant(x[None])
+    assert float(s[0]) == 1.0
+    np.testing.assert_array_equal(c[0, :8], [127, 2, 4, -2, -4, 0, 0, 2])
+
+
+# ------------------------------------------------------------ Int8 GEMM
+def test_int8_gemm_brute_force_and_closed_form():
+    a = rng.integers(-128, 128, size=(3, 7)).astype(np.int8)
+    b = rng.integers(-128, 128, size=(5, 7)).astype(np.int8)
+    sa = np.array([1.0, 0.5, 2.0], np.float16)
+    sb = np.array([1.0, 0.25, 3.0, 0.125, 1.5], np.float16)
+    got = O.int8_gemm_dequant(a, sa, b, sb)
+    for i in range(3):
+        for j in range(5):
+            acc = sum(int(a[i, k]) * int(b[j, k]) for k in range(7))
+            assert got[i, j] == acc * float(sa[i]) * float(sb[j])
+    K = 1536
+    full = O.int8_gemm_dequant(np.full((2, K), 127, np.int8), np.ones(2, np.float16),
+                               np.full((3, K), 127, np.int8), np.ones(3, np.float16))
+    assert (full == 16129 * K).all()
+    neg = O.int8_gemm_dequant(np.full((1, K), -128, np.int8), np.ones(1, np.float16),
+                              np.full((1, K), -128, np.int8), np.ones(1, np.float16))
+    assert neg[0, 0] == 16384 * K
+
+
+# ------------------------------------------------------------------ RoPE
+def _tables(max_pos, d_rope, base=10000.0):
+    from sparse_attention_prolog_gb300.workloads import rope_tables
+    return rope_tables(max_pos, d_rope, base)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_rope_matches_complex_rotation(interleaved):
+    T, H, d, dr = 5, 3, 128, 64
+    cos, sin = _tables(70000, dr)
+    pos = np.array([0, 1, 17, 4095, 65535])
+    x = rng.standard_normal((T, H, d))
+    y = O.rope(x, pos, cos, sin, dr, interleaved)
+    half = dr // 2
+    theta = 10000.0 ** (-(2.0 * np.arange(half)) / dr)
+    ia = 2 * np.arange(half) if interleaved else np.arange(half)
+    ib = ia + 1 if interleaved else ia + half
+    z = (x[..., ia] + 1j * x[..., ib]) * np.exp(1j * pos[:, None, None] * theta)
+    # tables are fp32-rounded: compare within fp32 angle rounding
+    np.testing.assert_allclose(y[..., ia], z.real, atol=2e-6 * np.abs(x).max())
+    np.testing.assert_allclose(y[..., ib], z.imag, atol=2e-6 * np.abs(x).max())
+    np.testing.assert_array_equal(y[..., dr:], x[..., dr:])
+    np.testing.assert_array_equal(y[0], x[0])  # pos 0 is the identity
+    np.testing.assert_allclose(np.hypot(y[..., ia], y[..., ib]), np.hypot(x[..., ia], x[..., ib]),
+                               rtol=1e-6)
+
+
+def test_rope_conventions_agree_after_permutation():
+    cos, sin = _tables(64, 64)
+    x = rng.standard_normal((4, 2, 128))
+    pos = np.array([3, 9, 27, 63])
+    perm = np.concatenate([np.stack([np.arange(32), np.arange(32) + 32], 1).reshape(-1),
+                           np.arange(64, 128)])  # half-split order -> interleaved order
+    y_half = O.rope(x, pos, cos, sin, 64, False)
+    y_int = O.rope(x[..., perm], pos, cos, sin, 64, True)
+    np.testing.assert_allclose(y_int, y_half[..., perm], rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------- LayerNorm
+def test_layer_norm_matches_torch_and_closed_form():
+    x = rng.standard_normal((6, 128)) * 3 + 1
+    g = rng.standard_normal(128)
+    b = rng.standard_normal(128)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (128,), torch.from_numpy(g),
+                                         torch.from_numpy(b), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.layer_norm(x, g, b, 1e-6), ref, rtol=1e-12, atol=1e-12)
+    y = O.layer_norm(x, np.ones(128), np.zeros(128), 1e-6)
+    v = x.var(axis=1)
+    np.testing.assert_allclose(y.mean(1), 0, atol=1e-12)
+    np.testing.assert_allclose(y.var(1), v / (v + 1e-6), rtol=1e-12)
+
+
+# ---------------------------------------------------------- Indexer Prolog
+def _prolog_fixture(T=1, H=2, D=128, Kq=16, Dx=32, pos=(0,)):
+    from sparse_attention_prolog_gb300.workloads import PrologInputs, f32_to_bf16_bits
+    cos, sin = _tables(max(pos) + 1, 64)
+    return PrologInputs(
+        T=T, H_I=H, d_I=D, d_rope=64,
+        q_lora=np.zeros((T, Kq), np.int8), q_lora_scale=np.ones(T, np.float16),
+        w_qb=np.zeros((H * D, Kq), np.int8), w_qb_scale=np.ones(H * D, np.float16),
+        x=f32_to_bf16_bits(np.zeros((T, Dx), np.float32)),
+        w_k=f32_to_bf16_bits(np.zeros((D, Dx), np.float32)),
+        ln_gamma=np.ones(D, np.float32), ln_beta=np.zeros(D, np.float32), ln_eps=1e-6,
+        w_proj=None, w_scale=1.0, pos=np.array(pos, np.int32), rope_cos=cos, rope_sin=sin,
+        rope_interleaved=0, slot=np.full(T, -1, np.int64))
+
+
+def test_prolog_q_one_hot_gives_hadamard_row_codes():
+    """q_lora . w_qb = one-hot e_j per head -> Hadamard row j -> codes 127*H[j]."""
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    p = _prolog_fixture()
+    p.q_lora[0, 3] = 5
+    p.q_lora_scale[0] = np.float16(0.5)
+    js = [70, 5]       # head 0: a pass-through dim; head 1: a rotated dim at pos 0
+    for h, j in enumerate(js):
+        p.w_qb[h * 128 + j, 3] = 2
+        p.w_qb_scale[h * 128 + j] = np.float16(0.2)
+    p.x = f32_to_bf16_bits(np.zeros((1, 32), np.float32))
+    r = O.indexer_prolog(p)
+    H = scipy.linalg.hadamard(128)
+    amp = 5 * 2 * 0.5 * float(np.float16(0.2)) / math.sqrt(128)
+    for h, j in enumerate(js):
+        np.testing.assert_array_equal(r["q"][0, h], 127 * H[j])
+        expect = np.float16(np.float32(amp) / np.float32(127))
+        assert r["q_scale"][0, h] == expect
+
+
+def test_prolog_k_alternating_gives_single_code():
+    """x . w_k = alternating +-a -> LayerNorm -> +-1 -> Hadamard -> sqrt(128) e_1."""
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    p = _prolog_fixture(Dx=4)
+    p.x = f32_to_bf16_bits(np.array([[3.0, 0, 0, 0]], np.float32))
+    wk = np.zeros((128, 4), np.float32)
+    wk[:, 0] = np.where(np.arange(128) % 2 == 0, 1.0, -1.0)
+    p.w_k = f32_to_bf16_bits(wk)
+    p.ln_eps = 0.0
+    r = O.indexer_prolog(p)
+    expect = np.zeros(128, np.int64); expect[1] = 127
+    np.testing.assert_array_equal(r["k"][0], expect)
+    assert r["k_scale"][0] == np.float16(np.float32(math.sqrt(128)) / np.float32(127))
+
+
+def test_prolog_weight_stream_and_cache_write_brute_force():
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    p = _prolog_fixture(T=2, Dx=6, pos=(0, 1))
+    xv = rng.standard_normal((2, 6)).astype(np.float32)
+    wp = rng.standard_normal((2, 6)).astype(np.float32)
+    p.x, p.w_proj, p.w_scale = f32_to_bf16_bits(xv), f32_to_bf16_bits(wp), 0.125
+    p.slot = np.array([3, -1], np.int64)
+    cache = np.full((5, 128), 9, np.int8)
+    cs = np.full(5, 7, np.float16)
+    r = O.indexer_prolog(p, cache, cs)
+    xb = O.bf16_bits_to_f64(p.x)
+    wb = O.bf16_bits_to_f64(p.w_proj)
+    for t in range(2):
+        for h in range(2):
+            ref = sum(xb[t, c] * wb[h, c] for c in range(6)) * 0.125
+            assert abs(float(r["w"][t, h]) - ref) <= 1e-6 * max(1.0, abs(ref))
+    np.testing.assert_array_equal(cache[3], r["k"][0])
+    assert cs[3] == r["k_scale"][0]
+    assert (cache[[0, 1, 2, 4]] == 9).all() and (cs[[0, 1, 2, 4]] == 7).all()
+
+
+# ------------------------------------------------------- Lightning Indexer
+def _read_golden():
+    g = {}
+    with open(os.path.join(GOLDEN, "indexer_hand_case.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            key = parts[0] + ("_" + parts[1] if parts[0] in ("q", "k", "dots") else "")
+            vals = parts[2:] if parts[0] in ("q", "k", "dots") else parts[1:]
+            g[key] = [float(v) for v in vals]
+    return g
+
+
+def test_indexer_hand_worked_case():
+    g = _read_golden()
+    q = np.array([g["q_h0"], g["q_h1"]], np.int8)
+    K = np.array([g["k_s0"], g["k_s1"]], np.int8)
+    w = np.array(g["w"], np.float32)
+    np.testing.assert_array_equal(O.indexer_dots(q, K), [g["dots_h0"], g["dots_h1"]])
+    I = O.indexer_scores_token(q, np.ones(2, np.float16), w, K, np.ones(2, np.float16), pos_t=1)
+    np.testing.assert_array_equal(I, g["scores"])
+    np.testing.assert_array_equal(O.topk_indices(I, 2, 1), g["top1"])
+    np.testing.assert_array_equal(O.topk_indices(I, 2, 2), g["top2"])
+    I0 = O.indexer_scores_token(q, np.ones(2, np.float16), w, K, np.ones(2, np.float16), pos_t=0)
+    np.testing.assert_array_equal(O.topk_indices(I0, 1, 2), g["top2_pos0"])
+
+
+def test_indexer_scores_brute_force_loops():
+    H, D, n = 3, 8, 11
+    q = rng.integers(-127, 128, size=(H, D)).astype(np.int8)
+    K = rng.integers(-127, 128, size=(n, D)).astype(np.int8)
+    qs = rng.uniform(0.01, 0.05, H).astype(np.float16)
+    ks = rng.uniform(0.01, 0.05, n).astype(np.float16)
+    w = rng.standard_normal(H).astype(np.float32)
+    I = O.indexer_scores_token(q, qs, w, K, ks, pos_t=7)
+    for s in range(n):
+        if s > 7:
+            assert I[s] == -np.inf
+            continue
+        ref = 0.0
+        for h in range(H):
+            # dequantise both operands first, then ReLU of the real dot
+            dot = sum(float(q[h, d]) * float(qs[h]) * float(K[s, d]) * float(ks[s]) for d in range(D))
+            ref += float(w[h]) * max(dot, 0.0)
+        assert abs(I[s] - ref) <= 1e-12 * max(1.0, abs(ref))
+    assert O.indexer_dots(np.full((1, 128), 127, np.int8), np.full((1, 128), -127, np.int8))[0, 0] \
+        == -16129 * 128
+
+
+# ------------------------------------------------------------------ Top-k
+def test_topk_against_library_selection():
+    s = rng.standard_normal(5000)
+    k = 300
+    got = O.topk_indices(s, 4000, k)
+    ref = np.argpartition(-s[:4000], k)[:k]
+    assert set(got.tolist()) == set(ref.tolist())
+    assert (np.diff(s[got]) <= 0).all()  # sorted by score, descending
+    perm = rng.permutation(4000)
+    got_p = O.topk_indices(s[:4000][perm], 4000, k)
+    assert set(perm[got_p].tolist()) == set(got.tolist())
+
+
+def test_topk_short_rows_and_ties():
+    s = np.array([1.0, 5.0, 5.0, -2.0, 7.0])
+    np.testing.assert_array_equal(O.topk_indices(s, 3, 5), [1, 2, 0, -1, -1])
+    np.testing.assert_array_equal(O.topk_indices(s, 5, 2), [4, 1])   # tie 1/2 -> lower index
+    np.testing.assert_array_equal(O.topk_indices(s, 0, 3), [-1, -1, -1])
+
+
+# ------------------------------------------------------- Sparse attention
+def _bf16(x):
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    return O.bf16_bits_to_f64(f32_to_bf16_bits(x.astype(np.float32)))
+
+
+def test_attention_equals_dense_masked_sdpa():
+    H, L, d, dv, scale = 4, 40, 576, 512, 192 ** -0.5
+    q = _bf16(rng.standard_normal((H, d)))
+    kv = _bf16(rng.standard_normal((L, d)))
+    sel = np.array([3, 17, 0, 39, 22, 8])
+    out, lse = O.sparse_attention_token(q, kv[sel], scale, dv)
+    mask = torch.zeros(H, L, dtype=torch.bool)
+    mask[:, torch.from_numpy(sel)] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(kv)[None], torch.from_numpy(kv[:, :dv])[None],
+        attn_mask=mask[None], scale=scale)[0].numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    full = scale * q @ kv.T
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(full[:, sel], axis=1), rtol=1e-12)
+
+
+def test_attention_special_cases():
+    H, d, dv = 3, 576, 512
+    q = _bf16(rng.standard_normal((H, d)))
+    rows = _bf16(rng.standard_normal((5, d)))
+    out, _ = O.sparse_attention_token(q, rows[:1], 0.1, dv)      # one row -> its value
+    np.testing.assert_allclose(out, np.repeat(rows[:1, :dv], H, 0), rtol=1e-14)
+    # identical keys -> mean of the values: q is zero on the value dims and
+    # all rows share dims >= dv, so every score is equal
+    q2 = q.copy(); q2[:, :dv] = 0
+    mix = rows[1:5].copy(); mix[:, dv:] = rows[0, dv:]
+    out2, lse2 = O.sparse_attention_token(q2, mix, 0.1, dv)
+    np.testing.assert_allclose(out2, np.repeat(mix[:, :dv].mean(0, keepdims=True), H, 0), rtol=1e-12)
+    np.testing.assert_allclose(lse2, 0.1 * q2 @ rows[0] + math.log(4), rtol=1e-12)
+    out3, lse3 = O.sparse_attention_token(q, rows[:0], 0.1, dv)
+    assert (out3 == 0).all() and np.isneginf(lse3).all()
+    # a duplicated index is counted twice
+    o_dup, _ = O.sparse_attention_token(q, rows[[0, 0, 1]], 0.1, dv)
+    w = np.exp(0.1 * q @ rows[[0, 1]].T)
+    w[:, 0] *= 2
+    ref = (w @ rows[[0, 1], :dv]) / w.sum(1, keepdims=True)
+    np.testing.assert_allclose(o_dup, ref, rtol=1e-12)
+
+
+def test_attention_all_causal_keys_is_causal_attention():
+    H, L, d, dv, scale = 2, 16, 576, 512, 192 ** -0.5
+    q = _bf16(rng.standard_normal((L, H, d)))
+    kv = _bf16(rng.standard_normal((L, d)))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).transpose(0, 1), torch.from_numpy(kv)[None].expand(H, L, d),
+        torch.from_numpy(kv[:, :dv])[None].expand(H, L, dv), is_causal=True,
+        scale=scale).transpose(0, 1).numpy()
+    for t in range(L):
+        out, _ = O.sparse_attention_token(q[t], kv[: t + 1], scale, dv)
+        np.testing.assert_allclose(out, ref[t], rtol=1e-10, atol=1e-12)
