@@ -1,0 +1,225 @@
+/*
+ * dsa.h - C ABI of the DeepSeek Sparse Attention (DSA) decode hot path on
+ * GB300 (sm_103a):
+ *
+ *   dsa_indexer_prolog  : Indexer Prolog (q / k / weight streams)
+ *   dsa_indexer_topk    : Lightning Indexer scores + per-query top-k
+ *   dsa_sparse_attn     : Sparse (MLA) flash attention over the top-k rows
+ *
+ * Page citations:
+ *   [V3.2-PyPTO]  "NPU DeepSeek-V3.2-Exp PyPTO 融合算子开发优化实践",
+ *                 sections Indexer Prolog, Deepseek Indexer Attention,
+ *                 Lightning Indexer.
+ *   [V4-TileLang] "NPU DeepSeek-V4 TileLang算子开发实践", sections Sparse
+ *                 Flash Attention, Int8 General Matrix Multiplication,
+ *                 Activation Quantization.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer inside an args struct is a DEVICE pointer owned by the
+ *     caller; the library never allocates or frees device memory on these
+ *     paths.  Scratch memory is a caller-provided device workspace whose
+ *     size the matching *_workspace() call returns.
+ *   - fp16 / bf16 values are passed as their raw 16-bit patterns
+ *     (uint16_t).  All arrays are dense, row-major, without padding.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; argument checks run on the host before any
+ *     launch, and a rejected call enqueues nothing.
+ *   - Return value: DSA_OK or an error status.  No C++ exception crosses
+ *     this boundary.  A launch failure returns DSA_ERR_CUDA.  A kernel whose
+ *     bounded wait expired records it in a device error word that
+ *     dsa_get_device_error() reads (DSA_ERR_DEVICE_TIMEOUT).
+ *   - T = 0 (no query tokens) is a no-op returning DSA_OK.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size or alignment        */
+  DSA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d_I = 96)  */
+  DSA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than needed   */
+  DSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed       */
+  DSA_ERR_DEVICE_TIMEOUT = 5 /* a device-side bounded wait expired         */
+} dsa_status_t;
+
+/* Static description of a status code.  Never NULL. */
+const char* dsa_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int dsa_abi_version(void);
+
+/* Synchronises `stream`, then returns DSA_OK if no kernel of this library
+ * has recorded a device-side error since the last call, else
+ * DSA_ERR_DEVICE_TIMEOUT; the error word is cleared.  DSA_ERR_CUDA if the
+ * synchronisation itself fails. */
+int dsa_get_device_error(void* stream);
+
+/* ------------------------------------------------------------------------
+ * Indexer Prolog  [V3.2-PyPTO §Indexer Prolog, the three formulas; the
+ * quantisation paragraph: W8A8 q.w_qb, A8 indexer q, C8 key cache, FP16
+ * dequant factors; V4-TileLang §Int8 GEMM steps 1-3 and §Activation
+ * Quantization steps 1-3]
+ *
+ *   q, q_scale = DynamicQuant(Hadamard(RoPE(DeQuant(q_lora . w_qb))))
+ *   k, k_scale = DynamicQuant(Hadamard(RoPE(LayerNorm(x . w_k))))
+ *   w          = (x . w_proj) * w_scale                (optional)
+ *
+ * DeQuant: acc[t,n] = sum_c q_lora[t,c] * w_qb[n,c] (exact int32), times
+ * q_lora_scale[t] * w_qb_scale[n] in fp32.  RoPE rotates dims [0, d_rope)
+ * of each d_I-dim head by the fp32 tables rope_cos/rope_sin
+ * [rope_max_pos, d_rope/2] at row pos[t]; pairs are (i, i + d_rope/2), or
+ * (2i, 2i+1) if rope_interleaved.  Hadamard is the Sylvester transform of
+ * order d_I scaled by d_I^-1/2.  DynamicQuant per (token, head) row:
+ * scale = fp16(absmax / 127) (the division in fp32), code =
+ * round_half_even(clamp(x / scale, -127, 127)), code 0 when scale is 0.
+ * LayerNorm: biased variance, eps inside the square root, fp32 gamma/beta.
+ *
+ * Shapes: q_lora int8 [T, K_q]; q_lora_scale fp16 [T]; w_qb int8
+ * [H_I*d_I, K_q] (K-major: row n is output channel n); w_qb_scale fp16
+ * [H_I*d_I]; x bf16 [T, D_x]; w_k bf16 [d_I, D_x]; w_proj bf16 [H_I, D_x]
+ * or NULL; pos int32 [T] (each in [0, rope_max_pos)); q_out int8
+ * [T, H_I, d_I]; q_scale_out fp16 [T, H_I]; k_cache int8 [cache_rows, d_I];
+ * k_scale_cache fp16 [cache_rows]; slot int64 [T]: row of k_cache that
+ * receives token t's key, -1 = none (slots must not repeat); w_out fp32
+ * [T, H_I] (required iff w_proj != NULL).
+ * Supported: 1 <= T <= 32, d_I in {64, 128}, 1 <= H_I <= 128, d_rope even
+ * with d_rope <= d_I and (d_rope/2) a multiple of d_I/32, K_q and D_x
+ * multiples of 64.  Workspace: dsa_indexer_prolog_workspace() bytes; it must
+ * be zero-filled once before its first use (the library leaves it zeroed).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, H_I, d_I, d_rope, K_q, D_x;
+  const int8_t* q_lora;
+  const uint16_t* q_lora_scale;
+  const int8_t* w_qb;
+  const uint16_t* w_qb_scale;
+  const uint16_t* x;
+  const uint16_t* w_k;
+  const float* ln_gamma;
+  const float* ln_beta;
+  float ln_eps;
+  const uint16_t* w_proj;
+  float w_scale;
+  const int32_t* pos;
+  const float* rope_cos;
+  const float* rope_sin;
+  int32_t rope_max_pos;
+  int32_t rope_interleaved;
+  int8_t* q_out;
+  uint16_t* q_scale_out;
+  int8_t* k_cache;
+  uint16_t* k_scale_cache;
+  const int64_t* slot;
+  int64_t cache_rows;
+  float* w_out;
+} dsa_prolog_args;
+
+size_t dsa_indexer_prolog_workspace(const dsa_prolog_args* args);
+int dsa_indexer_prolog(const dsa_prolog_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Lightning Indexer + top-k  [V3.2-PyPTO §Lightning Indexer: the int8 q
+ * scored against the C8 key cache, then a per-query TopK; V4-TileLang
+ * §Sparse Flash Attention step 2 for the -1 marker of unused slots]
+ *
+ *   I[t,s] = ks[s] * sum_h (w[t,h] * qs[t,h]) * ReLU(sum_d q[t,h,d] K[s,d])
+ *
+ * for keys 0 <= s <= pos[t] of token t's sequence; topk_idx[t] receives the
+ * positions of the `topk` largest I[t,.] (as a set, in no particular order),
+ * followed by -1 when fewer than `topk` keys are visible.  Equal scores at
+ * the boundary are broken arbitrarily.
+ *
+ * Token layout: T = B * n_q; token t belongs to sequence t / n_q.
+ * Shapes: q int8 [T, H_I, d_I]; q_scale fp16 [T, H_I]; w fp32 [T, H_I];
+ * pos int32 [T] with 0 <= pos[t] < max_L; topk_idx int32 [T, topk];
+ * scores_out fp32 [T, max_L] or NULL (when given it receives I, with -inf
+ * for s > pos[t]; columns past the largest visible key are unspecified).
+ * Key cache, contiguous (block_table == NULL): k_cache int8 [B, max_L, d_I],
+ * k_scale fp16 [B, max_L].  Paged: k_cache int8 [n_rows, d_I], k_scale fp16
+ * [n_rows], key s of sequence b at row block_table[b, s / block_size] *
+ * block_size + s % block_size, block_table int32 [B, max_blocks],
+ * max_L = max_blocks * block_size.
+ * Supported: d_I in {64, 128}; H_I in {4, 8, 16, 32, 64, 128}; topk >= 1;
+ * max_L a multiple of 128; block_size a multiple of 8 that divides 128 or
+ * is a multiple of 128.  Workspace: dsa_indexer_topk_workspace() bytes (the
+ * fp32 score rows live there when scores_out is NULL).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, B, n_q, H_I, d_I, topk, max_L;
+  const int8_t* q;
+  const uint16_t* q_scale;
+  const float* w;
+  const int8_t* k_cache;
+  const uint16_t* k_scale;
+  const int32_t* block_table;
+  int32_t block_size, max_blocks;
+  const int32_t* pos;
+  int32_t* topk_idx;
+  float* scores_out;
+} dsa_topk_args;
+
+size_t dsa_indexer_topk_workspace(const dsa_topk_args* args);
+int dsa_indexer_topk(const dsa_topk_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The two halves of dsa_indexer_topk as separate calls, for pipelines that
+ * keep the score rows.  dsa_indexer_scores writes I into `scores` fp32
+ * [T, max_L] (device; -inf for s > pos[t]; columns past the largest visible
+ * key of a token's group are not written); args->topk_idx and
+ * args->scores_out are ignored.  dsa_topk_from_scores selects, per token,
+ * the args->topk largest of scores[t, 0..pos[t]] (rows `ld` floats apart,
+ * ld >= max_L) into args->topk_idx, with the same output rules as above. */
+int dsa_indexer_scores(const dsa_topk_args* args, float* scores, void* stream);
+int dsa_topk_from_scores(const dsa_topk_args* args, const float* scores, int64_t ld, void* stream);
+
+/* Exact int32 dot products dots[t, h, s] = sum_d q[t,h,d] K[b(t),s,d] for
+ * s in [0, max_L), for checking the integer contraction bit by bit (test
+ * use; a plain SIMT kernel, not the production path).  dots int32
+ * [T, H_I, max_L]. */
+int dsa_indexer_dots_debug(const dsa_topk_args* args, int32_t* dots, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse MLA attention  [V4-TileLang §Sparse Flash Attention steps 1-6 and
+ * 8; V3.2-PyPTO §Deepseek Indexer Attention: the TopK rows are gathered
+ * from the latent cache straight into on-chip memory]
+ *
+ *   out[t,h,:] = sum_j softmax_j(scale * q[t,h,:] . KV[r_j, :]) KV[r_j, :d_v]
+ *
+ * over the rows r_j of token t's sequence named by topk_idx[t, j] >= 0
+ * (logical positions; -1 selects nothing).  lse[t,h] = natural log of
+ * sum_j exp(scale * q . k_j); a token with no selected row gets out = 0 and
+ * lse = -inf.  The attention sink (step 7) is not applied.
+ *
+ * Token layout: T = B * n_q, token t in sequence t / n_q.
+ * Shapes: q bf16 [T, H, d_qk]; kv bf16 contiguous [B, max_L, d_qk] or paged
+ * [n_rows, d_qk] through block_table int32 [B, max_blocks] as above;
+ * topk_idx int32 [T, topk] with entries in [-1, max_L); out bf16
+ * [T, H, d_v]; lse fp32 [T, H] or NULL.
+ * Supported: d_qk = 576, d_v = 512, 1 <= H <= 128, 1 <= topk <= 65536.
+ * Workspace: dsa_sparse_attn_workspace() bytes.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, B, n_q, H, d_qk, d_v, topk, max_L;
+  float scale;
+  const uint16_t* q;
+  const uint16_t* kv;
+  const int32_t* block_table;
+  int32_t block_size, max_blocks;
+  const int32_t* topk_idx;
+  uint16_t* out;
+  float* lse;
+} dsa_attn_args;
+
+size_t dsa_sparse_attn_workspace(const dsa_attn_args* args);
+int dsa_sparse_attn(const dsa_attn_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

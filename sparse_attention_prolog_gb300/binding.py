@@ -1,0 +1,199 @@
+"""ctypes binding of libdsa.so: argument marshalling only.
+
+Each wrapper takes torch CUDA tensors, fills the C argument struct with their
+device pointers and calls the entry point of the same name; every step of
+the computation runs in the library's kernels.  Loading fails loudly when the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsa.so")
+
+c_int = ctypes.c_int32
+c_ptr = ctypes.c_void_p
+
+
+class PrologArgs(ctypes.Structure):
+    _fields_ = [
+        ("T", c_int), ("H_I", c_int), ("d_I", c_int), ("d_rope", c_int), ("K_q", c_int), ("D_x", c_int),
+        ("q_lora", c_ptr), ("q_lora_scale", c_ptr), ("w_qb", c_ptr), ("w_qb_scale", c_ptr),
+        ("x", c_ptr), ("w_k", c_ptr), ("ln_gamma", c_ptr), ("ln_beta", c_ptr), ("ln_eps", ctypes.c_float),
+        ("w_proj", c_ptr), ("w_scale", ctypes.c_float), ("pos", c_ptr), ("rope_cos", c_ptr), ("rope_sin", c_ptr),
+        ("rope_max_pos", c_int), ("rope_interleaved", c_int), ("q_out", c_ptr), ("q_scale_out", c_ptr),
+        ("k_cache", c_ptr), ("k_scale_cache", c_ptr), ("slot", c_ptr), ("cache_rows", ctypes.c_int64),
+        ("w_out", c_ptr),
+    ]
+
+
+class TopkArgs(ctypes.Structure):
+    _fields_ = [
+        ("T", c_int), ("B", c_int), ("n_q", c_int), ("H_I", c_int), ("d_I", c_int), ("topk", c_int), ("max_L", c_int),
+        ("q", c_ptr), ("q_scale", c_ptr), ("w", c_ptr), ("k_cache", c_ptr), ("k_scale", c_ptr),
+        ("block_table", c_ptr), ("block_size", c_int), ("max_blocks", c_int), ("pos", c_ptr),
+        ("topk_idx", c_ptr), ("scores_out", c_ptr),
+    ]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("T", c_int), ("B", c_int), ("n_q", c_int), ("H", c_int), ("d_qk", c_int), ("d_v", c_int), ("topk", c_int),
+        ("max_L", c_int), ("scale", ctypes.c_float), ("q", c_ptr), ("kv", c_ptr), ("block_table", c_ptr),
+        ("block_size", c_int), ("max_blocks", c_int), ("topk_idx", c_ptr), ("out", c_ptr), ("lse", c_ptr),
+    ]
+
+
+EXPORTS = [
+    "dsa_status_string", "dsa_abi_version", "dsa_get_device_error",
+    "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
+    "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
+    "dsa_indexer_scores", "dsa_topk_from_scores",
+    "dsa_sparse_attn_workspace", "dsa_sparse_attn",
+]
+
+_lib = None
+
+
+class DSAError(RuntimeError):
+    pass
+
+
+def load(path: str = LIB_PATH):
+    """Loads libdsa.so once; raises if it is missing (no fallback path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise DSAError(f"{path} is missing: build it with sparse_attention_prolog_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_status_string.argtypes = [c_int]
+    lib.dsa_abi_version.restype = c_int
+    lib.dsa_get_device_error.argtypes = [c_ptr]
+    lib.dsa_get_device_error.restype = c_int
+    for name, st in (("prolog", PrologArgs), ("topk", TopkArgs), ("attn", AttnArgs)):
+        ws = {"prolog": "dsa_indexer_prolog_workspace", "topk": "dsa_indexer_topk_workspace",
+              "attn": "dsa_sparse_attn_workspace"}[name]
+        run = {"prolog": "dsa_indexer_prolog", "topk": "dsa_indexer_topk", "attn": "dsa_sparse_attn"}[name]
+        getattr(lib, ws).argtypes = [ctypes.POINTER(st)]
+        getattr(lib, ws).restype = ctypes.c_size_t
+        getattr(lib, run).argtypes = [ctypes.POINTER(st), c_ptr, ctypes.c_size_t, c_ptr]
+        getattr(lib, run).restype = c_int
+    lib.dsa_indexer_dots_debug.argtypes = [ctypes.POINTER(TopkArgs), c_ptr, c_ptr]
+    lib.dsa_indexer_dots_debug.restype = c_int
+    lib.dsa_indexer_scores.argtypes = [ctypes.POINTER(TopkArgs), c_ptr, c_ptr]
+    lib.dsa_indexer_scores.restype = c_int
+    lib.dsa_topk_from_scores.argtypes = [ctypes.POINTER(TopkArgs), c_ptr, ctypes.c_int64, c_ptr]
+    lib.dsa_topk_from_scores.restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().dsa_status_string(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise DSAError(f"{what}: {status_string(code)} ({code})")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ws(nbytes: int, device, ws: Optional[torch.Tensor]):
+    if nbytes == 0:
+        return None, 0
+    if ws is not None:
+        assert ws.numel() * ws.element_size() >= nbytes
+        return ws, ws.numel() * ws.element_size()
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+# ---------------------------------------------------------------- prolog
+def prolog_args(T, H_I, d_I, d_rope, q_lora, q_lora_scale, w_qb, w_qb_scale, x, w_k, ln_gamma, ln_beta,
+                ln_eps, w_proj, w_scale, pos, rope_cos, rope_sin, rope_interleaved, q_out, q_scale_out,
+                k_cache, k_scale_cache, slot, w_out) -> PrologArgs:
+    return PrologArgs(
+        T, H_I, d_I, d_rope, q_lora.shape[1] if T else 0, x.shape[1] if T else 0,
+        _p(q_lora), _p(q_lora_scale), _p(w_qb), _p(w_qb_scale), _p(x), _p(w_k), _p(ln_gamma), _p(ln_beta),
+        float(ln_eps), _p(w_proj), float(w_scale), _p(pos), _p(rope_cos), _p(rope_sin), rope_cos.shape[0],
+        int(rope_interleaved), _p(q_out), _p(q_scale_out), _p(k_cache), _p(k_scale_cache), _p(slot),
+        k_cache.shape[0], _p(w_out))
+
+
+def dsa_indexer_prolog(args: PrologArgs, workspace: Optional[torch.Tensor] = None, stream=None,
+                       device=None):
+    lib = load()
+    need = lib.dsa_indexer_prolog_workspace(ctypes.byref(args))
+    ws, n = _ws(need, device or "cuda", workspace)
+    _check(lib.dsa_indexer_prolog(ctypes.byref(args), _p(ws), n, _stream(stream)), "dsa_indexer_prolog")
+    return ws
+
+
+# ----------------------------------------------------------------- top-k
+def topk_args(T, B, n_q, H_I, d_I, topk, max_L, q, q_scale, w, k_cache, k_scale, pos, topk_idx,
+              block_table=None, block_size=0, scores_out=None) -> TopkArgs:
+    max_blocks = 0 if block_table is None else block_table.shape[1]
+    return TopkArgs(T, B, n_q, H_I, d_I, topk, max_L, _p(q), _p(q_scale), _p(w), _p(k_cache), _p(k_scale),
+                    _p(block_table), block_size, max_blocks, _p(pos), _p(topk_idx), _p(scores_out))
+
+
+def dsa_indexer_topk(args: TopkArgs, workspace: Optional[torch.Tensor] = None, stream=None, device=None):
+    lib = load()
+    need = lib.dsa_indexer_topk_workspace(ctypes.byref(args))
+    ws, n = _ws(need, device or "cuda", workspace)
+    _check(lib.dsa_indexer_topk(ctypes.byref(args), _p(ws), n, _stream(stream)), "dsa_indexer_topk")
+    return ws
+
+
+def dsa_indexer_dots_debug(args: TopkArgs, dots: torch.Tensor, stream=None):
+    _check(load().dsa_indexer_dots_debug(ctypes.byref(args), _p(dots), _stream(stream)), "dsa_indexer_dots_debug")
+
+
+def dsa_indexer_scores(args: TopkArgs, scores: torch.Tensor, stream=None):
+    _check(load().dsa_indexer_scores(ctypes.byref(args), _p(scores), _stream(stream)), "dsa_indexer_scores")
+
+
+def dsa_topk_from_scores(args: TopkArgs, scores: torch.Tensor, stream=None):
+    _check(load().dsa_topk_from_scores(ctypes.byref(args), _p(scores), scores.stride(0), _stream(stream)),
+           "dsa_topk_from_scores")
+
+
+# -------------------------------------------------------------- attention
+def attn_args(T, B, n_q, H, topk, max_L, scale, q, kv, topk_idx, out, lse=None, block_table=None,
+              block_size=0, d_qk=576, d_v=512) -> AttnArgs:
+    max_blocks = 0 if block_table is None else block_table.shape[1]
+    return AttnArgs(T, B, n_q, H, d_qk, d_v, topk, max_L, float(scale), _p(q), _p(kv), _p(block_table),
+                    block_size, max_blocks, _p(topk_idx), _p(out), _p(lse))
+
+
+def dsa_sparse_attn(args: AttnArgs, workspace: Optional[torch.Tensor] = None, stream=None, device=None):
+    lib = load()
+    need = lib.dsa_sparse_attn_workspace(ctypes.byref(args))
+    ws, n = _ws(need, device or "cuda", workspace)
+    _check(lib.dsa_sparse_attn(ctypes.byref(args), _p(ws), n, _stream(stream)), "dsa_sparse_attn")
+    return ws
+
+
+def workspace_bytes(kind: str, args) -> int:
+    lib = load()
+    fn = {"prolog": lib.dsa_indexer_prolog_workspace, "topk": lib.dsa_indexer_topk_workspace,
+          "attn": lib.dsa_sparse_attn_workspace}[kind]
+    return int(fn(ctypes.byref(args)))
+
+
+def device_error(stream=None) -> int:
+    return int(load().dsa_get_device_error(_stream(stream)))

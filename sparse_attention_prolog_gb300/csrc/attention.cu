@@ -1,0 +1,572 @@
+// Sparse MLA flash attention over the top-k latent rows, on tcgen05.
+//
+// [V4-TileLang §Sparse Flash Attention] steps: (1) parallel over (b, m);
+// (2) idx = topk_idxs[...] or -1 past topk, gather the kv rows and build the
+// mask; (3) S = q . k^T, mask, scale; (4) online softmax with running max
+// and sum; (5) P . V; (6) accumulate and rescale; (8) write back.
+// [V3.2-PyPTO §Deepseek Indexer Attention] found the discrete gather to be
+// over 70% of the fused operator and fixed it by gathering straight into the
+// matrix unit's buffer.  On sm_103a the same idea is a cp.async row gather
+// straight into the 128B-swizzled layout tcgen05 reads.
+//
+// One 2-CTA cluster per (token, head block of 128, chunk of R selected rows):
+//
+//   CTA 0  (QK + softmax): q [128 x 576] bf16 lives in TMEM (288 columns)
+//          and is the A operand of S = q . K^T (M=128 heads, N=64 rows,
+//          K=576); S is double-buffered in TMEM.  Four softmax warps (one
+//          thread per head) apply the mask and scale, keep the running max
+//          (rescaling only when it grows by more than 2^8) and the row sum,
+//          and store P (bf16) and the per-row rescale factor straight into
+//          CTA 1's shared memory with st.async.
+//   CTA 1  (PV): O [128 x 512] fp32 fills its whole TMEM; P (shared memory,
+//          K-major) times V (the first 512 dims of the gathered rows, read
+//          MN-major from the same swizzled layout) accumulates into O.
+//          Correction warps rescale O rows in the rare case the max grew,
+//          and finally normalise O and write it (or a split-K partial).
+//
+// Both CTAs gather the same rows (the second read is an L2 hit).  Chunks of
+// one token are merged by attn_combine_kernel with their log-sum-exp.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include "dsa_internal.h"
+#include "dsa_ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kDqk = 576, kDv = 512;
+constexpr int kRows = 64;                       // rows per tile
+constexpr int kAtomsK = kDqk / 64;              // 9 swizzle atoms per full row
+constexpr int kAtomsV = kDv / 64;               // 8
+constexpr int kStageK = kAtomsK * kRows * 128;  // 73,728 B
+constexpr int kStageV = kAtomsV * kRows * 128;  // 65,536 B
+constexpr int kStagesK = 3, kStagesV = 2;
+constexpr int kPSlot = 128 * 128;               // P tile [128 heads x 64 rows] bf16
+constexpr int kThreads = 320;
+constexpr uint32_t kPBytes = 128 * (8 * 16 + 4);  // P row + alpha, per tile
+constexpr uint32_t kFinalBytes = 128 * 8;
+constexpr uint32_t kTmemQ = 0, kTmemS = 288;    // CTA 0 column map
+
+struct AttnParams {
+  int T, n_q, H, topk, max_L, n_chunks, chunk_rows, head_blocks;
+  float scale_log2;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kv;
+  const int32_t* block_table;
+  int block_size, max_blocks;
+  const int32_t* idx;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;   // [T][n_chunks][H][512] when n_chunks > 1
+  float2* part_ml; // [T][n_chunks][H]: (max, sum) in log2 units
+  uint32_t* err;
+};
+
+struct __align__(8) Bars {
+  uint64_t kfull[kStagesK], kempty[kStagesK];   // CTA 0 gather ring
+  uint64_t sfull[2], sempty[2];                 // CTA 0 S buffers
+  uint64_t pfree[2];                            // CTA 0: P slot of CTA 1 free
+  uint64_t vfull[kStagesV], vempty[kStagesV];   // CTA 1 gather ring
+  uint64_t pfull[2], pcons[2];                  // CTA 1 P slots
+  uint64_t ready[2], odone, ffull;              // CTA 1 correction / MMA
+};
+
+__device__ __forceinline__ int64_t kv_row(const AttnParams& P, int b, int s) {
+  if (P.block_table == nullptr) return static_cast<int64_t>(b) * P.max_L + s;
+  const int blk = __ldg(P.block_table + static_cast<size_t>(b) * P.max_blocks + s / P.block_size);
+  return blk < 0 ? -1 : static_cast<int64_t>(blk) * P.block_size + s % P.block_size;
+}
+
+// Gathers the rows of tile `j` into a swizzled stage: `atoms` 64-dim atoms
+// of every row, zero rows for masked slots.  128 threads, cp.async.
+__device__ __forceinline__ void gather_tile(const AttnParams& P, const int32_t* idx_row, int b, int slot0,
+                                            uint8_t* stage, int atoms, int ct) {
+  const int chunks = atoms * 8;
+  for (int task = ct; task < kRows * chunks; task += 128) {
+    const int r = task / chunks, c = task % chunks;
+    const int slot = slot0 + r;
+    const int s = (slot < P.topk) ? __ldg(idx_row + slot) : -1;
+    const __nv_bfloat16* src = P.kv;
+    uint32_t bytes = 0;
+    if (s >= 0 && s < P.max_L) {
+      const int64_t row = kv_row(P, b, s);
+      if (row >= 0) {
+        src = P.kv + row * kDqk + c * 8;
+        bytes = 16;
+      }
+    }
+    cp_async16(smem_u32(stage + (c / 8) * (kRows * 128) + sw128_off(r, c % 8)), src, bytes);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Bars bars;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int chunk = blockIdx.x >> 1, hb = blockIdx.y, t = blockIdx.z;
+  const int b = t / P.n_q;
+  const int slot_begin = chunk * P.chunk_rows;
+  const int rows_here = max(0, min(P.chunk_rows, P.topk - slot_begin));
+  const int n_tiles = (rows_here + kRows - 1) / kRows;
+  const int32_t* idx_row = P.idx + static_cast<size_t>(t) * P.topk;
+
+  // CTA 1 layout: V stages, then P slots, alpha, final (m, l)
+  uint8_t* sV = smem;
+  uint8_t* sP = smem + kStagesV * kStageV;
+  float* sAlpha = reinterpret_cast<float*>(sP + 2 * kPSlot);  // [2][128]
+  float2* sFinal = reinterpret_cast<float2*>(sAlpha + 256);     // [128]
+  uint8_t* sK = smem;                                           // CTA 0: K stages
+
+  if (tid == 0) {
+    for (int i = 0; i < kStagesK; ++i) { mbar_init(&bars.kfull[i], 4); mbar_init(&bars.kempty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.sfull[i], 1); mbar_init(&bars.sempty[i], 4); mbar_init(&bars.pfree[i], 1);
+      mbar_init(&bars.pfull[i], 1); mbar_init(&bars.pcons[i], 1); mbar_init(&bars.ready[i], 4);
+    }
+    for (int i = 0; i < kStagesV; ++i) { mbar_init(&bars.vfull[i], 4); mbar_init(&bars.vempty[i], 1); }
+    mbar_init(&bars.odone, 1);
+    mbar_init(&bars.ffull, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    if (rank == 1) {
+      mbar_arrive_expect_tx(&bars.pfull[0], kPBytes);
+      mbar_arrive_expect_tx(&bars.pfull[1], kPBytes);
+      mbar_arrive_expect_tx(&bars.ffull, kFinalBytes);
+    }
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  volatile int* abort_v = &abort_flag;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+
+  if (rank == 0 && warp < 4) {
+    // q row of this thread's head into TMEM columns [0, 288).
+    const int h = hb * 128 + warp * 32 + lane;
+    const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (static_cast<size_t>(t) * P.H + h) * kDqk);
+    for (int a = 0; a < kAtomsK; ++a) {
+      uint32_t r[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (h < P.H) v = __ldg(qrow + a * 8 + c);
+        r[4 * c] = v.x; r[4 * c + 1] = v.y; r[4 * c + 2] = v.z; r[4 * c + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_off + kTmemQ + a * 32, r);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote use
+  griddep_launch_dependents();
+  griddep_wait();  // topk_idx comes from the previous kernel
+
+  if (rank == 0) {
+    if (warp >= 4 && warp < 8) {
+      // ------------------------------------------------ gather K (CTA 0)
+      const int ct = tid - 128;
+      int st = 0, prev = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait(&bars.kempty[st], ph ^ 1, P.err, abort_v)) break;
+        gather_tile(P, idx_row, b, slot_begin + j * kRows, sK + st * kStageK, kAtomsK, ct);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        // keep two tiles in flight: publish the previous one
+        if (j > 0) {
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.kfull[prev]);
+        }
+        prev = st;
+        if (++st == kStagesK) { st = 0; ph ^= 1; }
+      }
+      if (n_tiles > 0 && !*abort_v) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.kfull[prev]);
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 8) {
+      // ---------------------------------------------- QK^T MMA (CTA 0)
+      if (lane == 0) {
+        const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
+        int st = 0, sb = 0;
+        uint32_t ph = 0, phs = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+          if (!mbar_wait(&bars.kfull[st], ph, P.err, abort_v)) break;
+          if (!mbar_wait(&bars.sempty[sb], phs ^ 1, P.err, abort_v)) break;
+          tc_fence_after();
+          const uint32_t base = smem_u32(sK + st * kStageK);
+          for (int kk = 0; kk < kDqk / 16; ++kk) {
+            const uint64_t bd = smem_desc(base + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
+            mma_ts(tmem + kTmemS + sb * kRows, tmem + kTmemQ + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars.kempty[st]);
+          mma_commit(&bars.sfull[sb]);
+          if (++st == kStagesK) { st = 0; ph ^= 1; }
+          if (++sb == 2) { sb = 0; phs ^= 1; }
+        }
+      }
+    } else if (warp < 4) {
+      // ------------------------------------------------- softmax (CTA 0)
+      const int hrow = warp * 32 + lane;
+      const uint32_t remote_p = mapa(smem_u32(sP), 1);
+      const uint32_t remote_alpha = mapa(smem_u32(sAlpha), 1);
+      const uint32_t remote_final = mapa(smem_u32(sFinal), 1);
+      const uint32_t remote_pfull[2] = {mapa(smem_u32(&bars.pfull[0]), 1), mapa(smem_u32(&bars.pfull[1]), 1)};
+      const uint32_t remote_ffull = mapa(smem_u32(&bars.ffull), 1);
+      const float ninf = -__int_as_float(0x7f800000);
+      float m_used = ninf, l_sum = 0.f;
+      int sb = 0;
+      uint32_t phs = 0;
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int slot0 = slot_begin + j * kRows;
+        const int s_lo = (slot0 + lane < P.topk) ? __ldg(idx_row + slot0 + lane) : -1;
+        const int s_hi = (slot0 + 32 + lane < P.topk) ? __ldg(idx_row + slot0 + 32 + lane) : -1;
+        const uint32_t v_lo = __ballot_sync(0xffffffffu, s_lo >= 0 && s_lo < P.max_L);
+        const uint32_t v_hi = __ballot_sync(0xffffffffu, s_hi >= 0 && s_hi < P.max_L);
+        if (!mbar_wait(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tmem + lane_off + kTmemS + sb * kRows, s0);
+        tmem_ld32(tmem + lane_off + kTmemS + sb * kRows + 32, s1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.sempty[sb]);
+        float x[64];
+        float mt = ninf;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          x[k] = ((v_lo >> k) & 1u) ? __uint_as_float(s0[k]) * P.scale_log2 : ninf;
+          x[32 + k] = ((v_hi >> k) & 1u) ? __uint_as_float(s1[k]) * P.scale_log2 : ninf;
+          mt = fmaxf(mt, fmaxf(x[k], x[32 + k]));
+        }
+        float alpha = 1.f;
+        if (mt > m_used + 8.f) {  // also taken when m_used is -inf
+          alpha = ex2_approx(m_used - mt);
+          l_sum *= alpha;
+          m_used = mt;
+        }
+        uint32_t pk[32];
+        float lt = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = (x[2 * k] == ninf) ? 0.f : ex2_approx(x[2 * k] - m_used);
+          const float p1 = (x[2 * k + 1] == ninf) ? 0.f : ex2_approx(x[2 * k + 1] - m_used);
+          lt += p0 + p1;
+          __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          pk[k] = *reinterpret_cast<uint32_t*>(&pb);
+        }
+        l_sum += lt;
+        const int ps = j & 1;
+        if (!mbar_wait_cluster(&bars.pfree[ps], ((j >> 1) & 1) ^ 1, P.err, abort_v)) { ok = false; break; }
+        const uint32_t prow = remote_p + ps * kPSlot;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(prow + sw128_off(hrow, c), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]),
+                      remote_pfull[ps]);
+        st_async_b32(remote_alpha + (ps * 128 + hrow) * 4, __float_as_uint(alpha), remote_pfull[ps]);
+        if (++sb == 2) { sb = 0; phs ^= 1; }
+      }
+      st_async_v2(remote_final + hrow * 8, __float_as_uint(m_used), __float_as_uint(l_sum), remote_ffull);
+    }
+  } else {
+    if (warp >= 4 && warp < 8) {
+      // ------------------------------------------------ gather V (CTA 1)
+      const int ct = tid - 128;
+      int st = 0, prev = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait(&bars.vempty[st], ph ^ 1, P.err, abort_v)) break;
+        gather_tile(P, idx_row, b, slot_begin + j * kRows, sV + st * kStageV, kAtomsV, ct);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        // keep two tiles in flight: publish the previous one
+        if (j > 0) {
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.vfull[prev]);
+        }
+        prev = st;
+        if (++st == kStagesV) { st = 0; ph ^= 1; }
+      }
+      if (n_tiles > 0 && !*abort_v) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.vfull[prev]);
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 8) {
+      // ------------------------------------------------- PV MMA (CTA 1)
+      if (lane == 0) {
+        const uint32_t idesc = idesc_f16(128, 256, kFmtBF16, 0, 1);
+        int st = 0;
+        uint32_t ph = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+          const int ps = j & 1;
+          if (!mbar_wait(&bars.vfull[st], ph, P.err, abort_v)) break;
+          if (!mbar_wait(&bars.ready[ps], (j >> 1) & 1, P.err, abort_v)) break;
+          tc_fence_after();
+          const uint32_t pbase = smem_u32(sP + ps * kPSlot);
+          const uint32_t vbase = smem_u32(sV + st * kStageV);
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            const uint64_t ad = smem_desc(pbase + kk * 32, 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+              const uint64_t bd = smem_desc(vbase + nh * 4 * (kRows * 128) + kk * 16 * 128, kRows * 128, 1024,
+                                            kSwizzle128B);
+              mma_ss(tmem + nh * 256, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&bars.vempty[st]);
+          mma_commit(&bars.pcons[ps]);
+          mma_commit(&bars.odone);
+          if (++st == kStagesV) { st = 0; ph ^= 1; }
+        }
+      }
+    } else if (warp == 9) {
+      // ----------------------------------- relay: P slot consumed -> CTA 0
+      if (lane == 0) {
+        const uint32_t remote_pfree[2] = {mapa(smem_u32(&bars.pfree[0]), 0), mapa(smem_u32(&bars.pfree[1]), 0)};
+        for (int j = 0; j + 2 < n_tiles; ++j) {
+          const int ps = j & 1;
+          if (!mbar_wait(&bars.pcons[ps], (j >> 1) & 1, P.err, abort_v)) break;
+          mbar_arrive_expect_tx(&bars.pfull[ps], kPBytes);  // arm the slot's next use
+          mbar_arrive_remote(remote_pfree[ps]);
+        }
+      }
+    } else if (warp < 4) {
+      // --------------------------------- correction + epilogue (CTA 1)
+      const int hrow = warp * 32 + lane;
+      int consumed = 0;  // odone phases observed
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int ps = j & 1;
+        if (!mbar_wait_cluster(&bars.pfull[ps], (j >> 1) & 1, P.err, abort_v)) { ok = false; break; }
+        const float alpha = sAlpha[ps * 128 + hrow];
+        const bool need = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
+        if (need) {
+          // O must hold PV of tile j-1 before it is rescaled.
+          while (consumed < j) {
+            if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
+            ++consumed;
+          }
+          if (!ok) break;
+          tc_fence_after();
+          for (int c0 = 0; c0 < kDv; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st32(tmem + lane_off + c0, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+        }
+        fence_proxy_async_smem();  // P arrived through st.async; the MMA reads it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.ready[ps]);
+        // keep at most one PV completion unobserved
+        while (consumed < j) {
+          if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
+          ++consumed;
+        }
+      }
+      while (ok && consumed < n_tiles) {
+        if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
+        ++consumed;
+      }
+      if (ok) ok = mbar_wait_cluster(&bars.ffull, 0, P.err, abort_v);
+      tc_fence_after();
+      const float2 ml = sFinal[hrow];
+      const int h = hb * 128 + hrow;
+      const bool empty = (n_tiles == 0) || !(ml.y > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / ml.y;
+      if (P.n_chunks == 1) {
+        __nv_bfloat16* orow = P.out + (static_cast<size_t>(t) * P.H + h) * kDv;
+        for (int c0 = 0; c0 < kDv; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + c0, v);
+          tmem_ld_wait();
+          if (h < P.H) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float a = empty ? 0.f : __uint_as_float(v[2 * k]) * inv_l;
+              const float bb = empty ? 0.f : __uint_as_float(v[2 * k + 1]) * inv_l;
+              __nv_bfloat162 pb = __floats2bfloat162_rn(a, bb);
+              pk[k] = *reinterpret_cast<uint32_t*>(&pb);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
+        }
+        if (h < P.H && P.lse != nullptr)
+          P.lse[static_cast<size_t>(t) * P.H + h] =
+              empty ? -__int_as_float(0x7f800000) : (ml.x + log2f(ml.y)) * 0.69314718055994531f;
+      } else {
+        float* orow = P.part_o + ((static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h) * kDv;
+        for (int c0 = 0; c0 < kDv; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + c0, v);
+          tmem_ld_wait();
+          if (h < P.H) {
+            float4* dst = reinterpret_cast<float4*>(orow + c0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = empty ? make_float4(0.f, 0.f, 0.f, 0.f)
+                             : make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
+                                           __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
+          }
+        }
+        if (h < P.H)
+          P.part_ml[(static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h] =
+              empty ? make_float2(-__int_as_float(0x7f800000), 0.f) : make_float2(ml.x, ml.y);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still address it
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Merges the split chunks of every (token, head): out = sum_c w_c O_c /
+// sum_c w_c with w_c = l_c 2^(m_c - M) (O_c already divided by l_c).
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int th = blockIdx.x * 8 + warp;  // (token, head)
+  if (th >= P.T * P.H) return;
+  const int t = th / P.H, h = th % P.H;
+  float M = -__int_as_float(0x7f800000);
+  for (int c = 0; c < P.n_chunks; ++c) {
+    const float2 ml = P.part_ml[(static_cast<size_t>(t) * P.n_chunks + c) * P.H + h];
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float wsum = 0.f;
+  for (int c = 0; c < P.n_chunks; ++c) {
+    const float2 ml = P.part_ml[(static_cast<size_t>(t) * P.n_chunks + c) * P.H + h];
+    if (!(ml.y > 0.f)) continue;
+    const float wc = ml.y * exp2f(ml.x - M);
+    wsum += wc;
+    const float4* src = reinterpret_cast<const float4*>(
+        P.part_o + ((static_cast<size_t>(t) * P.n_chunks + c) * P.H + h) * kDv);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = __ldcg(src + lane + 32 * k);
+      acc[4 * k] = fmaf(wc, v.x, acc[4 * k]);
+      acc[4 * k + 1] = fmaf(wc, v.y, acc[4 * k + 1]);
+      acc[4 * k + 2] = fmaf(wc, v.z, acc[4 * k + 2]);
+      acc[4 * k + 3] = fmaf(wc, v.w, acc[4 * k + 3]);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* orow = P.out + (static_cast<size_t>(t) * P.H + h) * kDv;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * k] * inv, acc[4 * k + 1] * inv);
+    __nv_bfloat162 c2 = __floats2bfloat162_rn(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
+    uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&c2));
+    *reinterpret_cast<uint2*>(orow + 4 * (lane + 32 * k)) = pk;
+  }
+  if (lane == 0 && P.lse != nullptr)
+    P.lse[static_cast<size_t>(t) * P.H + h] =
+        wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+}
+
+void plan(const dsa_attn_args& a, int& head_blocks, int& n_chunks, int& chunk_rows) {
+  head_blocks = (a.H + 127) / 128;
+  const int tiles = (a.topk + kRows - 1) / kRows;
+  const long long pairs_per_chunk = static_cast<long long>(a.T) * head_blocks;
+  long long target = sm_count() / (2 * pairs_per_chunk);
+  if (target < 1) target = 1;
+  const int tiles_per_chunk = static_cast<int>((tiles + target - 1) / target);
+  chunk_rows = tiles_per_chunk * kRows;
+  n_chunks = (tiles + tiles_per_chunk - 1) / tiles_per_chunk;
+}
+
+}  // namespace
+
+size_t attn_workspace(const dsa_attn_args& a) {
+  int hb, nc, cr;
+  plan(a, hb, nc, cr);
+  if (nc == 1) return 0;
+  const size_t o = static_cast<size_t>(a.T) * nc * a.H * kDv * sizeof(float);
+  const size_t ml = static_cast<size_t>(a.T) * nc * a.H * sizeof(float2);
+  return round_up(o, 256) + round_up(ml, 256);
+}
+
+int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
+  AttnParams P{};
+  plan(a, P.head_blocks, P.n_chunks, P.chunk_rows);
+  P.T = a.T; P.n_q = a.n_q; P.H = a.H; P.topk = a.topk; P.max_L = a.max_L;
+  P.scale_log2 = a.scale * 1.4426950408889634f;
+  P.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  P.kv = reinterpret_cast<const __nv_bfloat16*>(a.kv);
+  P.block_table = a.block_table; P.block_size = a.block_size; P.max_blocks = a.max_blocks;
+  P.idx = a.topk_idx;
+  P.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  P.lse = a.lse;
+  if (P.n_chunks > 1) {
+    P.part_o = static_cast<float*>(ws);
+    P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +
+                                          round_up(static_cast<size_t>(a.T) * P.n_chunks * a.H * kDv * 4, 256));
+  }
+  P.err = error_word();
+  if (!P.err) return DSA_ERR_CUDA;
+
+  const size_t smem = 1024 + (kStagesK * kStageK > kStagesV * kStageV + 2 * kPSlot + 2048
+                                  ? static_cast<size_t>(kStagesK) * kStageK
+                                  : static_cast<size_t>(kStagesV) * kStageV + 2 * kPSlot + 2048);
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(P.n_chunks * 2, P.head_blocks, a.T);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, P);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (P.n_chunks > 1) {
+    cudaLaunchConfig_t c2 = {};
+    c2.gridDim = dim3((a.T * a.H + 7) / 8);
+    c2.blockDim = dim3(256);
+    c2.dynamicSmemBytes = 0;
+    c2.stream = s;
+    c2.attrs = &attr[1];
+    c2.numAttrs = 1;
+    e = cudaLaunchKernelEx(&c2, attn_combine_kernel, P);
+  }
+  return cuda_status(e);
+}
+
+}  // namespace dsa

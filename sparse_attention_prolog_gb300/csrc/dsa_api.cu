@@ -1,0 +1,216 @@
+// The C ABI: argument validation, workspace sizing, device error word.
+#include <cuda_runtime.h>
+#include <mutex>
+#include "dsa_internal.h"
+
+namespace dsa {
+
+// One word per device; kernels OR error bits into it.
+static __device__ uint32_t g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+}  // namespace
+
+uint32_t* error_word() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 1;
+    g_sms[d] = n;
+  }
+  return g_sms[d];
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+namespace {
+
+bool bad_ptr(const void* p, size_t align) { return p == nullptr || !aligned(p, align); }
+
+int check_prolog(const dsa_prolog_args* a) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  if (a->T < 0 || a->T > 32) return a->T < 0 ? DSA_ERR_INVALID_ARG : DSA_ERR_UNSUPPORTED;
+  if (a->d_I != 64 && a->d_I != 128) return DSA_ERR_UNSUPPORTED;
+  if (a->H_I < 1 || a->H_I > 128) return DSA_ERR_UNSUPPORTED;
+  if (a->d_rope < 0 || a->d_rope > a->d_I || (a->d_rope % 2) != 0 || ((a->d_rope / 2) % (a->d_I / 32)) != 0)
+    return DSA_ERR_UNSUPPORTED;
+  if (a->K_q <= 0 || a->K_q % 64 != 0 || a->K_q > 4096) return DSA_ERR_UNSUPPORTED;
+  if (a->D_x <= 0 || a->D_x % 64 != 0) return DSA_ERR_UNSUPPORTED;
+  if (a->rope_max_pos <= 0 || a->cache_rows < 0 || !(a->ln_eps >= 0.f)) return DSA_ERR_INVALID_ARG;
+  if (a->T == 0) return DSA_OK;
+  const size_t code_align = a->d_I == 128 ? 4 : 2;
+  if (bad_ptr(a->q_lora, 16) || bad_ptr(a->q_lora_scale, 2) || bad_ptr(a->w_qb, 16) ||
+      bad_ptr(a->w_qb_scale, 2) || bad_ptr(a->x, 16) || bad_ptr(a->w_k, 16) || bad_ptr(a->ln_gamma, 4) ||
+      bad_ptr(a->ln_beta, 4) || bad_ptr(a->pos, 4) || bad_ptr(a->rope_cos, 4) || bad_ptr(a->rope_sin, 4) ||
+      bad_ptr(a->q_out, code_align) || bad_ptr(a->q_scale_out, 2) || bad_ptr(a->k_cache, code_align) ||
+      bad_ptr(a->k_scale_cache, 2) || bad_ptr(a->slot, 8))
+    return DSA_ERR_INVALID_ARG;
+  if ((a->w_proj == nullptr) != (a->w_out == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (a->w_proj && (bad_ptr(a->w_proj, 16) || bad_ptr(a->w_out, 4))) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+int check_topk(const dsa_topk_args* a) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  if (a->T < 0 || a->B < 1 || a->n_q < 1 || static_cast<long long>(a->B) * a->n_q != a->T)
+    return a->T == 0 ? DSA_OK : DSA_ERR_INVALID_ARG;
+  if (a->d_I != 64 && a->d_I != 128) return DSA_ERR_UNSUPPORTED;
+  switch (a->H_I) {
+    case 4: case 8: case 16: case 32: case 64: case 128: break;
+    default: return DSA_ERR_UNSUPPORTED;
+  }
+  if (a->topk < 1) return DSA_ERR_INVALID_ARG;
+  if (a->max_L < 128 || a->max_L % 128 != 0) return DSA_ERR_UNSUPPORTED;
+  if (bad_ptr(a->q, 16) || bad_ptr(a->q_scale, 2) || bad_ptr(a->w, 4) || bad_ptr(a->k_cache, 16) ||
+      bad_ptr(a->k_scale, 2) || bad_ptr(a->pos, 4) || bad_ptr(a->topk_idx, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (a->scores_out && !aligned(a->scores_out, 16)) return DSA_ERR_INVALID_ARG;
+  if (a->block_table) {
+    if (!aligned(a->block_table, 4) || a->block_size < 8 || a->block_size % 8 != 0) return DSA_ERR_INVALID_ARG;
+    if (!(128 % a->block_size == 0 || a->block_size % 128 == 0)) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(a->max_blocks) * a->block_size != a->max_L) return DSA_ERR_INVALID_ARG;
+  }
+  return DSA_OK;
+}
+
+int check_attn(const dsa_attn_args* a) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  if (a->T < 0 || a->B < 1 || a->n_q < 1 || static_cast<long long>(a->B) * a->n_q != a->T)
+    return a->T == 0 ? DSA_OK : DSA_ERR_INVALID_ARG;
+  if (a->d_qk != 576 || a->d_v != 512) return DSA_ERR_UNSUPPORTED;
+  if (a->H < 1 || a->topk < 1 || a->topk > 65536 || a->max_L < 1) return DSA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f)) return DSA_ERR_INVALID_ARG;
+  if (bad_ptr(a->q, 16) || bad_ptr(a->kv, 16) || bad_ptr(a->topk_idx, 4) || bad_ptr(a->out, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (a->lse && !aligned(a->lse, 4)) return DSA_ERR_INVALID_ARG;
+  if (a->block_table) {
+    if (!aligned(a->block_table, 4) || a->block_size < 1) return DSA_ERR_INVALID_ARG;
+    if (static_cast<long long>(a->max_blocks) * a->block_size != a->max_L) return DSA_ERR_INVALID_ARG;
+  }
+  return DSA_OK;
+}
+
+size_t topk_scores_bytes(const dsa_topk_args* a) {
+  return a->scores_out ? 0 : round_up(static_cast<size_t>(a->T) * a->max_L * sizeof(float), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case DSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int dsa_abi_version(void) { return 100; }
+
+int dsa_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  uint32_t* p = error_word();
+  if (!p) return DSA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  if (v == 0) return DSA_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DSA_ERR_CUDA;
+  return DSA_ERR_DEVICE_TIMEOUT;
+}
+
+size_t dsa_indexer_prolog_workspace(const dsa_prolog_args* a) {
+  if (check_prolog(a) != DSA_OK) return 0;
+  return prolog_workspace(*a);
+}
+
+int dsa_indexer_prolog(const dsa_prolog_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_prolog(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < prolog_workspace(*a)) return DSA_ERR_WORKSPACE;
+  return launch_prolog(*a, ws, static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_indexer_topk_workspace(const dsa_topk_args* a) {
+  if (check_topk(a) != DSA_OK) return 0;
+  return topk_scores_bytes(a);
+}
+
+int dsa_indexer_topk(const dsa_topk_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_topk(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  const size_t need = topk_scores_bytes(a);
+  if (need > 0 && (ws == nullptr || !aligned(ws, 256) || ws_bytes < need)) return DSA_ERR_WORKSPACE;
+  float* scores = a->scores_out ? a->scores_out : static_cast<float*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int r = launch_indexer(*a, scores, s);
+  if (r != DSA_OK) return r;
+  return launch_topk(*a, scores, a->max_L, s);
+}
+
+int dsa_indexer_scores(const dsa_topk_args* a, float* scores, void* stream) {
+  const int st = check_topk(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  if (bad_ptr(scores, 16)) return DSA_ERR_INVALID_ARG;
+  return launch_indexer(*a, scores, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_topk_from_scores(const dsa_topk_args* a, const float* scores, int64_t ld, void* stream) {
+  const int st = check_topk(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  if (bad_ptr(scores, 4) || ld < a->max_L) return DSA_ERR_INVALID_ARG;
+  return launch_topk(*a, scores, ld, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_indexer_dots_debug(const dsa_topk_args* a, int32_t* dots, void* stream) {
+  const int st = check_topk(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  if (bad_ptr(dots, 4)) return DSA_ERR_INVALID_ARG;
+  return launch_indexer_dots(*a, dots, static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_sparse_attn_workspace(const dsa_attn_args* a) {
+  if (check_attn(a) != DSA_OK || a->T == 0) return 0;
+  return attn_workspace(*a);
+}
+
+int dsa_sparse_attn(const dsa_attn_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_attn(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  const size_t need = attn_workspace(*a);
+  if (need > 0 && (ws == nullptr || !aligned(ws, 256) || ws_bytes < need)) return DSA_ERR_WORKSPACE;
+  return launch_attn(*a, ws, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every
+declared entry point, its ctypes structs match the C layout, and host-side
+argument checks reject bad calls before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import glob
+    from sparse_attention_prolog_gb300 import binding, build
+    srcs = glob.glob(os.path.join(build.CSRC, "*")) + [HEADER]
+    if not os.path.exists(binding.LIB_PATH) or \
+            os.path.getmtime(binding.LIB_PATH) < max(os.path.getmtime(s) for s in srcs):
+        build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dsa.h but not exported"
+    from sparse_attention_prolog_gb300 import binding
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_struct_layout_matches_header(lib, tmp_path):
+    from sparse_attention_prolog_gb300 import binding as B
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dsa.h"', "int main(void) {"]
+    for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
+                      ("dsa_attn_args", B.AttnArgs)):
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = dict(line.split() for line in out if line)
+    for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
+                      ("dsa_attn_args", B.AttnArgs)):
+        assert int(got[cname]) == ctypes.sizeof(py)
+        for f, _ in py._fields_:
+            assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, f"{cname}.{f}"
+
+
+def test_status_strings(lib):
+    from sparse_attention_prolog_gb300 import binding as B
+    assert B.status_string(0) == "ok"
+    assert "workspace" in B.status_string(3)
+    assert lib.dsa_abi_version() == 100
+
+
+def test_host_validation_rejects_before_launch(lib):
+    from sparse_attention_prolog_gb300 import binding as B
+    null = ctypes.c_void_p(0)
+    assert lib.dsa_indexer_prolog(None, null, 0, null) == 1
+    a = B.PrologArgs()
+    a.T, a.H_I, a.d_I, a.d_rope, a.K_q, a.D_x, a.rope_max_pos = 8, 64, 96, 64, 1536, 7168, 10
+    assert lib.dsa_indexer_prolog(ctypes.byref(a), null, 0, null) == 2      # d_I 96 unsupported
+    a.d_I = 128
+    a.T = 33
+    assert lib.dsa_indexer_prolog(ctypes.byref(a), null, 0, null) == 2      # too many tokens
+    a.T = 8
+    assert lib.dsa_indexer_prolog(ctypes.byref(a), null, 0, null) == 1      # null tensors
+    a.T = 0
+    assert lib.dsa_indexer_prolog(ctypes.byref(a), null, 0, null) == 0      # empty: no-op
+    t = B.TopkArgs()
+    t.T, t.B, t.n_q, t.H_I, t.d_I, t.topk, t.max_L = 8, 4, 3, 64, 128, 2048, 65536
+    assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 1        # T != B * n_q
+    t.n_q = 2
+    t.max_L = 1000
+    assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 2        # max_L % 128
+    t.max_L, t.H_I = 65536, 48
+    assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 2        # H_I 48
+    t.H_I = 64
+    assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 1        # null tensors
+    assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) == 0            # invalid -> 0
+    at = B.AttnArgs()
+    at.T, at.B, at.n_q, at.H, at.d_qk, at.d_v, at.topk, at.max_L, at.scale = 8, 4, 2, 128, 512, 512, 2048, 65536, 0.07
+    assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 2        # d_qk 512
+    at.d_qk = 576
+    assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 1        # null tensors
+    at.T = 0
+    assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from sparse_attention_prolog_gb300 import binding as B
+    with pytest.raises(B.DSAError):
+        _fresh_load(B, str(tmp_path / "nope.so"))
+
+
+def _fresh_load(B, path):
+    saved = B._lib
+    B._lib = None
+    try:
+        B.load(path)
+    finally:
+        B._lib = saved

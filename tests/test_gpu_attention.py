@@ -1,0 +1,86 @@
+"""Sparse MLA attention: CUDA path vs oracle (max-abs 2e-2, rel-RMS 5e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_utils import check_attention
+from sparse_attention_prolog_gb300 import binding as B
+from sparse_attention_prolog_gb300 import workloads as W
+from sparse_attention_prolog_gb300.pipeline import DecodeBuffers, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _attn_with_idx(inp, idx_np, tokens=None):
+    buf = DecodeBuffers(inp, DEV, with_attention=True)
+    buf.topk_idx.copy_(torch.from_numpy(idx_np.astype(np.int32)))
+    buf.run_attn()
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    tokens = list(range(inp.T)) if tokens is None else tokens
+    ref_o, ref_l = O.sparse_attention(inp, idx_np, tokens)
+    out = buf.out.float().cpu().numpy()[tokens]
+    lse = buf.lse.cpu().numpy()[tokens]
+    return check_attention(out, ref_o, lse, ref_l, "attn")
+
+
+def _random_idx(rng, inp, frac_invalid=0.0):
+    idx = np.empty((inp.T, inp.topk), np.int64)
+    for t in range(inp.T):
+        n = int(inp.pos[t]) + 1
+        idx[t] = rng.choice(n, size=inp.topk, replace=n < inp.topk)
+        if frac_invalid:
+            idx[t, rng.random(inp.topk) < frac_invalid] = -1
+    return idx
+
+
+def test_tiny_heads_single_chunk(cuda_lib):
+    inp = W.tiny_decode()
+    rng = np.random.default_rng(1)
+    _attn_with_idx(inp, _random_idx(rng, inp))
+
+
+@pytest.mark.parametrize("topk", [64, 200, 1000])
+def test_128_heads_chunks_and_ragged_tiles(topk, cuda_lib):
+    """128 heads, several split chunks, a ragged last tile, masked slots."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[3001, 4096], H_I=4, d_I=64, topk=topk, H=128, seed=21)
+    rng = np.random.default_rng(topk)
+    _attn_with_idx(inp, _random_idx(rng, inp, frac_invalid=0.1))
+
+
+def test_all_masked_and_duplicates(cuda_lib):
+    inp = W.make_decode_inputs(B=1, n_q=4, seq_lens=[600], H_I=4, d_I=64, topk=96, H=128, seed=22)
+    idx = np.full((4, 96), -1, np.int64)          # token 0: nothing selected
+    idx[1, :1] = 5                                 # token 1: one row
+    idx[2] = 7                                     # token 2: one row, 96 times
+    idx[3] = np.random.default_rng(3).integers(0, 597, 96)
+    _attn_with_idx(inp, idx)
+
+
+def test_large_scores_trigger_rescale(cuda_lib):
+    """Scaled-up q and rope dims make later tiles exceed the running max by
+    far more than 2^8, exercising the O rescale path; the value dims keep
+    their N(0,1) scale."""
+    inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[2048], H_I=4, d_I=64, topk=512, H=128, seed=23)
+    q = O.bf16_bits_to_f64(inp.q_attn) * 6.0
+    inp.q_attn = W.f32_to_bf16_bits(q.astype(np.float32))
+    kv = O.bf16_bits_to_f64(inp.kv_cache)
+    kv[1200:, 512:] *= 8.0                      # rows late in the selection dominate
+    inp.kv_cache = W.f32_to_bf16_bits(kv.astype(np.float32))
+    idx = np.tile(np.arange(1024, 1536), (2, 1))
+    _attn_with_idx(inp, idx)
+
+
+def test_paged_kv(cuda_lib):
+    inp = W.make_decode_inputs(B=3, n_q=1, seq_lens=[700, 2048, 1500], H_I=4, d_I=64, topk=300, H=128,
+                               seed=24, block_size=64, max_L=2048)
+    rng = np.random.default_rng(5)
+    _attn_with_idx(inp, _random_idx(rng, inp))
+
+
+def test_heads_above_128(cuda_lib):
+    inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[512], H_I=4, d_I=64, topk=128, H=160, seed=25)
+    rng = np.random.default_rng(6)
+    _attn_with_idx(inp, _random_idx(rng, inp))

@@ -1,0 +1,116 @@
+"""Lightning Indexer + top-k: CUDA path vs oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_utils import check_topk_exact_on_scores, check_topk_set, oracle_scores_row
+from sparse_attention_prolog_gb300 import binding as B
+from sparse_attention_prolog_gb300 import workloads as W
+from sparse_attention_prolog_gb300.pipeline import DecodeBuffers, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _check_all(inp, buf, tokens=None):
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    idx = buf.topk_idx.cpu().numpy()
+    sc = buf.scores.cpu().numpy()
+    tokens = range(inp.T) if tokens is None else tokens
+    for t in tokens:
+        ref = oracle_scores_row(inp, t)
+        n = int(inp.pos[t]) + 1
+        g = sc[t, :n].astype(np.float64)
+        scale = max(np.abs(ref).max(), 1e-30)
+        assert np.abs(g - ref).max() <= 2e-6 * scale, f"t={t}: score err {np.abs(g - ref).max() / scale:.2e}"
+        if n < inp.max_L:
+            pass
+        check_topk_set(idx[t], ref, n, inp.topk, f"t={t}")
+        check_topk_exact_on_scores(idx[t], sc[t], n, inp.topk, f"t={t}")
+
+
+def test_tiny_decode_indexer(cuda_lib):
+    inp = W.tiny_decode()
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
+def test_ragged_mid_decode_indexer(cuda_lib):
+    """Two sequences (3001 and 4096 keys), MTP1, H_I=64 x d_I=128, top-512:
+    many key tiles, a ragged last tile, masked tail columns."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[3001, 4096], H_I=64, d_I=128, topk=512, H=8, seed=11,
+                               with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
+def test_paged_decode_indexer(cuda_lib):
+    """Paged key cache, 64-token blocks, shuffled block table, n_q=1."""
+    inp = W.make_decode_inputs(B=3, n_q=1, seq_lens=[700, 2048, 1500], H_I=64, d_I=128, topk=256, H=8, seed=12,
+                               block_size=64, max_L=2048, with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
+def test_short_rows_pad_with_minus_one(cuda_lib):
+    """Prefill-like causal rows where early tokens see fewer than k keys."""
+    inp = W.make_decode_inputs(B=1, n_q=384, seq_lens=[384], H_I=64, d_I=128, topk=200, H=8, seed=13,
+                               with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf, tokens=[0, 1, 63, 199, 200, 201, 255, 383])
+
+
+@pytest.mark.parametrize("sign", [1, -1])
+def test_tensor_core_dots_bit_exact(sign, cuda_lib):
+    """One-hot head weights with unit scales make I[t,s] = ReLU(dot[t,h0,s])
+    an exact integer in fp32, exposing the tcgen05 contraction bit by bit
+    (negated q exposes the negative dots)."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[1000, 1024], H_I=64, d_I=128, topk=64, H=8, seed=14,
+                               with_attention=False)
+    inp.q_idx[0, :, :4] = 127
+    inp.k_cache[:8, :4] = -128  # extreme operands in the contraction
+    q = (inp.q_idx.astype(np.int16) * sign).clip(-128, 127).astype(np.int8)
+    ones = np.ones_like(inp.q_idx_scale)
+    for h0 in (0, 17, 63):
+        w = np.zeros_like(inp.w_idx)
+        w[:, h0] = 1.0
+        buf = DecodeBuffers(inp, DEV, q_idx=to_dev(q, DEV), q_idx_scale=to_dev(ones, DEV), w_idx=to_dev(w, DEV),
+                            k_scale=to_dev(np.ones_like(inp.k_scale), DEV), with_attention=False, keep_scores=True)
+        buf.run_topk()
+        torch.cuda.synchronize()
+        sc = buf.scores.cpu().numpy()
+        for t in range(inp.T):
+            n = int(inp.pos[t]) + 1
+            rows = O.logical_rows(inp, int(inp.seq_of_token[t]), n)
+            dots = O.indexer_dots(q[t, h0:h0 + 1], inp.k_cache[rows])[0]
+            np.testing.assert_array_equal(sc[t, :n], np.maximum(dots, 0).astype(np.float32))
+
+
+def test_debug_dots_kernel(cuda_lib):
+    inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[256], H_I=4, d_I=64, topk=32, H=4, seed=15,
+                               with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False)
+    dots = torch.zeros(inp.T, inp.H_I, inp.max_L, dtype=torch.int32, device=DEV)
+    B.dsa_indexer_dots_debug(buf.targs, dots)
+    torch.cuda.synchronize()
+    for t in range(inp.T):
+        ref = O.indexer_dots(inp.q_idx[t], inp.k_cache[O.logical_rows(inp, 0, inp.max_L)])
+        np.testing.assert_array_equal(dots[t].cpu().numpy(), ref)
+
+
+def test_workspace_scores_path(cuda_lib):
+    """Without scores_out the score rows live in the caller's workspace."""
+    inp = W.tiny_decode()
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=False)
+    assert B.workspace_bytes("topk", buf.targs) >= inp.T * inp.max_L * 4
+    buf.run_topk()
+    torch.cuda.synchronize()
+    idx = buf.topk_idx.cpu().numpy()
+    for t in range(inp.T):
+        check_topk_set(idx[t], oracle_scores_row(inp, t), int(inp.pos[t]) + 1, inp.topk)

@@ -1,0 +1,76 @@
+"""Indexer Prolog: CUDA path vs oracle (codes within 1 LSB, scales 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_utils import check_codes
+from sparse_attention_prolog_gb300 import workloads as W
+from sparse_attention_prolog_gb300.pipeline import PrologBuffers
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _run_and_check(p, cuda_lib, cache_rows=None):
+    rows = int(p.slot.max()) + 1 if cache_rows is None else cache_rows
+    kc = torch.full((rows, p.d_I), 99, dtype=torch.int8, device=DEV)
+    ks = torch.full((rows,), 7.0, dtype=torch.float16, device=DEV)
+    buf = PrologBuffers(p, DEV, kc, ks)
+    buf.run()
+    torch.cuda.synchronize()
+    from sparse_attention_prolog_gb300 import binding
+    assert binding.device_error() == 0
+    ref_cache = np.full((rows, p.d_I), 99, np.int8)
+    ref_cs = np.full(rows, 7.0, np.float16)
+    ref = O.indexer_prolog(p, ref_cache, ref_cs)
+    fq = check_codes(buf.q_out.cpu().numpy(), buf.q_scale_out.cpu().numpy(), ref["q"], ref["q_scale"], "q")
+    sl = p.slot[p.slot >= 0]
+    fk = 0.0
+    if sl.size:
+        fk = check_codes(kc.cpu().numpy()[sl], ks.cpu().numpy()[sl], ref_cache[sl], ref_cs[sl], "k")
+    untouched = np.setdiff1d(np.arange(rows), sl)
+    assert (kc.cpu().numpy()[untouched] == 99).all(), "rows without a slot were written"
+    if p.w_proj is not None:
+        wg = buf.w_out.cpu().numpy().astype(np.float64)
+        wr = ref["w"].astype(np.float64)
+        assert np.abs(wg - wr).max() <= 1e-4 * max(1.0, np.abs(wr).max())
+    return fq, fk
+
+
+def test_prolog_alone_T8(cuda_lib):
+    """T=8 at positions 0..7, H_I=64 x d_I=128, K_q=1536, D_x=7168, no weights."""
+    _run_and_check(W.prolog_alone(), cuda_lib)
+
+
+def test_prolog_decode_with_weights(cuda_lib):
+    """The decode step's prolog: positions 65534/65535, cache slots at the
+    end of four 64K sequences, weight stream on."""
+    p = W.decode_64k_prolog()
+    _run_and_check(p, cuda_lib, cache_rows=4 * 65536)
+
+
+@pytest.mark.parametrize("T", [1, 5, 32])
+def test_prolog_token_counts_and_skip_slots(T, cuda_lib):
+    pos = (np.arange(T) * 37) % 4096
+    slot = np.arange(T, dtype=np.int64) * 3
+    slot[::4] = -1  # some tokens write no key
+    p = W.make_prolog_inputs(T=T, pos=pos, slot=slot, seed=50 + T, max_pos=4096)
+    _run_and_check(p, cuda_lib, cache_rows=3 * T + 1)
+
+
+def test_prolog_small_heads_interleaved(cuda_lib):
+    """d_I=64, H_I=4, interleaved RoPE pairs, smaller K_q / D_x."""
+    p = W.make_prolog_inputs(T=6, pos=np.arange(6) * 11, slot=np.arange(6), seed=77, H_I=4, d_I=64,
+                             K_q=512, D_x=1024, rope_interleaved=1, max_pos=64)
+    _run_and_check(p, cuda_lib)
+
+
+def test_prolog_zero_tokens_is_noop(cuda_lib):
+    from sparse_attention_prolog_gb300 import binding as B
+    p = W.prolog_alone()
+    buf = PrologBuffers(p, DEV)
+    buf.args.T = 0
+    B.dsa_indexer_prolog(buf.args, buf.ws)
+    torch.cuda.synchronize()
+    assert (buf.q_out == 0).all()
