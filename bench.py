@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA decode step: Indexer Prolog -> Lightning Indexer ->
+top-k -> sparse MLA attention, B=4 sequences, MTP1 (2 query tokens each),
+64K keys per sequence, on one GB300 per process.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job query tokens per
+second measured on the device (CUDA events on the launching stream, one CUDA
+graph per step, L2 flushed before every step, max over ranks); `e2e` repeats
+the step through the C ABI with host buffers (pinned H2D of the step's new
+inputs, D2H of the attention output) timed on the host; `roofline` is the
+dominant kernel's algorithmic bytes / its event-timed duration against the
+measured HBM copy bandwidth.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparse_attention_prolog_gb300 import dist as D  # noqa: E402
+from sparse_attention_prolog_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode query-tok/s (prolog+indexer+topk+sparse attn), B=4 MTP1 64K; % roofline"
+UNIT = "query-tok/s"
+WORKLOAD = ("decode B=4 x MTP1 (T=8 query tokens), KV 65536 per sequence; indexer H_I=64 d_I=128 int8, "
+            "top-2048; sparse MLA attention 128 heads d_qk=576 d_v=512 bf16; prolog T=8 K_q=1536 D_x=7168")
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ bytes
+def prolog_bytes(p) -> int:
+    """Algorithmic HBM bytes of one prolog launch: every weight and input
+    read once, every output written once."""
+    n = p.q_lora.nbytes + p.q_lora_scale.nbytes + p.w_qb.nbytes + p.w_qb_scale.nbytes + p.x.nbytes
+    n += p.w_k.nbytes + (p.w_proj.nbytes if p.w_proj is not None else 0)
+    n += p.T * p.H_I * (p.d_I + 2) + p.T * (p.d_I + 2) + (p.T * p.H_I * 4 if p.w_proj is not None else 0)
+    return int(n)
+
+
+def indexer_bytes(inp) -> int:
+    """Keys visible to some token of their sequence (int8 d_I + fp16 scale
+    each) plus the query rows, their scales and weights."""
+    keys = sum(int(inp.pos[inp.seq_of_token == b].max()) + 1 for b in range(inp.B))
+    return int(keys * (inp.d_I + 2) + inp.T * inp.H_I * (inp.d_I + 2 + 4))
+
+
+def attention_bytes(inp, idx: np.ndarray) -> int:
+    """q, the distinct selected latent rows of each sequence (1152 B each),
+    the index rows and the bf16 output."""
+    rows = 0
+    for b in range(inp.B):
+        sel = idx[inp.seq_of_token == b]
+        rows += np.unique(sel[sel >= 0]).size
+    return int(inp.T * inp.H * inp.d_qk * 2 + rows * inp.d_qk * 2 + idx.size * 4 + inp.T * inp.H * inp.d_v * 2)
+
+
+def topk_bytes(inp) -> int:
+    return int(sum(int(p) + 1 for p in inp.pos) * 4 + inp.T * inp.topk * 4)
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        ids = {r[1] for r in rows}
+        want = self.uuid.lower().replace("gpu-", "")
+        mine = [r for r in rows if r[1].lower().replace("gpu-", "") == want]
+        if mine:
+            rows = mine
+        elif len(ids) > 1:
+            rows = [r for r in rows if r[0] == "0"]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def device_uuid(dev) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return ""
+
+
+# ------------------------------------------------------------------- ours
+def src_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_attention_prolog_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file: str, summary: str):
+    """dram read+write bytes per launch from a committed ncu summary, if it
+    was taken on the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != src_hash(kernel_file):
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, rank, world, local):
+    from sparse_attention_prolog_gb300 import binding as B
+    from sparse_attention_prolog_gb300.pipeline import DecodeBuffers, PrologBuffers
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+    inp = W.decode_64k(seed=D.replica_seed(1002, rank))
+    p = W.decode_64k_prolog(seed=D.replica_seed(2002, rank))
+    kc = torch.from_numpy(inp.k_cache).to(dev)
+    ks = torch.from_numpy(inp.k_scale).to(dev)
+    pro = PrologBuffers(p, dev, kc, ks)
+    buf = DecodeBuffers(inp, dev, q_idx=pro.q_out, q_idx_scale=pro.q_scale_out, w_idx=pro.w_out, k_cache=kc,
+                        k_scale=ks, keep_scores=True)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(s):
+        pro.run(s)
+        buf.run(s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step(stream)
+    stream.synchronize()
+    if B.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        step(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            graph.replay()
+    stream.synchronize()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(device_uuid(dev)) as clk:
+        D.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                flush.zero_()
+                starts[k].record(stream)
+                graph.replay()
+                ends[k].record(stream)
+        torch.cuda.synchronize()
+        D.barrier()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms_max = D.max_over_ranks(ms, dev)
+    tokens_total = D.sum_over_ranks(inp.T, dev)
+    value = tokens_total / (ms_max / 1e3)
+    clocks = clk.summary()
+
+    # per-stage event timing (each stage alone after an L2 flush)
+    def time_stage(fn, reps):
+        t = []
+        for _ in range(reps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn(stream)
+                b.record(stream)
+            stream.synchronize()
+            t.append(a.elapsed_time(b))
+        return statistics.mean(t)
+
+    reps = min(max(K, 5), 50)
+    st_ms = {
+        "prolog": time_stage(lambda s: pro.run(s), reps),
+        "indexer": time_stage(lambda s: B.dsa_indexer_scores(buf.targs, buf.scores, s), reps),
+        "topk": time_stage(lambda s: B.dsa_topk_from_scores(buf.targs, buf.scores, s), reps),
+        "attention+combine": time_stage(lambda s: buf.run_attn(s), reps),
+    }
+    idx = buf.topk_idx.cpu().numpy()
+    peak, peak_kind = measured_peaks()
+    alg = {"prolog": prolog_bytes(p), "indexer": indexer_bytes(inp), "topk": topk_bytes(inp),
+           "attention+combine": attention_bytes(inp, idx)}
+    dom = max(["prolog", "indexer", "attention+combine"], key=lambda k: st_ms[k])
+    kfile = {"prolog": ("prolog.cu", "prolog_decode64k.txt"), "indexer": ("indexer.cu", "indexer_decode64k.txt"),
+             "attention+combine": ("attention.cu", "attention_decode64k.txt")}[dom]
+    achieved = alg[dom] / (st_ms[dom] / 1e3) / 1e9
+    step_bytes = sum(alg.values())
+
+    # end to end through the C ABI with host buffers
+    h2d = {"q_lora": pro.q_lora, "q_lora_scale": pro.q_lora_scale, "x": pro.x, "pos_prolog": pro.pos,
+           "slot": pro.slot, "pos": buf.pos, "q_attn": buf.q_attn}
+    pinned = {k: v.detach().cpu().pin_memory() for k, v in h2d.items()}
+    out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    h2d_bytes = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h_bytes = out_host.numel() * out_host.element_size()
+    e2e_t = []
+    for k in range(min(K, 50) + 2):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for name, host in pinned.items():
+                h2d[name].copy_(host, non_blocking=True)
+            step(stream)
+            out_host.copy_(buf.out, non_blocking=True)
+        stream.synchronize()
+        if k >= 2:
+            e2e_t.append(time.perf_counter() - t0)
+    e2e_s = D.max_over_ranks(statistics.mean(e2e_t), dev)
+    e2e_value = tokens_total / e2e_s
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 indexer (exact f16 MMA), bf16 attention, fp32 accumulate",
+        "data": "synthetic (seeded; replica r uses seed + 100 r)",
+        "config": {"workload": WORKLOAD, "global_batch": inp.B * world, "query_tokens_per_step": int(tokens_total),
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "timing": "one CUDA graph per step, CUDA events on its stream", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes": alg[dom],
+                     "traffic": profiled_traffic(*kfile)},
+        "step_roofline": {"algorithmic_bytes": step_bytes,
+                          "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
+                          "frac": round(step_bytes / (peak * 1e9) / (ms_max / 1e3), 4)},
+        "stages_ms": {k: round(v, 5) for k, v in st_ms.items()},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d_bytes),
+                "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": K * 5,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, p, budget_s=args.cpu_budget)
+    return result
+
+
+# ---------------------------------------------------------------- oracle
+def oracle_step(inp, p, tokens):
+    """The whole decode step on the CPU oracle for the given query tokens:
+    prolog (all T tokens' q / k / w rows are one GEMM of the sample),
+    indexer scores, full-sort top-k and attention for `tokens`."""
+    import oracle as O
+    kc = inp.k_cache
+    ks = inp.k_scale
+    pr = O.indexer_prolog(p)
+    kc_rows = {int(s): (pr["k"][i], pr["k_scale"][i]) for i, s in enumerate(p.slot)}
+    idx = np.full((inp.T, inp.topk), -1, np.int64)
+    for t in tokens:
+        b = int(inp.seq_of_token[t])
+        n = int(inp.pos[t]) + 1
+        rows = O.logical_rows(inp, b, n)
+        keys, kscale = kc[rows].copy(), ks[rows].copy()
+        for j, r in enumerate(rows[-2:]):
+            if int(r) in kc_rows:
+                keys[n - 2 + j], kscale[n - 2 + j] = kc_rows[int(r)]
+        sc = O.indexer_scores_token(pr["q"][t], pr["q_scale"][t], pr["w"][t], keys, kscale, n - 1)
+        idx[t] = O.topk_indices(sc, n, inp.topk)
+    out, _ = O.sparse_attention(inp, idx, tokens)
+    return out
+
+
+def cpu_baseline(inp, p, budget_s=20.0):
+    t0 = time.perf_counter()
+    done = 0
+    reps = 0
+    while True:
+        oracle_step(inp, p, list(range(inp.T)))
+        done += inp.T
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 200:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(done / el, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} full decode step(s) of the same workload ({inp.T} query tokens each), numpy float64 "
+                      "(BLAS threads up to the core count)", "seconds": round(el, 2)}
+
+
+def run_reference(args, rank, world):
+    inp = W.decode_64k(seed=1002)
+    p = W.decode_64k_prolog(seed=2002)
+    per_step = list(range(args.ref_tokens))
+
+    def one():
+        oracle_step(inp, p, per_step)
+
+    for _ in range(args.warmup):
+        one()
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        t.append(time.perf_counter() - t0)
+    s = statistics.mean(t)
+    value = len(per_step) / s
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "global_batch": inp.B, "query_tokens_per_step": len(per_step)},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"each step: the prolog of all {inp.T} tokens plus indexer, top-k and "
+                                   f"attention of {len(per_step)} query token(s)"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = D.init()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        D.shutdown()
+        return
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    D.barrier()
+    D.shutdown()
+
+
+if __name__ == "__main__":
+    main()
