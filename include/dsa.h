@@ -124,6 +124,29 @@ typedef struct {
 size_t dsa_indexer_prolog_workspace(const dsa_prolog_args* args);
 int dsa_indexer_prolog(const dsa_prolog_args* args, void* workspace, size_t workspace_bytes, void* stream);
 
+/* dsa_indexer_prolog_noalloc: the Indexer Prolog for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an
+ * interface convenience of this library, not part of the method.
+ *
+ * Some callers are handed only their input and output tensors and have no
+ * device allocator (a plug-in inside a host framework that owns all device
+ * memory), or run a loop that must never call cudaMalloc because it can
+ * synchronise the device.  This entry point takes the same arguments and
+ * gives the same results as dsa_indexer_prolog but needs no workspace: its
+ * scratch is one 64 KiB array compiled into the library, held on every GPU
+ * that loads the library until the process exits.  It allocates nothing.
+ *
+ *   - Requests whose workspace would exceed 64 KiB are rejected with
+ *     DSA_ERR_WORKSPACE before anything is enqueued (every supported prolog
+ *     shape, T <= 32 and d_I + H_I <= 256 channels, fits).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array and clears the part that must start at
+ *     zero itself; calls that may overlap on the GPU (other streams, other
+ *     threads) race on it and must be serialised by the caller. */
+int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
+
 /* ------------------------------------------------------------------------
  * Lightning Indexer + top-k  [V3.2-PyPTO §Lightning Indexer: the int8 q
  * scored against the C8 key cache, then a per-query TopK; V4-TileLang

@@ -54,7 +54,7 @@ EXPORTS = [
     "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
     "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
     "dsa_indexer_scores", "dsa_topk_from_scores",
-    "dsa_sparse_attn_workspace", "dsa_sparse_attn",
+    "dsa_sparse_attn_workspace", "dsa_sparse_attn", "dsa_indexer_prolog_noalloc",
 ]
 
 _lib = None
@@ -85,6 +85,8 @@ def load(path: str = LIB_PATH):
         getattr(lib, ws).restype = ctypes.c_size_t
         getattr(lib, run).argtypes = [ctypes.POINTER(st), c_ptr, ctypes.c_size_t, c_ptr]
         getattr(lib, run).restype = c_int
+    lib.dsa_indexer_prolog_noalloc.argtypes = [ctypes.POINTER(PrologArgs), c_ptr]
+    lib.dsa_indexer_prolog_noalloc.restype = c_int
     lib.dsa_indexer_dots_debug.argtypes = [ctypes.POINTER(TopkArgs), c_ptr, c_ptr]
     lib.dsa_indexer_dots_debug.restype = c_int
     lib.dsa_indexer_scores.argtypes = [ctypes.POINTER(TopkArgs), c_ptr, c_ptr]
@@ -141,6 +143,12 @@ def dsa_indexer_prolog(args: PrologArgs, workspace: Optional[torch.Tensor] = Non
     ws, n = _ws(need, device or "cuda", workspace)
     _check(lib.dsa_indexer_prolog(ctypes.byref(args), _p(ws), n, _stream(stream)), "dsa_indexer_prolog")
     return ws
+
+
+def dsa_indexer_prolog_noalloc(args: PrologArgs, stream=None):
+    """The prolog without a workspace: its scratch is a fixed array inside the
+    library, for callers that cannot allocate device memory."""
+    _check(load().dsa_indexer_prolog_noalloc(ctypes.byref(args), _stream(stream)), "dsa_indexer_prolog_noalloc")
 
 
 # ----------------------------------------------------------------- top-k
