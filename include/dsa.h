@@ -90,8 +90,8 @@ int dsa_get_device_error(void* stream);
  * receives token t's key, -1 = none (slots must not repeat); w_out fp32
  * [T, H_I] (required iff w_proj != NULL).
  * Supported: 1 <= T <= 32, d_I in {64, 128}, 1 <= H_I <= 128, d_rope even
- * with d_rope <= d_I and (d_rope/2) a multiple of d_I/32, K_q and D_x
- * multiples of 64.  Workspace: dsa_indexer_prolog_workspace() bytes; it must
+ * with d_rope <= d_I and (d_rope/2) a multiple of d_I/32, K_q <= 2048 and
+ * D_x <= 12288, both multiples of 64.  Workspace: dsa_indexer_prolog_workspace() bytes; it must
  * be zero-filled once before its first use (the library leaves it zeroed).
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -170,9 +170,13 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * block_size + s % block_size, block_table int32 [B, max_blocks],
  * max_L = max_blocks * block_size.
  * Supported: d_I in {64, 128}; H_I in {4, 8, 16, 32, 64, 128}; topk >= 1;
+ * B * ceil(n_q / G) <= 4096 token groups, G = min(n_q, 128 / H_I, 32);
  * max_L a multiple of 128; block_size a multiple of 8 that divides 128 or
  * is a multiple of 128.  Workspace: dsa_indexer_topk_workspace() bytes (the
- * fp32 score rows live there when scores_out is NULL).
+ * fp32 score rows live there when scores_out is NULL, and, for H_I >= 64
+ * with at most 512 tokens, per-token score histograms and top-k
+ * candidates); it must be zero-filled once before its first use (the
+ * library leaves it zeroed).
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t T, B, n_q, H_I, d_I, topk, max_L;

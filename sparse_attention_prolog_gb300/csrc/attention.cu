@@ -46,6 +46,7 @@ constexpr int kThreads = 320;
 constexpr uint32_t kPBytes = 128 * (8 * 16 + 4);  // P row + alpha, per tile
 constexpr uint32_t kFinalBytes = 128 * 8;
 constexpr uint32_t kTmemQ = 0, kTmemS = 288;    // CTA 0 column map
+constexpr int kSmemA = kStagesK * kStageK;  // 221,184 B
 
 struct AttnParams {
   int T, n_q, H, topk, max_L, n_chunks, chunk_rows, head_blocks;
@@ -57,7 +58,7 @@ struct AttnParams {
   const int32_t* idx;
   __nv_bfloat16* out;
   float* lse;
-  float* part_o;   // [T][n_chunks][H][512] when n_chunks > 1
+  __nv_bfloat16* part_o;  // [T][n_chunks][H][512], O_c / l_c, when n_chunks > 1
   float2* part_ml; // [T][n_chunks][H]: (max, sum) in log2 units
   uint32_t* err;
 };
@@ -69,6 +70,7 @@ struct __align__(8) Bars {
   uint64_t vfull[kStagesV], vempty[kStagesV];   // CTA 1 gather ring
   uint64_t pfull[2], pcons[2];                  // CTA 1 P slots
   uint64_t ready[2], odone, ffull;              // CTA 1 correction / MMA
+  uint64_t qready;                              // CTA 0: q is in TMEM
 };
 
 __device__ __forceinline__ int64_t kv_row(const AttnParams& P, int b, int s) {
@@ -77,25 +79,32 @@ __device__ __forceinline__ int64_t kv_row(const AttnParams& P, int b, int s) {
   return blk < 0 ? -1 : static_cast<int64_t>(blk) * P.block_size + s % P.block_size;
 }
 
-// Gathers the rows of tile `j` into a swizzled stage: `atoms` 64-dim atoms
-// of every row, zero rows for masked slots.  128 threads, cp.async.
-__device__ __forceinline__ void gather_tile(const AttnParams& P, const int32_t* idx_row, int b, int slot0,
-                                            uint8_t* stage, int atoms, int ct) {
+// Physical row of the slot this lane looks up for tile slot0 of producer
+// warp pw (lane l covers row pw*16 + l%16); -1 for masked slots.
+__device__ __forceinline__ long long gather_row(const AttnParams& P, const int32_t* idx_row, int b, int slot0,
+                                                int pw, int lane) {
+  const int slot = slot0 + pw * 16 + (lane & 15);
+  const int s = (slot < P.topk) ? __ldg(idx_row + slot) : -1;
+  return (s >= 0 && s < P.max_L) ? kv_row(P, b, s) : -1;
+}
+
+// Gathers the 64 rows of one tile into a swizzled stage: `atoms` 64-dim
+// atoms of every row, zero rows for masked slots.  Producer warp pw (0..3)
+// owns rows pw*16 .. pw*16+15 whose physical addresses (one per lane, see
+// gather_row, looked up a tile ahead) are broadcast by shuffle.  Lanes copy
+// consecutive 16-byte chunks of a row (coalesced) with cp.async.
+__device__ __forceinline__ void gather_tile(const AttnParams& P, long long row, uint8_t* stage, int atoms, int pw,
+                                            int lane) {
   const int chunks = atoms * 8;
-  for (int task = ct; task < kRows * chunks; task += 128) {
-    const int r = task / chunks, c = task % chunks;
-    const int slot = slot0 + r;
-    const int s = (slot < P.topk) ? __ldg(idx_row + slot) : -1;
-    const __nv_bfloat16* src = P.kv;
-    uint32_t bytes = 0;
-    if (s >= 0 && s < P.max_L) {
-      const int64_t row = kv_row(P, b, s);
-      if (row >= 0) {
-        src = P.kv + row * kDqk + c * 8;
-        bytes = 16;
-      }
-    }
-    cp_async16(smem_u32(stage + (c / 8) * (kRows * 128) + sw128_off(r, c % 8)), src, bytes);
+  const uint32_t sbase = smem_u32(stage);
+#pragma unroll 4
+  for (int rr = 0; rr < 16; ++rr) {
+    const long long prow = __shfl_sync(0xffffffffu, row, rr);
+    const int r = pw * 16 + rr;
+    const __nv_bfloat16* rsrc = P.kv + (prow >= 0 ? prow : 0) * kDqk;
+    const uint32_t bytes = prow >= 0 ? 16u : 0u;
+    for (int c = lane; c < chunks; c += 32)
+      cp_async16(sbase + (c >> 3) * (kRows * 128) + sw128_off(r, c & 7), rsrc + c * 8, bytes);
   }
 }
 
@@ -123,14 +132,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   uint8_t* sK = smem;                                           // CTA 0: K stages
 
   if (tid == 0) {
-    for (int i = 0; i < kStagesK; ++i) { mbar_init(&bars.kfull[i], 4); mbar_init(&bars.kempty[i], 1); }
+    for (int i = 0; i < kStagesK; ++i) { mbar_init(&bars.kfull[i], 128); mbar_init(&bars.kempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.sfull[i], 1); mbar_init(&bars.sempty[i], 4); mbar_init(&bars.pfree[i], 1);
       mbar_init(&bars.pfull[i], 1); mbar_init(&bars.pcons[i], 1); mbar_init(&bars.ready[i], 4);
     }
-    for (int i = 0; i < kStagesV; ++i) { mbar_init(&bars.vfull[i], 4); mbar_init(&bars.vempty[i], 1); }
+    for (int i = 0; i < kStagesV; ++i) { mbar_init(&bars.vfull[i], 128); mbar_init(&bars.vempty[i], 1); }
     mbar_init(&bars.odone, 1);
     mbar_init(&bars.ffull, 1);
+    mbar_init(&bars.qready, 4);
     abort_flag = 0;
     fence_mbar_init();
     if (rank == 1) {
@@ -147,25 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   volatile int* abort_v = &abort_flag;
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  if (rank == 0 && warp < 4) {
-    // q row of this thread's head into TMEM columns [0, 288).
-    const int h = hb * 128 + warp * 32 + lane;
-    const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (static_cast<size_t>(t) * P.H + h) * kDqk);
-    for (int a = 0; a < kAtomsK; ++a) {
-      uint32_t r[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < P.H) v = __ldg(qrow + a * 8 + c);
-        r[4 * c] = v.x; r[4 * c + 1] = v.y; r[4 * c + 2] = v.z; r[4 * c + 3] = v.w;
-      }
-      tmem_st32(tmem + lane_off + kTmemQ + a * 32, r);
-    }
-    tmem_st_wait();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  const int q_rows = max(0, min(128, P.H - hb * 128));  // real heads of this block
   cluster_sync();  // both CTAs' barriers are initialised before any remote use
   griddep_launch_dependents();
   griddep_wait();  // topk_idx comes from the previous kernel
@@ -173,28 +165,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   if (rank == 0) {
     if (warp >= 4 && warp < 8) {
       // ------------------------------------------------ gather K (CTA 0)
-      const int ct = tid - 128;
-      int st = 0, prev = 0;
+      int st = 0;
       uint32_t ph = 0;
+      long long row_next = n_tiles > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
       for (int j = 0; j < n_tiles; ++j) {
+        const long long row = row_next;
+        if (j + 1 < n_tiles) row_next = gather_row(P, idx_row, b, slot_begin + (j + 1) * kRows, warp - 4, lane);
         if (!mbar_wait(&bars.kempty[st], ph ^ 1, P.err, abort_v)) break;
-        gather_tile(P, idx_row, b, slot_begin + j * kRows, sK + st * kStageK, kAtomsK, ct);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        // keep two tiles in flight: publish the previous one
-        if (j > 0) {
-          asm volatile("cp.async.wait_group 1;" ::: "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.kfull[prev]);
-        }
-        prev = st;
+        gather_tile(P, row, sK + st * kStageK, kAtomsK, warp - 4, lane);
+        // the stage's barrier counts this thread once its copies have landed
+        cp_async_mbar_arrive(&bars.kfull[st]);
         if (++st == kStagesK) { st = 0; ph ^= 1; }
-      }
-      if (n_tiles > 0 && !*abort_v) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.kfull[prev]);
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == 8) {
@@ -203,9 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
         int st = 0, sb = 0;
         uint32_t ph = 0, phs = 0;
+        if (n_tiles > 0 && mbar_wait(&bars.qready, 0, P.err, abort_v)) tc_fence_after();
         for (int j = 0; j < n_tiles; ++j) {
           if (!mbar_wait(&bars.kfull[st], ph, P.err, abort_v)) break;
           if (!mbar_wait(&bars.sempty[sb], phs ^ 1, P.err, abort_v)) break;
+          fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
           tc_fence_after();
           const uint32_t base = smem_u32(sK + st * kStageK);
           for (int kk = 0; kk < kDqk / 16; ++kk) {
@@ -226,18 +209,51 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       const uint32_t remote_final = mapa(smem_u32(sFinal), 1);
       const uint32_t remote_pfull[2] = {mapa(smem_u32(&bars.pfull[0]), 1), mapa(smem_u32(&bars.pfull[1]), 1)};
       const uint32_t remote_ffull = mapa(smem_u32(&bars.ffull), 1);
+      // q row of this thread's head: global -> registers -> TMEM columns
+      // [0, 288), three atoms (24 independent 16-byte loads) per round.
+      {
+        const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (static_cast<size_t>(t) * P.H + hb * 128 + hrow) * kDqk);
+        const bool real = hrow < q_rows;
+#pragma unroll 1
+        for (int a0 = 0; a0 < kAtomsK; a0 += 3) {
+          uint4 v[24];
+#pragma unroll
+          for (int i = 0; i < 24; ++i) v[i] = real ? __ldg(qrow + a0 * 8 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int a = 0; a < 3; ++a) {
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              r[4 * c] = v[a * 8 + c].x; r[4 * c + 1] = v[a * 8 + c].y;
+              r[4 * c + 2] = v[a * 8 + c].z; r[4 * c + 3] = v[a * 8 + c].w;
+            }
+            tmem_st32(tmem + lane_off + kTmemQ + (a0 + a) * 32, r);
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.qready);
       const float ninf = -__int_as_float(0x7f800000);
       float m_used = ninf, l_sum = 0.f;
       int sb = 0;
       uint32_t phs = 0;
       bool ok = true;
+      // this lane's two index slots of a tile, loaded one tile ahead
+      auto load_idx = [&](int jj, int& lo, int& hi) {
+        const int slot0 = slot_begin + jj * kRows;
+        lo = (slot0 + lane < P.topk) ? __ldg(idx_row + slot0 + lane) : -1;
+        hi = (slot0 + 32 + lane < P.topk) ? __ldg(idx_row + slot0 + 32 + lane) : -1;
+      };
+      int nx_lo = -1, nx_hi = -1;
+      if (n_tiles > 0) load_idx(0, nx_lo, nx_hi);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int slot0 = slot_begin + j * kRows;
-        const int s_lo = (slot0 + lane < P.topk) ? __ldg(idx_row + slot0 + lane) : -1;
-        const int s_hi = (slot0 + 32 + lane < P.topk) ? __ldg(idx_row + slot0 + 32 + lane) : -1;
+        const int s_lo = nx_lo, s_hi = nx_hi;
+        if (j + 1 < n_tiles) load_idx(j + 1, nx_lo, nx_hi);
+        if (!mbar_wait(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
         const uint32_t v_lo = __ballot_sync(0xffffffffu, s_lo >= 0 && s_lo < P.max_L);
         const uint32_t v_hi = __ballot_sync(0xffffffffu, s_hi >= 0 && s_hi < P.max_L);
-        if (!mbar_wait(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
         tc_fence_after();
         uint32_t s0[32], s1[32];
         tmem_ld32(tmem + lane_off + kTmemS + sb * kRows, s0);
@@ -286,28 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   } else {
     if (warp >= 4 && warp < 8) {
       // ------------------------------------------------ gather V (CTA 1)
-      const int ct = tid - 128;
-      int st = 0, prev = 0;
+      int st = 0;
       uint32_t ph = 0;
+      long long row_next = n_tiles > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
       for (int j = 0; j < n_tiles; ++j) {
+        const long long row = row_next;
+        if (j + 1 < n_tiles) row_next = gather_row(P, idx_row, b, slot_begin + (j + 1) * kRows, warp - 4, lane);
         if (!mbar_wait(&bars.vempty[st], ph ^ 1, P.err, abort_v)) break;
-        gather_tile(P, idx_row, b, slot_begin + j * kRows, sV + st * kStageV, kAtomsV, ct);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        // keep two tiles in flight: publish the previous one
-        if (j > 0) {
-          asm volatile("cp.async.wait_group 1;" ::: "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.vfull[prev]);
-        }
-        prev = st;
+        gather_tile(P, row, sV + st * kStageV, kAtomsV, warp - 4, lane);
+        // the stage's barrier counts this thread once its copies have landed
+        cp_async_mbar_arrive(&bars.vfull[st]);
         if (++st == kStagesV) { st = 0; ph ^= 1; }
-      }
-      if (n_tiles > 0 && !*abort_v) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.vfull[prev]);
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == 8) {
@@ -320,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
           const int ps = j & 1;
           if (!mbar_wait(&bars.vfull[st], ph, P.err, abort_v)) break;
           if (!mbar_wait(&bars.ready[ps], (j >> 1) & 1, P.err, abort_v)) break;
+          fence_proxy_async_smem();  // cp.async / st.async data -> tensor core reads
           tc_fence_after();
           const uint32_t pbase = smem_u32(sP + ps * kPSlot);
           const uint32_t vbase = smem_u32(sV + st * kStageV);
@@ -421,18 +427,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
           P.lse[static_cast<size_t>(t) * P.H + h] =
               empty ? -__int_as_float(0x7f800000) : (ml.x + log2f(ml.y)) * 0.69314718055994531f;
       } else {
-        float* orow = P.part_o + ((static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h) * kDv;
+        __nv_bfloat16* orow = P.part_o + ((static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h) * kDv;
         for (int c0 = 0; c0 < kDv; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + c0, v);
           tmem_ld_wait();
           if (h < P.H) {
-            float4* dst = reinterpret_cast<float4*>(orow + c0);
+            uint32_t pk[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[k] = empty ? make_float4(0.f, 0.f, 0.f, 0.f)
-                             : make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
-                                           __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
+            for (int k = 0; k < 16; ++k) {
+              const float a = empty ? 0.f : __uint_as_float(v[2 * k]) * inv_l;
+              const float bb = empty ? 0.f : __uint_as_float(v[2 * k + 1]) * inv_l;
+              __nv_bfloat162 pb = __floats2bfloat162_rn(a, bb);
+              pk[k] = *reinterpret_cast<uint32_t*>(&pb);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
           }
         }
         if (h < P.H)
@@ -469,15 +480,17 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
     if (!(ml.y > 0.f)) continue;
     const float wc = ml.y * exp2f(ml.x - M);
     wsum += wc;
-    const float4* src = reinterpret_cast<const float4*>(
+    const uint2* src = reinterpret_cast<const uint2*>(
         P.part_o + ((static_cast<size_t>(t) * P.n_chunks + c) * P.H + h) * kDv);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float4 v = __ldcg(src + lane + 32 * k);
-      acc[4 * k] = fmaf(wc, v.x, acc[4 * k]);
-      acc[4 * k + 1] = fmaf(wc, v.y, acc[4 * k + 1]);
-      acc[4 * k + 2] = fmaf(wc, v.z, acc[4 * k + 2]);
-      acc[4 * k + 3] = fmaf(wc, v.w, acc[4 * k + 3]);
+      const uint2 raw = __ldcg(src + lane + 32 * k);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      acc[4 * k] = fmaf(wc, a.x, acc[4 * k]);
+      acc[4 * k + 1] = fmaf(wc, a.y, acc[4 * k + 1]);
+      acc[4 * k + 2] = fmaf(wc, b2.x, acc[4 * k + 2]);
+      acc[4 * k + 3] = fmaf(wc, b2.y, acc[4 * k + 3]);
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -511,7 +524,7 @@ size_t attn_workspace(const dsa_attn_args& a) {
   int hb, nc, cr;
   plan(a, hb, nc, cr);
   if (nc == 1) return 0;
-  const size_t o = static_cast<size_t>(a.T) * nc * a.H * kDv * sizeof(float);
+  const size_t o = static_cast<size_t>(a.T) * nc * a.H * kDv * sizeof(__nv_bfloat16);
   const size_t ml = static_cast<size_t>(a.T) * nc * a.H * sizeof(float2);
   return round_up(o, 256) + round_up(ml, 256);
 }
@@ -528,16 +541,16 @@ int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
   P.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   P.lse = a.lse;
   if (P.n_chunks > 1) {
-    P.part_o = static_cast<float*>(ws);
+    P.part_o = static_cast<__nv_bfloat16*>(ws);
     P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +
-                                          round_up(static_cast<size_t>(a.T) * P.n_chunks * a.H * kDv * 4, 256));
+                                          round_up(static_cast<size_t>(a.T) * P.n_chunks * a.H * kDv * 2, 256));
   }
   P.err = error_word();
   if (!P.err) return DSA_ERR_CUDA;
 
-  const size_t smem = 1024 + (kStagesK * kStageK > kStagesV * kStageV + 2 * kPSlot + 2048
-                                  ? static_cast<size_t>(kStagesK) * kStageK
-                                  : static_cast<size_t>(kStagesV) * kStageV + 2 * kPSlot + 2048);
+  const size_t smem = 1024 + static_cast<size_t>(kSmemA > kStagesV * kStageV + 2 * kPSlot + 2048
+                                                    ? kSmemA
+                                                    : kStagesV * kStageV + 2 * kPSlot + 2048);
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};

@@ -1,4 +1,6 @@
 // The C ABI: argument validation, workspace sizing, device error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <mutex>
 #include "dsa_internal.h"
@@ -45,6 +47,34 @@ int sm_count() {
   return g_sms[d];
 }
 
+bool encode_tmap_u8_2d(void* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                       uint32_t box_rows, int swizzle_bytes) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!fn) {
+      cudaDriverEntryPointQueryResult q;
+      void* p = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !p)
+        return false;
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_stride};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                               : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                     : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUresult r = fn(static_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -60,8 +90,8 @@ int check_prolog(const dsa_prolog_args* a) {
   if (a->H_I < 1 || a->H_I > 128) return DSA_ERR_UNSUPPORTED;
   if (a->d_rope < 0 || a->d_rope > a->d_I || (a->d_rope % 2) != 0 || ((a->d_rope / 2) % (a->d_I / 32)) != 0)
     return DSA_ERR_UNSUPPORTED;
-  if (a->K_q <= 0 || a->K_q % 64 != 0 || a->K_q > 4096) return DSA_ERR_UNSUPPORTED;
-  if (a->D_x <= 0 || a->D_x % 64 != 0) return DSA_ERR_UNSUPPORTED;
+  if (a->K_q <= 0 || a->K_q % 64 != 0 || a->K_q > 2048) return DSA_ERR_UNSUPPORTED;
+  if (a->D_x <= 0 || a->D_x % 64 != 0 || a->D_x > 12288) return DSA_ERR_UNSUPPORTED;
   if (a->rope_max_pos <= 0 || a->cache_rows < 0 || !(a->ln_eps >= 0.f)) return DSA_ERR_INVALID_ARG;
   if (a->T == 0) return DSA_OK;
   const size_t code_align = a->d_I == 128 ? 4 : 2;
@@ -120,6 +150,12 @@ size_t topk_scores_bytes(const dsa_topk_args* a) {
   return a->scores_out ? 0 : round_up(static_cast<size_t>(a->T) * a->max_L * sizeof(float), 256);
 }
 
+// Workspace of dsa_indexer_topk: score rows (unless scores_out is given),
+// then, on the fused path, the histogram / counters / candidates region.
+size_t topk_total_bytes(const dsa_topk_args* a) {
+  return topk_scores_bytes(a) + (topk_hist_eligible(*a) ? topk_hist_workspace(*a) : 0);
+}
+
 }  // namespace
 
 extern "C" {
@@ -164,17 +200,23 @@ int dsa_indexer_prolog(const dsa_prolog_args* a, void* ws, size_t ws_bytes, void
 
 size_t dsa_indexer_topk_workspace(const dsa_topk_args* a) {
   if (check_topk(a) != DSA_OK) return 0;
-  return topk_scores_bytes(a);
+  return topk_total_bytes(a);
 }
 
 int dsa_indexer_topk(const dsa_topk_args* a, void* ws, size_t ws_bytes, void* stream) {
   const int st = check_topk(a);
   if (st != DSA_OK || a->T == 0) return st;
-  const size_t need = topk_scores_bytes(a);
+  const size_t need = topk_total_bytes(a);
   if (need > 0 && (ws == nullptr || !aligned(ws, 256) || ws_bytes < need)) return DSA_ERR_WORKSPACE;
   float* scores = a->scores_out ? a->scores_out : static_cast<float*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int r = launch_indexer(*a, scores, s);
+  if (topk_hist_eligible(*a)) {
+    void* hws = static_cast<uint8_t*>(ws) + topk_scores_bytes(a);
+    int r = launch_indexer(*a, scores, static_cast<uint32_t*>(hws), s);
+    if (r != DSA_OK) return r;
+    return launch_topk_hist(*a, scores, a->max_L, hws, s);
+  }
+  int r = launch_indexer(*a, scores, nullptr, s);
   if (r != DSA_OK) return r;
   return launch_topk(*a, scores, a->max_L, s);
 }
@@ -183,7 +225,7 @@ int dsa_indexer_scores(const dsa_topk_args* a, float* scores, void* stream) {
   const int st = check_topk(a);
   if (st != DSA_OK || a->T == 0) return st;
   if (bad_ptr(scores, 16)) return DSA_ERR_INVALID_ARG;
-  return launch_indexer(*a, scores, static_cast<cudaStream_t>(stream));
+  return launch_indexer(*a, scores, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int dsa_topk_from_scores(const dsa_topk_args* a, const float* scores, int64_t ld, void* stream) {

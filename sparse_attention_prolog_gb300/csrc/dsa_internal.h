@@ -18,13 +18,28 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Encodes a 2-D tiled tensor map of uint8 rows (inner extent `inner` bytes,
+// `rows` rows, `row_stride` bytes apart) with box {inner, box_rows} and the
+// given swizzle (0 none, 64 or 128 bytes) into `out` (128 bytes, 64-aligned).
+// Returns false if the driver entry point is unavailable or rejects it.
+bool encode_tmap_u8_2d(void* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                       uint32_t box_rows, int swizzle_bytes);
+
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 // Launchers implemented by the kernel translation units.
 int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t s);
 size_t prolog_workspace(const dsa_prolog_args& a);
 
-int launch_indexer(const dsa_topk_args& a, float* scores, cudaStream_t s);
+int launch_indexer(const dsa_topk_args& a, float* scores, uint32_t* hist, cudaStream_t s);
+
+// Fused top-k path: the indexer also counts each token's scores by their
+// leading 12 key bits; the top-k pass then needs one read of the row.
+constexpr int kTopkHistBins = 4096;
+constexpr int kTopkCandCap = 16384;
+bool topk_hist_eligible(const dsa_topk_args& a);
+size_t topk_hist_workspace(const dsa_topk_args& a);  // hist + counters + candidates
+int launch_topk_hist(const dsa_topk_args& a, const float* scores, int64_t ld, void* ws, cudaStream_t s);
 int launch_indexer_dots(const dsa_topk_args& a, int32_t* dots, cudaStream_t s);
 int launch_topk(const dsa_topk_args& a, const float* scores, int64_t scores_ld, cudaStream_t s);
 

@@ -18,16 +18,23 @@
 // dots equal the int32 ones bit for bit.
 //
 // Warp roles of the persistent CTA (one per SM):
-//   warp 8     producer: cp.async.bulk of the raw int8 key tile (16 KB)
-//   warps 4-7  converters: int8 -> f16 into the 128B-swizzled K-major
-//              layout the MMA reads; also stage Q for each new group
-//   warp 9     one thread issues tcgen05.mma into a double-buffered TMEM
-//              accumulator and commits to mbarriers
+//   warp 8     producer: 2-D TMA loads (128B swizzle) of the raw int8 key
+//              tile into an 8-deep shared-memory ring
+//   warps 4-7  converters: one thread per key row reads its 128 bytes
+//              (bank-conflict free thanks to the swizzle), converts them to
+//              f16 and stores the row into TMEM, where it is the A operand
+//              of the MMA; they also stage Q (the B operand, shared memory)
+//              for each new group
+//   warp 9     one thread issues tcgen05.mma (A from TMEM, B from shared
+//              memory) into a double-buffered TMEM accumulator
+// Keeping the keys out of shared memory after the TMA halves the shared
+// memory traffic per tile, which otherwise bounds the kernel.
 //   warps 0-3  epilogue: tcgen05.ld of the accumulator row of its key,
 //              ReLU + head-weighted sum per token, times ks[s], causal mask,
 //              and the fp32 score row store (coalesced over keys)
 // The per-head scores [T, H_I, L] never leave the SM; only I[t, s] (fp32,
 // [T, max_L]) is written, for the top-k pass.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include "dsa_internal.h"
@@ -37,11 +44,12 @@ namespace dsa {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kStages8 = 4;   // raw int8 key tiles in flight
-constexpr int kStages16 = 2;  // converted f16 tiles
+constexpr int kStages8 = 8;   // raw int8 key tiles in flight
+constexpr int kStages16 = 2;  // converted f16 key tiles (in TMEM)
 constexpr int kThreads = 320;
 constexpr int kMaxG = 32;     // tokens per group
 constexpr int kCoef = 256;    // max query rows (N) of a group
+constexpr int kHistBins = 4096;  // leading 12 bits of the score's order key
 
 struct IdxParams {
   int T, n_q, H_I, d_I, G, N, groups_per_seq, n_groups, n_tiles, max_L;
@@ -51,10 +59,11 @@ struct IdxParams {
   const int8_t* k_cache;
   const __half* k_scale;
   const int32_t* block_table;
-  int block_size, max_blocks;
+  int block_size, max_blocks, box_rows;
   const int32_t* pos;
   float* scores;
   int64_t ld;
+  uint32_t* hist;  // [T][kHistBins] leading-digit counts of the scores, or null
   uint32_t* err;
 };
 
@@ -74,19 +83,33 @@ __device__ __forceinline__ Group group_of(const IdxParams& P, int g) {
   return G;
 }
 
-// Next active item (a tile that holds at least one visible key) of this
-// CTA at or after item i; returns n_items when none is left.
-__device__ __forceinline__ int next_item(const IdxParams& P, int i, int& g_cache, int& maxpos_cache) {
-  const int n_items = P.n_groups * P.n_tiles;
-  for (; i < n_items; i += gridDim.x) {
-    const int g = i / P.n_tiles, j = i % P.n_tiles;
-    if (g != g_cache) {
-      g_cache = g;
-      maxpos_cache = group_of(P, g).maxpos;
-    }
-    if (j * kTileKeys <= maxpos_cache) return i;
+// Work list: the active tiles (tiles holding at least one visible key) of
+// all groups in group-major order.  Every CTA computes the per-group tile
+// counts and their prefix sum, then walks its own contiguous, equal share of
+// the list, so a decode CTA stays in one group and a prefill CTA gets an
+// equal number of tiles however causal masking thins the groups.
+constexpr int kMaxGroupsScheduled = 4096;
+
+struct Walker {
+  int g, j, left;  // current group, tile within the group, items left
+};
+
+__device__ __forceinline__ int group_tiles(const IdxParams& P, int g) {
+  const Group G = group_of(P, g);
+  return G.maxpos < 0 ? 0 : min(P.n_tiles, G.maxpos / kTileKeys + 1);
+}
+
+// Advances to the next tile of the walk (skips groups without tiles).
+__device__ __forceinline__ bool walk_next(const int* tiles_prefix, int n_groups, Walker& w) {
+  if (w.left <= 0) return false;
+  --w.left;
+  if (w.left == 0) return false;
+  ++w.j;
+  while (w.g < n_groups && w.j >= tiles_prefix[w.g + 1] - tiles_prefix[w.g]) {
+    ++w.g;
+    w.j = 0;
   }
-  return n_items;
+  return true;
 }
 
 __device__ __forceinline__ int64_t key_row(const IdxParams& P, int b, int s) {
@@ -102,28 +125,39 @@ struct __align__(8) Bars {
   uint64_t tfull[2], tempty[2];
 };
 
-template <int HI>
-__global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P) {
+template <int HI, int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ IdxParams P, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int d_I = P.d_I;
+  constexpr int d_I = DI;
   const int N = P.N;
-  const uint32_t tile8_bytes = kTileKeys * d_I;        // int8 tile
-  const uint32_t tile16_bytes = kTileKeys * d_I * 2;   // f16 swizzled tile
+  constexpr uint32_t tile8_bytes = kTileKeys * DI;     // int8 tile (TMA-swizzled)
   uint8_t* s8 = smem;                                  // [kStages8][tile8]
-  uint8_t* s16 = s8 + kStages8 * tile8_bytes;          // [kStages16][tile16]
-  uint8_t* sQ = s16 + kStages16 * tile16_bytes;        // [d_I/64 atoms][N rows][128 B]
+  uint8_t* sQ = s8 + kStages8 * tile8_bytes;           // [d_I/64 atoms][N rows][128 B]
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float coef[kCoef];
   __shared__ int tok_pos[kMaxG];
+  __shared__ int tiles_prefix[kMaxGroupsScheduled + 1];
+  __shared__ int scan_tmp[kThreads / 32];
+  // Per-token histogram of each visible score's leading 12 key bits (groups
+  // of at most two tokens, H_I >= 64); flushed to global memory at every
+  // group change so the top-k pass can find its threshold digit at once.
+  constexpr bool kHist = HI >= 64;
+  __shared__ uint32_t hist_s[kHist ? 2 * kHistBins : 1];
+  if (kHist)
+    for (int i = threadIdx.x; i < 2 * kHistBins; i += kThreads) hist_s[i] = 0;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Accumulator buffers start on 32-column boundaries so that every 32-column
   // load stays inside its own buffer.
+  // TMEM: two fp32 accumulators, then two f16 key tiles (DI/2 columns each).
   const int acc_stride = (N + 31) & ~31;
-  const uint32_t tmem_cols = (2 * acc_stride <= 64) ? 64 : (2 * acc_stride <= 128) ? 128 : (2 * acc_stride <= 256) ? 256 : 512;
+  const uint32_t a_col0 = 2 * acc_stride;
+  const int need_cols = 2 * acc_stride + DI;
+  const uint32_t tmem_cols = need_cols <= 64 ? 64 : need_cols <= 128 ? 128 : need_cols <= 256 ? 256 : 512;
 
   if (tid == 0) {
     for (int i = 0; i < kStages8; ++i) { mbar_init(&bars.full8[i], 1); mbar_init(&bars.empty8[i], 4); }
@@ -143,38 +177,74 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
   const uint32_t tmem = tmem_base;
   volatile int* abort_v = &abort_flag;
 
-  int g_cache = -1, maxpos_cache = -1;
+  // Per-group tile counts and their exclusive prefix (block-wide scan).
+  {
+    const int ng = P.n_groups;
+    const int per = (ng + kThreads - 1) / kThreads;
+    const int g0 = min(ng, tid * per), g1 = min(ng, g0 + per);
+    int local = 0;
+    for (int g = g0; g < g1; ++g) local += group_tiles(P, g);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) scan_tmp[warp] = incl;
+    __syncthreads();
+    int woff = 0;
+    for (int w2 = 0; w2 < warp; ++w2) woff += scan_tmp[w2];
+    int run = woff + incl - local;
+    for (int g = g0; g < g1; ++g) {
+      tiles_prefix[g] = run;
+      run += group_tiles(P, g);
+    }
+    if (tid == kThreads - 1) tiles_prefix[ng] = run;
+    __syncthreads();
+  }
+  const int total_items = tiles_prefix[P.n_groups];
+  const int item_lo = static_cast<int>((static_cast<long long>(total_items) * blockIdx.x) / gridDim.x);
+  const int item_hi = static_cast<int>((static_cast<long long>(total_items) * (blockIdx.x + 1)) / gridDim.x);
+  // First (group, tile) of this CTA's share: binary search in the prefix.
+  Walker w0{0, 0, item_hi - item_lo};
+  {
+    int lo = 0, hi = P.n_groups;  // largest g with tiles_prefix[g] <= item_lo
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tiles_prefix[mid] <= item_lo) lo = mid; else hi = mid;
+    }
+    while (lo < P.n_groups && tiles_prefix[lo + 1] <= item_lo) ++lo;
+    w0.g = lo;
+    w0.j = item_lo - tiles_prefix[lo];
+  }
+
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0;
-      for (int i = next_item(P, blockIdx.x, g_cache, maxpos_cache); i < P.n_groups * P.n_tiles;
-           i = next_item(P, i + gridDim.x, g_cache, maxpos_cache)) {
-        const int g = i / P.n_tiles, j = i % P.n_tiles;
+      int cur_g = -1, maxpos_cache = -1;
+      Walker w = w0;
+      for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w)) {
+        const int g = w.g, j = w.j;
         const int b = g / P.groups_per_seq;
+        if (g != cur_g) { cur_g = g; maxpos_cache = group_of(P, g).maxpos; }
         if (!mbar_wait(&bars.empty8[st], ph ^ 1, P.err, abort_v)) break;
         uint8_t* dst = s8 + st * tile8_bytes;
         const int s0 = j * kTileKeys;
-        if (P.block_table == nullptr) {
-          mbar_arrive_expect_tx(&bars.full8[st], tile8_bytes);
-          bulk_g2s(dst, P.k_cache + (static_cast<int64_t>(b) * P.max_L + s0) * d_I, tile8_bytes, &bars.full8[st]);
-        } else {
-          const int bs = P.block_size;
-          const int span = bs < kTileKeys ? bs : kTileKeys;  // keys per copy
-          int64_t rows[kTileKeys / 8];
-          uint32_t bytes = 0;
-          int n_copies = 0;
-          for (int k = 0; k < kTileKeys && s0 + k <= maxpos_cache; k += span) {
-            const int64_t row = key_row(P, b, s0 + k);
-            rows[n_copies++] = row;
-            if (row >= 0) bytes += span * d_I;
-            else atomicOr(P.err, kErrBadIndex);
-          }
-          mbar_arrive_expect_tx(&bars.full8[st], bytes);
-          for (int c = 0; c < n_copies; ++c)
-            if (rows[c] >= 0) bulk_g2s(dst + c * span * d_I, P.k_cache + rows[c] * d_I, span * d_I, &bars.full8[st]);
+        const int bh = P.box_rows;  // 128 (contiguous) or the page size (< 128)
+        int ys[kTileKeys / 8];
+        int n_loads = 0;
+        for (int k = 0; k < kTileKeys && s0 + k <= maxpos_cache; k += bh) {
+          const int64_t row = key_row(P, b, s0 + k);
+          if (row < 0) { atomicOr(P.err, kErrBadIndex); ys[n_loads++] = -1; continue; }
+          ys[n_loads++] = static_cast<int>(row);
         }
+        uint32_t bytes = 0;
+        for (int c = 0; c < n_loads; ++c) bytes += ys[c] >= 0 ? static_cast<uint32_t>(bh * DI) : 0u;
+        mbar_arrive_expect_tx(&bars.full8[st], bytes);
+        for (int c = 0; c < n_loads; ++c)
+          if (ys[c] >= 0) tma_load_2d(dst + c * bh * DI, &tmap, 0, ys[c], &bars.full8[st]);
         if (++st == kStages8) { st = 0; ph ^= 1; }
       }
     }
@@ -186,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
     int cur_g = -1;
     bool first_group = true;
     const int chunks = d_I / 16;  // 16-byte int8 chunks per row
-    for (int i = next_item(P, blockIdx.x, g_cache, maxpos_cache); i < P.n_groups * P.n_tiles;
-         i = next_item(P, i + gridDim.x, g_cache, maxpos_cache)) {
-      const int g = i / P.n_tiles;
+    Walker w = w0;
+    for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w)) {
+      const int g = w.g;
       if (g != cur_g) {
         cur_g = g;
         if (!first_group && !mbar_wait(&bars.qempty, qph, P.err, abort_v)) break;
@@ -219,22 +289,36 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
       }
       if (!mbar_wait(&bars.full8[st8], ph8, P.err, abort_v)) break;
       if (!mbar_wait(&bars.empty16[st16], ph16 ^ 1, P.err, abort_v)) break;
-      const uint8_t* src = s8 + st8 * tile8_bytes;
-      uint8_t* dst = s16 + st16 * tile16_bytes;
-      for (int task = ct; task < kTileKeys * chunks; task += 128) {
-        const int r = task / chunks, c = task % chunks;
-        const uint4 v = *reinterpret_cast<const uint4*>(src + r * d_I + c * 16);
-        uint32_t f[8];
-        i8x4_to_f16x4(v.x, f[0], f[1]);
-        i8x4_to_f16x4(v.y, f[2], f[3]);
-        i8x4_to_f16x4(v.z, f[4], f[5]);
-        i8x4_to_f16x4(v.w, f[6], f[7]);
-        uint8_t* atom = dst + (c / 4) * (kTileKeys * 128);
-        const int cc = (c % 4) * 2;
-        *reinterpret_cast<uint4*>(atom + sw128_off(r, cc)) = make_uint4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<uint4*>(atom + sw128_off(r, cc + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+      tc_fence_after();
+      {
+        // This thread's key row: TMA swizzle (16-byte chunk c of row r sits
+        // at chunk c ^ (r & 7) for 128-byte rows, c ^ ((r >> 1) & 3) for
+        // 64-byte rows), so a quarter warp reads 8 distinct bank groups.
+        const int r = ct;
+        const uint8_t* tile = s8 + st8 * tile8_bytes;
+        constexpr uint32_t kSwMask = DI == 128 ? 7u : 3u;
+        uint32_t f[DI / 2];
+#pragma unroll
+        for (int c = 0; c < DI / 16; ++c) {
+          uint32_t off = static_cast<uint32_t>(r * DI + c * 16);
+          off ^= ((off >> 7) & kSwMask) << 4;
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + off);
+          i8x4_to_f16x4(v.x, f[8 * c + 0], f[8 * c + 1]);
+          i8x4_to_f16x4(v.y, f[8 * c + 2], f[8 * c + 3]);
+          i8x4_to_f16x4(v.z, f[8 * c + 4], f[8 * c + 5]);
+          i8x4_to_f16x4(v.w, f[8 * c + 6], f[8 * c + 7]);
+        }
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + a_col0 + st16 * (DI / 2);
+#pragma unroll
+        for (int c0 = 0; c0 < DI / 2; c0 += 32) {
+          uint32_t rr[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) rr[k] = f[c0 + k];
+          tmem_st32(lane_base + c0, rr);
+        }
+        tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars.full16[st16]);
@@ -250,11 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
       int st16 = 0, acc = 0;
       uint32_t ph16 = 0, qph = 0, aph = 0;
       int cur_g = -1;
-      const int n_items = P.n_groups * P.n_tiles;
-      int i = next_item(P, blockIdx.x, g_cache, maxpos_cache);
-      while (i < n_items) {
-        const int g = i / P.n_tiles;
-        const int nxt = next_item(P, i + gridDim.x, g_cache, maxpos_cache);
+      Walker w = w0;
+      for (bool more = w.left > 0; more;) {
+        const int g = w.g;
+        more = walk_next(tiles_prefix, P.n_groups, w);
         if (g != cur_g) {
           cur_g = g;
           if (!mbar_wait(&bars.qfull, qph, P.err, abort_v)) break;
@@ -263,21 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
         if (!mbar_wait(&bars.full16[st16], ph16, P.err, abort_v)) break;
         if (!mbar_wait(&bars.tempty[acc], aph ^ 1, P.err, abort_v)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(s16 + st16 * tile16_bytes);
+        const uint32_t a_tmem = tmem + a_col0 + st16 * (DI / 2);
         const uint32_t b_base = smem_u32(sQ);
         const uint32_t d_tmem = tmem + acc * acc_stride;
-        for (int kk = 0; kk < d_I / 16; ++kk) {
-          const uint64_t ad = smem_desc(a_base + (kk / 4) * (kTileKeys * 128) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int kk = 0; kk < DI / 16; ++kk) {
           const uint64_t bd = smem_desc(b_base + (kk / 4) * (N * 128) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
-          mma_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          mma_ts(d_tmem, a_tmem + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.empty16[st16]);
         mma_commit(&bars.tfull[acc]);
-        const bool group_ends = (nxt >= n_items) || (nxt / P.n_tiles != g);
+        const bool group_ends = !more || w.g != g;
         if (group_ends) mma_commit(&bars.qempty);
         if (++st16 == kStages16) { st16 = 0; ph16 ^= 1; }
         if (++acc == 2) { acc = 0; aph ^= 1; }
-        i = nxt;
       }
     }
   } else if (warp < 4) {
@@ -287,10 +369,47 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
     int cur_g = -1;
     Group G{};
     const int r = warp * 32 + lane;  // key within the tile = TMEM lane
-    for (int i = next_item(P, blockIdx.x, g_cache, maxpos_cache); i < P.n_groups * P.n_tiles;
-         i = next_item(P, i + gridDim.x, g_cache, maxpos_cache)) {
-      const int g = i / P.n_tiles, j = i % P.n_tiles;
+    const float ninf = -__int_as_float(0x7f800000);
+    // ks of the key this thread scores in a given item (0 past the group's
+    // last visible key); loaded one item ahead to hide its latency.  The
+    // group's (b, maxpos) are re-derived only when the walk enters a new
+    // group, so no per-tile branch waits on a global load.
+    Group Gload{};
+    int gload = -1;
+    auto load_ks = [&](const Walker& it) -> float {
+      if (it.g != gload) {
+        gload = it.g;
+        Gload = group_of(P, it.g);
+      }
+      const int sx = it.j * kTileKeys + r;
+      if (sx > Gload.maxpos) return 0.f;
+      const int64_t row = key_row(P, Gload.b, sx);
+      return row >= 0 ? __half2float(__ldg(P.k_scale + row)) : 0.f;
+    };
+    const bool do_hist = kHist && P.hist != nullptr;
+    auto flush_hist = [&]() {  // G is the group whose counts are flushed
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int gi = 0; gi < G.ntok && gi < 2; ++gi)
+        for (int bin = tid; bin < kHistBins; bin += 128) {
+          const uint32_t v = hist_s[gi * kHistBins + bin];
+          if (v) {
+            atomicAdd(P.hist + static_cast<size_t>(G.t0 + gi) * kHistBins + bin, v);
+            hist_s[gi * kHistBins + bin] = 0;
+          }
+        }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    };
+    Walker w = w0;
+    bool more = w.left > 0;
+    float ks_next = more ? load_ks(w) : 0.f;
+    while (more) {
+      const int g = w.g, j = w.j;
+      const float ks = ks_next;
+      Walker wn = w;
+      const bool more_n = walk_next(tiles_prefix, P.n_groups, wn);
+      if (more_n) ks_next = load_ks(wn);
       if (g != cur_g) {
+        if (do_hist && cur_g >= 0) flush_hist();
         cur_g = g;
         G = group_of(P, g);
         asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -310,27 +429,41 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
       if (!mbar_wait(&bars.tfull[acc], aph, P.err, abort_v)) break;
       tc_fence_after();
       const int s = j * kTileKeys + r;
-      float ks = 0.f;
-      if (s <= G.maxpos) {
-        const int64_t row = key_row(P, G.b, s);
-        if (row >= 0) ks = __half2float(__ldg(P.k_scale + row));
-      }
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * acc_stride;
-      const float ninf = -__int_as_float(0x7f800000);
       // Column n = gi * HI + h of the accumulator is token gi, head h.
       if (HI >= 32) {
         for (int gi = 0; gi < G.ntok; ++gi) {
-          float sacc = 0.f;
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < HI / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(lane_addr + gi * HI + c * 32, v);
+          for (int c = 0; c < HI / 32; c += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(lane_addr + gi * HI + c * 32, v0);
+            if (c + 1 < HI / 32) tmem_ld32(lane_addr + gi * HI + (c + 1) * 32, v1);
             tmem_ld_wait();
+            if (gi == G.ntok - 1 && c + 2 >= HI / 32) {  // last columns read: free the buffer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars.tempty[acc]);
+            }
             const float* cf = coef + gi * HI + c * 32;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) sacc = fmaf(cf[k], fmaxf(__uint_as_float(v[k]), 0.f), sacc);
+            for (int k = 0; k < 32; ++k) part[k & 3] = fmaf(cf[k], fmaxf(__uint_as_float(v0[k]), 0.f), part[k & 3]);
+            if (c + 1 < HI / 32) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                part[k & 3] = fmaf(cf[32 + k], fmaxf(__uint_as_float(v1[k]), 0.f), part[k & 3]);
+            }
           }
-          P.scores[static_cast<size_t>(G.t0 + gi) * P.ld + s] = (s <= tok_pos[gi]) ? sacc * ks : ninf;
+          const float sacc = (part[0] + part[1]) + (part[2] + part[3]);
+          const bool vis = s <= tok_pos[gi];
+          const float val = vis ? sacc * ks : ninf;
+          P.scores[static_cast<size_t>(G.t0 + gi) * P.ld + s] = val;
+          if (kHist && do_hist && vis && gi < 2) atomicAdd(&hist_s[gi * kHistBins + (order_key(val) >> 20)], 1u);
+        }
+        if (G.ntok == 0) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.tempty[acc]);
         }
       } else {
         constexpr int kTokPerChunk = HI >= 32 ? 1 : 32 / HI;
@@ -339,23 +472,34 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const IdxParams P)
           uint32_t v[32];
           tmem_ld32(lane_addr + cc * 32, v);
           tmem_ld_wait();
+          if (cc == n_chunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.tempty[acc]);
+          }
 #pragma unroll
           for (int u = 0; u < kTokPerChunk; ++u) {
             const int gi = cc * kTokPerChunk + u;
-            float sacc = 0.f;
+            float part[2] = {0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < HI; ++k)
-              sacc = fmaf(coef[cc * 32 + u * HI + k], fmaxf(__uint_as_float(v[u * HI + k]), 0.f), sacc);
+              part[k & 1] = fmaf(coef[cc * 32 + u * HI + k], fmaxf(__uint_as_float(v[u * HI + k]), 0.f), part[k & 1]);
             if (gi < G.ntok)
-              P.scores[static_cast<size_t>(G.t0 + gi) * P.ld + s] = (s <= tok_pos[gi]) ? sacc * ks : ninf;
+              P.scores[static_cast<size_t>(G.t0 + gi) * P.ld + s] =
+                  (s <= tok_pos[gi]) ? (part[0] + part[1]) * ks : ninf;
           }
         }
+        if (n_chunks == 0) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.tempty[acc]);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.tempty[acc]);
       if (++acc == 2) { acc = 0; aph ^= 1; }
+      w = wn;
+      more = more_n;
     }
+    if (do_hist && cur_g >= 0 && !*abort_v) flush_hist();
   }
   tc_fence_before();
   __syncthreads();
@@ -380,7 +524,7 @@ __global__ void dots_kernel(const IdxParams P, int32_t* dots) {
   }
 }
 
-IdxParams make_params(const dsa_topk_args& a, float* scores, int64_t ld) {
+IdxParams make_params(const dsa_topk_args& a, float* scores, int64_t ld, uint32_t* hist) {
   IdxParams P{};
   P.T = a.T; P.n_q = a.n_q; P.H_I = a.H_I; P.d_I = a.d_I; P.max_L = a.max_L;
   P.G = a.H_I >= 128 ? 1 : (128 / a.H_I < a.n_q ? 128 / a.H_I : a.n_q);
@@ -392,16 +536,15 @@ IdxParams make_params(const dsa_topk_args& a, float* scores, int64_t ld) {
   P.q = a.q; P.q_scale = reinterpret_cast<const __half*>(a.q_scale); P.w = a.w;
   P.k_cache = a.k_cache; P.k_scale = reinterpret_cast<const __half*>(a.k_scale);
   P.block_table = a.block_table; P.block_size = a.block_size; P.max_blocks = a.max_blocks;
-  P.pos = a.pos; P.scores = scores; P.ld = ld;
+  P.pos = a.pos; P.scores = scores; P.ld = ld; P.hist = hist;
   P.err = error_word();
   return P;
 }
 
-template <int HI>
-cudaError_t launch_hi(const IdxParams& P, cudaStream_t s) {
-  const size_t smem = 1024 + static_cast<size_t>(kStages8) * kTileKeys * P.d_I +
-                      static_cast<size_t>(kStages16) * kTileKeys * P.d_I * 2 + static_cast<size_t>(P.N) * P.d_I * 2;
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int HI, int DI>
+cudaError_t launch_hi(const IdxParams& P, const CUtensorMap& tmap, cudaStream_t s) {
+  const size_t smem = 1024 + static_cast<size_t>(kStages8) * kTileKeys * DI + static_cast<size_t>(P.N) * DI * 2;
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(P.n_groups) * P.n_tiles;
   const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
@@ -415,29 +558,41 @@ cudaError_t launch_hi(const IdxParams& P, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, indexer_kernel<HI>, P);
+  return cudaLaunchKernelEx(&cfg, indexer_kernel<HI, DI>, P, tmap);
+}
+
+template <int DI>
+cudaError_t launch_di(int H_I, const IdxParams& P, const CUtensorMap& tmap, cudaStream_t s) {
+  switch (H_I) {
+    case 4: return launch_hi<4, DI>(P, tmap, s);
+    case 8: return launch_hi<8, DI>(P, tmap, s);
+    case 16: return launch_hi<16, DI>(P, tmap, s);
+    case 32: return launch_hi<32, DI>(P, tmap, s);
+    case 64: return launch_hi<64, DI>(P, tmap, s);
+    default: return launch_hi<128, DI>(P, tmap, s);
+  }
 }
 
 }  // namespace
 
-int launch_indexer(const dsa_topk_args& a, float* scores, cudaStream_t s) {
-  const IdxParams P = make_params(a, scores, a.max_L);
+int launch_indexer(const dsa_topk_args& a, float* scores, uint32_t* hist, cudaStream_t s) {
+  IdxParams P = make_params(a, scores, a.max_L, hist);
   if (!P.err) return DSA_ERR_CUDA;
-  cudaError_t e;
-  switch (a.H_I) {
-    case 4: e = launch_hi<4>(P, s); break;
-    case 8: e = launch_hi<8>(P, s); break;
-    case 16: e = launch_hi<16>(P, s); break;
-    case 32: e = launch_hi<32>(P, s); break;
-    case 64: e = launch_hi<64>(P, s); break;
-    case 128: e = launch_hi<128>(P, s); break;
-    default: return DSA_ERR_UNSUPPORTED;
-  }
+  if (P.n_groups > kMaxGroupsScheduled) return DSA_ERR_UNSUPPORTED;
+  if (a.H_I != 4 && a.H_I != 8 && a.H_I != 16 && a.H_I != 32 && a.H_I != 64 && a.H_I != 128)
+    return DSA_ERR_UNSUPPORTED;
+  // One TMA box is a whole 128-key tile of a contiguous cache, or one page.
+  P.box_rows = a.block_table ? (a.block_size < kTileKeys ? a.block_size : kTileKeys) : kTileKeys;
+  const uint64_t rows = a.block_table ? (1ull << 31) - 1 : static_cast<uint64_t>(a.B) * a.max_L;
+  alignas(64) CUtensorMap tmap;
+  if (!encode_tmap_u8_2d(&tmap, a.k_cache, a.d_I, rows, a.d_I, P.box_rows, a.d_I == 128 ? 128 : 64))
+    return DSA_ERR_CUDA;
+  const cudaError_t e = a.d_I == 128 ? launch_di<128>(a.H_I, P, tmap, s) : launch_di<64>(a.H_I, P, tmap, s);
   return cuda_status(e);
 }
 
 int launch_indexer_dots(const dsa_topk_args& a, int32_t* dots, cudaStream_t s) {
-  const IdxParams P = make_params(a, nullptr, a.max_L);
+  const IdxParams P = make_params(a, nullptr, a.max_L, nullptr);
   dim3 grid((a.max_L + 127) / 128, a.T);
   dots_kernel<<<grid, 128, 0, s>>>(P, dots);
   return cuda_status(cudaGetLastError());

@@ -4,21 +4,24 @@
 //
 // [V3.2-PyPTO §Indexer Prolog] gives the three formulas and observes that
 // the q stream (an (8,1536)x(1536,8192) int8 GEMM) dominates and is bound by
-// weight traffic.  At T <= 32 tokens every output channel is a 1536-long dot
+// weight traffic.  At T <= 32 tokens every output channel is a K_q-long dot
 // against <= 32 activation rows: the work is a weight stream, not a GEMM
-// that tensor cores would speed up, so it runs as dp4a over shared-memory
-// tiles filled by bulk async copies, spread over every SM:
+// that tensor cores would shorten, so it runs as dp4a over shared-memory
+// slabs filled by bulk async copies, one CTA per SM, in a single wave:
 //
-//   * q stream: a cluster of 4 CTAs per head splits K_q in 4; each CTA
-//     streams its [d_I x K_q/4] weight slab into shared memory with
-//     cp.async.bulk, computes int32 partial dots, and the cluster sums the
-//     4 partials through distributed shared memory.  Each CTA then finishes
-//     the tokens t = rank (mod 4): dequant -> RoPE -> 128-point Hadamard
-//     (warp butterfly over shuffles) -> int8 quantisation.
-//   * k / weight streams: 2 output channels per CTA over the full D_x; the
-//     fp32 results go to the workspace and the last CTA to finish (atomic
-//     ticket) runs LayerNorm -> RoPE -> Hadamard -> quantisation and writes
-//     the key-cache rows and the weights.
+//   * q stream: a cluster of 2 CTAs per head splits K_q in two; each CTA
+//     streams its [d_I x K_q/2] weight slab (96 KB at the decode shape) with
+//     cp.async.bulk, computes int32 partial dots, and the pair sums its
+//     partials through distributed shared memory.  Each CTA then finishes
+//     the tokens t = rank (mod 2): dequant -> RoPE -> Hadamard (warp
+//     butterfly over shuffles) -> int8 quantisation.
+//   * k / weight streams: CTAs of 8 output channels over the full D_x (the
+//     8 weight rows are bulk-copied into shared memory); fp32 results go to
+//     the workspace and the last CTA to finish (atomic ticket) runs
+//     LayerNorm -> RoPE -> Hadamard -> quantisation, writes the key-cache
+//     rows and the weights.
+// Every scale, RoPE row, gamma/beta and position an epilogue needs is
+// prefetched into shared memory while the weight slabs are in flight.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -29,12 +32,13 @@ namespace dsa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kQSplit = 4;  // cluster size and K_q split of the q stream
-constexpr int kKwChannels = 2;
+constexpr int kQSplit = 2;       // cluster size and K_q split of the q stream
+constexpr int kKwChannels = 8;   // output channels per k/weight CTA
 constexpr int kMaxT = 32;
+constexpr int kMaxRope = 64;     // max d_rope / 2 entries per RoPE row
 
 struct PrologParams {
-  int T, H_I, d_I, d_rope, K_q, D_x, rope_max_pos, interleaved, n_q_ctas, n_kw_ctas, n_kw_channels;
+  int T, H_I, d_I, d_rope, K_q, D_x, interleaved, n_q_ctas, n_kw_ctas, n_kw_channels;
   const int8_t* q_lora;
   const __half* q_lora_scale;
   const int8_t* w_qb;
@@ -61,6 +65,17 @@ struct PrologParams {
   uint32_t* err;
 };
 
+// Small per-CTA tables filled before the big wait.
+struct Pre {
+  float cos_t[kMaxT][kMaxRope];
+  float sin_t[kMaxT][kMaxRope];
+  float sa[kMaxT];
+  float sb[128];
+  float gamma[128];
+  float beta[128];
+  int64_t slot[kMaxT];
+};
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -72,16 +87,25 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// RoPE rows of the tokens (d_rope/2 cos and sin each) into shared memory.
+__device__ __forceinline__ void prefetch_rope(const PrologParams& P, Pre& pre, int tid) {
+  const int half = P.d_rope / 2;
+  for (int i = tid; i < P.T * half; i += kThreads) {
+    const int t = i / half, c = i % half;
+    const size_t off = static_cast<size_t>(__ldg(P.pos + t)) * half + c;
+    pre.cos_t[t][c] = __ldg(P.rope_cos + off);
+    pre.sin_t[t][c] = __ldg(P.rope_sin + off);
+  }
+}
+
 // One warp holds one d_I = 32*DPL row, lane l owning dims l*DPL .. l*DPL+DPL-1.
-// Applies RoPE (table row `p`), the scaled Sylvester Hadamard transform and
-// the int8 quantisation; returns the codes in c[] and the fp16 scale.
+// Applies RoPE (the token's cos/sin rows), the scaled Sylvester Hadamard
+// transform and the int8 quantisation; returns the codes and the fp16 scale.
 template <int DPL>
-__device__ __forceinline__ void rope_hadamard_quant(float (&v)[DPL], int lane, int p, const float* cos_t,
-                                                    const float* sin_t, int d_rope, int interleaved,
+__device__ __forceinline__ void rope_hadamard_quant(float (&v)[DPL], int lane, const float* crow,
+                                                    const float* srow, int d_rope, int interleaved,
                                                     int (&c)[DPL], __half& scale16) {
   const int half = d_rope / 2;
-  const float* crow = cos_t + static_cast<size_t>(p) * half;
-  const float* srow = sin_t + static_cast<size_t>(p) * half;
   if (interleaved) {
 #pragma unroll
     for (int j = 0; j < DPL; j += 2) {
@@ -165,16 +189,16 @@ __device__ __forceinline__ void store_codes(int8_t* dst, const int (&c)[DPL]) {
 }
 
 // ---------------------------------------------------------------- q stream
-template <int DPL>
-__device__ void q_stream(const PrologParams& P, uint8_t* smem) {
+template <int DPL, int TM>
+__device__ void q_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
   constexpr int D = 32 * DPL;           // d_I
   constexpr int TG = kThreads / D;      // token groups per channel
-  constexpr int TPT = kMaxT / TG;       // max tokens per thread
+  constexpr int TPT = TM / TG;          // tokens per thread (rows >= T are zero)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int head = blockIdx.x / kQSplit;
   const uint32_t rank = cluster_ctarank();
   const int kchunk = P.K_q / kQSplit;
-  const int wstride = kchunk + 16;
+  const int wstride = kchunk + 16;  // padded rows: conflict-free 16-byte reads
   const int T = P.T;
 
   uint8_t* sW = smem;                                   // [D][wstride]
@@ -189,6 +213,7 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem) {
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_launch_dependents();
   griddep_wait();
   if (warp == 0) {
     const uint32_t bytes = static_cast<uint32_t>((D + T) * kchunk);
@@ -199,7 +224,16 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem) {
     const int8_t* qsrc = P.q_lora + rank * kchunk;
     for (int t = lane; t < T; t += 32) bulk_g2s(sQ + t * kchunk, qsrc + static_cast<size_t>(t) * P.K_q, kchunk, &bar);
   }
+  // rows T..TM-1 of the activation slab are zero so that the dot loop
+  // below runs without per-token branches
+  for (int i = tid; i < (TM - T) * kchunk / 16; i += kThreads)
+    reinterpret_cast<int4*>(sQ + T * kchunk)[i] = make_int4(0, 0, 0, 0);
+  // epilogue inputs, while the slabs are in flight
+  if (tid < D) pre.sb[tid] = __half2float(__ldg(P.w_qb_scale + head * D + tid));
+  if (tid >= D && tid - D < T) pre.sa[tid - D] = __half2float(__ldg(P.q_lora_scale + (tid - D)));
+  prefetch_rope(P, pre, tid);
   mbar_wait(&bar, 0, P.err, &abort_flag);
+  __syncthreads();  // zero rows and prefetched tables written by other threads
 
   // int32 partial dots over this CTA's K_q slice.
   const int n = tid % D, tg = tid / D;
@@ -207,18 +241,19 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem) {
 #pragma unroll
   for (int i = 0; i < TPT; ++i) acc[i] = 0;
   const uint8_t* wrow = sW + n * wstride;
+  const uint8_t* qcol = sQ + tg * kchunk;
+#pragma unroll 2
   for (int k = 0; k < kchunk; k += 16) {
     const int4 w = *reinterpret_cast<const int4*>(wrow + k);
+    int4 q[TPT];
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) q[i] = *reinterpret_cast<const int4*>(qcol + i * TG * kchunk + k);
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
-      const int t = tg + i * TG;
-      if (t < T) {
-        const int4 q = *reinterpret_cast<const int4*>(sQ + t * kchunk + k);
-        acc[i] = __dp4a(w.x, q.x, acc[i]);
-        acc[i] = __dp4a(w.y, q.y, acc[i]);
-        acc[i] = __dp4a(w.z, q.z, acc[i]);
-        acc[i] = __dp4a(w.w, q.w, acc[i]);
-      }
+      acc[i] = __dp4a(w.x, q[i].x, acc[i]);
+      acc[i] = __dp4a(w.y, q[i].y, acc[i]);
+      acc[i] = __dp4a(w.z, q[i].z, acc[i]);
+      acc[i] = __dp4a(w.w, q[i].w, acc[i]);
     }
   }
 #pragma unroll
@@ -228,77 +263,118 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem) {
   }
   cluster_sync();
 
-  // Tokens t = rank (mod kQSplit): sum the cluster's partials, then the
+  // Tokens t = rank (mod kQSplit): sum the pair's partials, then the
   // dequant -> RoPE -> Hadamard -> quant epilogue, one warp per token.
   for (int t = rank + kQSplit * warp; t < T; t += kQSplit * (kThreads / 32)) {
     float v[DPL];
-    const float sa = __half2float(P.q_lora_scale[t]);
+    const float sa = pre.sa[t];
+    uint32_t pv[kQSplit][DPL];
+#pragma unroll
+    for (int r = 0; r < kQSplit; ++r)
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) pv[r][j] = ld_cluster_u32(mapa(smem_u32(&sPart[t * D + lane * DPL + j]), r));
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
-      const int d = lane * DPL + j;
-      const uint32_t local = smem_u32(&sPart[t * D + d]);
       int s = 0;
 #pragma unroll
-      for (int r = 0; r < kQSplit; ++r) s += static_cast<int>(ld_cluster_u32(mapa(local, r)));
-      const float sb = __half2float(P.w_qb_scale[head * D + d]);
-      v[j] = (static_cast<float>(s) * sa) * sb;
+      for (int r = 0; r < kQSplit; ++r) s += static_cast<int>(pv[r][j]);
+      v[j] = (static_cast<float>(s) * sa) * pre.sb[lane * DPL + j];
     }
     int c[DPL];
     __half s16;
-    rope_hadamard_quant<DPL>(v, lane, P.pos[t], P.rope_cos, P.rope_sin, P.d_rope, P.interleaved, c, s16);
+    rope_hadamard_quant<DPL>(v, lane, pre.cos_t[t], pre.sin_t[t], P.d_rope, P.interleaved, c, s16);
     store_codes<DPL>(P.q_out + (static_cast<size_t>(t) * P.H_I + head) * D + lane * DPL, c);
     if (lane == 0) P.q_scale_out[t * P.H_I + head] = s16;
   }
-  cluster_sync();  // peers may still read this CTA's partials
+  cluster_sync();  // the peer may still read this CTA's partials
 }
 
 // ------------------------------------------------------- k / weight stream
 template <int DPL>
-__device__ void kw_stream(const PrologParams& P) {
+__device__ void kw_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
   constexpr int D = 32 * DPL;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x - P.n_q_ctas;
-  if (cta >= P.n_kw_ctas) return;
+  if (cta >= P.n_kw_ctas) {  // padding CTA of the last cluster
+    griddep_launch_dependents();
+    return;
+  }
   const int T = P.T;
   const int c0 = cta * kKwChannels;
-  __shared__ float red[kThreads / 32][kMaxT * kKwChannels];
+  const int nch = min(kKwChannels, P.n_kw_channels - c0);
+  const size_t row_bytes = static_cast<size_t>(P.D_x) * 2;
+  __nv_bfloat16* sWk = reinterpret_cast<__nv_bfloat16*>(smem);  // [nch][D_x]
+  __shared__ float red[kThreads / 32][8 * kKwChannels];
   __shared__ bool is_last;
-  griddep_wait();
-
-  float acc[kMaxT][kKwChannels];
-#pragma unroll
-  for (int t = 0; t < kMaxT; ++t)
-#pragma unroll
-    for (int c = 0; c < kKwChannels; ++c) acc[t][c] = 0.f;
-
-  const __nv_bfloat16* wrow[kKwChannels];
-  bool cvalid[kKwChannels];
-#pragma unroll
-  for (int c = 0; c < kKwChannels; ++c) {
-    const int ch = c0 + c;
-    cvalid[c] = ch < P.n_kw_channels;
-    const int chc = cvalid[c] ? ch : 0;
-    wrow[c] = (chc < D) ? P.w_k + static_cast<size_t>(chc) * P.D_x
-                        : P.w_proj + static_cast<size_t>(chc - D) * P.D_x;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
   }
-  for (int k = tid * 8; k < P.D_x; k += kThreads * 8) {
-    float wf[kKwChannels][8];
-#pragma unroll
-    for (int c = 0; c < kKwChannels; ++c) {
-      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow[c] + k));
-      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __bfloat1622float2(w2[j]);
-        wf[c][2 * j] = f.x;
-        wf[c][2 * j + 1] = f.y;
-      }
+  __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nch * row_bytes));
+    __syncwarp();
+    for (int c = lane; c < nch; c += 32) {
+      const int ch = c0 + c;
+      const __nv_bfloat16* src = (ch < D) ? P.w_k + static_cast<size_t>(ch) * P.D_x
+                                          : P.w_proj + static_cast<size_t>(ch - D) * P.D_x;
+      bulk_g2s(sWk + static_cast<size_t>(c) * P.D_x, src, static_cast<uint32_t>(row_bytes), &bar);
     }
+  }
+  // inputs of the last CTA's epilogue
+  if (tid < D) {
+    pre.gamma[tid] = __ldg(P.ln_gamma + tid);
+    pre.beta[tid] = __ldg(P.ln_beta + tid);
+  }
+  if (tid >= D && tid - D < T) pre.slot[tid - D] = __ldg(P.slot + (tid - D));
+  prefetch_rope(P, pre, tid);
+
+  mbar_wait(&bar, 0, P.err, &abort_flag);
+  // Tokens in blocks of 8: each thread owns 16-byte column chunks of the
+  // weight rows (read once per block from shared memory) and streams the
+  // matching x chunks of the block's tokens from L2.
+  constexpr int kTB = 8;
+  for (int tb = 0; tb < T; tb += kTB) {
+    float acc[kTB][kKwChannels];
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-      if (t < T) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(P.x + static_cast<size_t>(t) * P.D_x + k));
-        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+    for (int t = 0; t < kTB; ++t)
+#pragma unroll
+      for (int c = 0; c < kKwChannels; ++c) acc[t][c] = 0.f;
+    // x chunks of the block's tokens, one iteration ahead (rows past T repeat
+    // the last row; their sums are discarded)
+    auto load_x = [&](int k, uint4 (&xv)[kTB]) {
+#pragma unroll
+      for (int t = 0; t < kTB; ++t)
+        xv[t] = __ldg(reinterpret_cast<const uint4*>(P.x + static_cast<size_t>(min(tb + t, T - 1)) * P.D_x + k));
+    };
+    uint4 xnext[kTB];
+    if (tid * 8 < P.D_x) load_x(tid * 8, xnext);
+    for (int k = tid * 8; k < P.D_x; k += kThreads * 8) {
+      uint4 xv[kTB];
+#pragma unroll
+      for (int t = 0; t < kTB; ++t) xv[t] = xnext[t];
+      if (k + kThreads * 8 < P.D_x) load_x(k + kThreads * 8, xnext);
+      float wf[kKwChannels][8];
+#pragma unroll
+      for (int c = 0; c < kKwChannels; ++c) {
+        uint4 wv = make_uint4(0, 0, 0, 0);
+        if (c < nch) wv = *reinterpret_cast<const uint4*>(sWk + static_cast<size_t>(c) * P.D_x + k);
+        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(w2[j]);
+          wf[c][2 * j] = f.x;
+          wf[c][2 * j + 1] = f.y;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTB; ++t) {
+        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv[t]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 f = __bfloat1622float2(x2[j]);
@@ -310,25 +386,28 @@ __device__ void kw_stream(const PrologParams& P) {
         }
       }
     }
-  }
-  // Block reduction of every (token, channel) sum.
+    // Block reduction of every (token, channel) sum of this token block.
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) {
-    if (t < T) {
+    for (int t = 0; t < kTB; ++t) {
+      if (tb + t < T) {
 #pragma unroll
-      for (int c = 0; c < kKwChannels; ++c) {
-        const float s = warp_sum(acc[t][c]);
-        if (lane == 0) red[warp][t * kKwChannels + c] = s;
+        for (int c = 0; c < kKwChannels; ++c) {
+          const float sum = warp_sum(acc[t][c]);
+          if (lane == 0) red[warp][t * kKwChannels + c] = sum;
+        }
       }
     }
-  }
-  __syncthreads();
-  for (int i = tid; i < T * kKwChannels; i += kThreads) {
-    float s = 0.f;
+    __syncthreads();
+    for (int i = tid; i < kTB * kKwChannels; i += kThreads) {
+      const int t = i / kKwChannels, c = i % kKwChannels;
+      if (tb + t < T && c < nch) {
+        float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s += red[w][i];
-    const int t = i / kKwChannels, c = i % kKwChannels;
-    if (c0 + c < P.n_kw_channels) P.kw[static_cast<size_t>(t) * P.n_kw_channels + c0 + c] = s;
+        for (int w = 0; w < kThreads / 32; ++w) sum += red[w][i];
+        P.kw[static_cast<size_t>(tb + t) * P.n_kw_channels + c0 + c] = sum;
+      }
+    }
+    __syncthreads();
   }
   __threadfence();
   __syncthreads();
@@ -358,12 +437,12 @@ __device__ void kw_stream(const PrologParams& P) {
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
       const int d = lane * DPL + j;
-      v[j] = (v[j] - mean) * rstd * P.ln_gamma[d] + P.ln_beta[d];
+      v[j] = (v[j] - mean) * rstd * pre.gamma[d] + pre.beta[d];
     }
     int c[DPL];
     __half s16;
-    rope_hadamard_quant<DPL>(v, lane, P.pos[t], P.rope_cos, P.rope_sin, P.d_rope, P.interleaved, c, s16);
-    const int64_t row = P.slot[t];
+    rope_hadamard_quant<DPL>(v, lane, pre.cos_t[t], pre.sin_t[t], P.d_rope, P.interleaved, c, s16);
+    const int64_t row = pre.slot[t];
     if (row >= 0 && row < P.cache_rows) {
       store_codes<DPL>(P.k_cache + row * D + lane * DPL, c);
       if (lane == 0) P.k_scale_cache[row] = s16;
@@ -380,15 +459,15 @@ __device__ void kw_stream(const PrologParams& P) {
   if (tid == 0) *P.ticket = 0u;  // ready for the next call
 }
 
-template <int DPL>
-__global__ void __launch_bounds__(kThreads) prolog_kernel(const PrologParams P) {
+template <int DPL, int TM>
+__global__ void __launch_bounds__(kThreads, 1) prolog_kernel(const PrologParams P) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ Pre pre;
   if (static_cast<int>(blockIdx.x) < P.n_q_ctas) {
-    q_stream<DPL>(P, smem);
+    q_stream<DPL, TM>(P, smem, pre);
   } else {
-    kw_stream<DPL>(P);
+    kw_stream<DPL>(P, smem, pre);
   }
-  griddep_launch_dependents();
 }
 
 }  // namespace
@@ -401,7 +480,7 @@ size_t prolog_workspace(const dsa_prolog_args& a) {
 int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   PrologParams P{};
   P.T = a.T; P.H_I = a.H_I; P.d_I = a.d_I; P.d_rope = a.d_rope; P.K_q = a.K_q; P.D_x = a.D_x;
-  P.rope_max_pos = a.rope_max_pos; P.interleaved = a.rope_interleaved;
+  P.interleaved = a.rope_interleaved;
   P.n_q_ctas = a.H_I * kQSplit;
   P.n_kw_channels = a.d_I + (a.w_proj ? a.H_I : 0);
   P.n_kw_ctas = (P.n_kw_channels + kKwChannels - 1) / kKwChannels;
@@ -421,8 +500,10 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   if (!P.err) return DSA_ERR_CUDA;
 
   const int kchunk = a.K_q / kQSplit;
-  const size_t smem = static_cast<size_t>(a.d_I) * (kchunk + 16) + static_cast<size_t>(kMaxT) * kchunk +
-                      static_cast<size_t>(kMaxT) * a.d_I * 4;
+  const size_t smem_q = static_cast<size_t>(a.d_I) * (kchunk + 16) + static_cast<size_t>(kMaxT) * kchunk +
+                        static_cast<size_t>(kMaxT) * a.d_I * 4;
+  const size_t smem_kw = static_cast<size_t>(kKwChannels) * a.D_x * 2;
+  const size_t smem = smem_q > smem_kw ? smem_q : smem_kw;
   const int grid = P.n_q_ctas + static_cast<int>(round_up(P.n_kw_ctas, kQSplit));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -437,12 +518,15 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
+  auto go = [&](auto kern) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return r == cudaSuccess ? cudaLaunchKernelEx(&cfg, kern, P) : r;
+  };
+  const int tm = a.T <= 8 ? 8 : (a.T <= 16 ? 16 : 32);
   if (a.d_I == 128) {
-    e = cudaFuncSetAttribute(prolog_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, prolog_kernel<4>, P);
+    e = tm == 8 ? go(prolog_kernel<4, 8>) : (tm == 16 ? go(prolog_kernel<4, 16>) : go(prolog_kernel<4, 32>));
   } else {
-    e = cudaFuncSetAttribute(prolog_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, prolog_kernel<2>, P);
+    e = tm == 8 ? go(prolog_kernel<2, 8>) : (tm == 16 ? go(prolog_kernel<2, 16>) : go(prolog_kernel<2, 32>));
   }
   return cuda_status(e);
 }
