@@ -155,23 +155,76 @@ def src_hash(*names) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_file: str, summary: str):
-    """dram read+write bytes per launch from a committed ncu summary, if it
-    was taken on the current source of the kernel."""
-    path = os.path.join(ROOT, "profiles", summary)
-    if not os.path.exists(path):
-        return None
-    vals = {}
-    for line in open(path):
-        if ":" in line:
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_sha256_16") != src_hash(kernel_file):
-        return None
+def profiled_traffic(parts):
+    """Sum over (kernel source, summary) pairs of the dram read+write bytes
+    per launch in each committed ncu summary; None unless every summary
+    exists and was taken on the current source of its kernel."""
+    total = 0.0
+    for kernel_file, summary in parts:
+        path = os.path.join(ROOT, "profiles", summary)
+        if not os.path.exists(path):
+            return None
+        vals = {}
+        for line in open(path):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("source_sha256_16") != src_hash(kernel_file):
+            return None
+        try:
+            total += float(vals["traffic_bytes_per_launch"])
+        except (KeyError, ValueError):
+            return None
+    return total
+
+
+def stage_times_in_graph(stage_fns, stream, flush, reps):
+    """Mean ms of each stage inside one graph of the whole step, from event
+    nodes recorded between the stages.  None if events cannot be captured."""
     try:
-        return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stage_fns) + 1)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            evs[0].record(stream)
+            for i, (_, fn) in enumerate(stage_fns):
+                fn(stream)
+                evs[i + 1].record(stream)
+        acc = [[] for _ in stage_fns]
+        for r in range(reps + 2):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                g.replay()
+            stream.synchronize()
+            if r >= 2:
+                for i in range(len(stage_fns)):
+                    acc[i].append(evs[i].elapsed_time(evs[i + 1]))
+    except (TypeError, RuntimeError):
+        return None, None
+    return ({name: statistics.mean(a) for (name, _), a in zip(stage_fns, acc)},
+            "event nodes between the C calls inside one step graph (L2 flushed before each replay)")
+
+
+def stage_times_separate(stage_fns, stream, flush, reps):
+    """Fallback: each stage in its own graph, replayed alone after a flush."""
+    out = {}
+    for name, fn in stage_fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            fn(stream)
+        t = []
+        for r in range(reps + 2):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            stream.synchronize()
+            if r >= 2:
+                t.append(a.elapsed_time(b))
+        out[name] = statistics.mean(t)
+    return out, "one graph per stage, replayed alone after an L2 flush"
 
 
 def run_ours(args, rank, world, local):
@@ -231,35 +284,23 @@ def run_ours(args, rank, world, local):
     value = tokens_total / (ms_max / 1e3)
     clocks = clk.summary()
 
-    # per-stage event timing (each stage alone after an L2 flush)
-    def time_stage(fn, reps):
-        t = []
-        for _ in range(reps):
-            with torch.cuda.stream(stream):
-                flush.zero_()
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn(stream)
-                b.record(stream)
-            stream.synchronize()
-            t.append(a.elapsed_time(b))
-        return statistics.mean(t)
-
+    # Per-stage times inside the step: a second copy of the step graph with
+    # event nodes at the boundaries of the three C calls (event nodes split
+    # the programmatic-launch overlap, so this copy is not the timed one).
+    stage_fns = [("prolog", lambda s: pro.run(s)), ("indexer+topk", lambda s: buf.run_topk(s)),
+                 ("attention+combine", lambda s: buf.run_attn(s))]
     reps = min(max(K, 5), 50)
-    st_ms = {
-        "prolog": time_stage(lambda s: pro.run(s), reps),
-        "indexer": time_stage(lambda s: B.dsa_indexer_scores(buf.targs, buf.scores, s), reps),
-        "topk": time_stage(lambda s: B.dsa_topk_from_scores(buf.targs, buf.scores, s), reps),
-        "attention+combine": time_stage(lambda s: buf.run_attn(s), reps),
-    }
+    st_ms, stage_timing = stage_times_in_graph(stage_fns, stream, flush, reps)
+    if st_ms is None:
+        st_ms, stage_timing = stage_times_separate(stage_fns, stream, flush, reps)
     idx = buf.topk_idx.cpu().numpy()
     peak, peak_kind = measured_peaks()
-    alg = {"prolog": prolog_bytes(p), "indexer": indexer_bytes(inp), "topk": topk_bytes(inp),
+    alg = {"prolog": prolog_bytes(p), "indexer+topk": indexer_bytes(inp) + topk_bytes(inp),
            "attention+combine": attention_bytes(inp, idx)}
-    dom = max(["prolog", "indexer", "attention+combine"], key=lambda k: st_ms[k])
-    kfile = {"prolog": ("prolog.cu", "prolog_decode64k.txt"), "indexer": ("indexer.cu", "indexer_decode64k.txt"),
-             "attention+combine": ("attention.cu", "attention_decode64k.txt")}[dom]
+    dom = max(alg, key=lambda k: st_ms[k])
+    kfile = {"prolog": [("prolog.cu", "prolog_decode64k.txt")],
+             "indexer+topk": [("indexer.cu", "indexer_decode64k.txt"), ("topk.cu", "topk_decode64k.txt")],
+             "attention+combine": [("attention.cu", "attention_decode64k.txt"), ("attention.cu", "combine_decode64k.txt")]}[dom]
     achieved = alg[dom] / (st_ms[dom] / 1e3) / 1e9
     step_bytes = sum(alg.values())
 
@@ -298,11 +339,12 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes": alg[dom],
-                     "traffic": profiled_traffic(*kfile)},
+                     "traffic": profiled_traffic(kfile)},
         "step_roofline": {"algorithmic_bytes": step_bytes,
                           "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
                           "frac": round(step_bytes / (peak * 1e9) / (ms_max / 1e3), 4)},
         "stages_ms": {k: round(v, 5) for k, v in st_ms.items()},
+        "stages_timing": stage_timing,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d_bytes),
                 "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": K * 5,
@@ -386,7 +428,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-tokens", type=int, default=8)
