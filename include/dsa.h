@@ -174,9 +174,9 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * max_L a multiple of 128; block_size a multiple of 8 that divides 128 or
  * is a multiple of 128.  Workspace: dsa_indexer_topk_workspace() bytes (the
  * fp32 score rows live there when scores_out is NULL, and, for H_I >= 64
- * with at most 512 tokens, per-token score histograms and top-k
- * candidates); it must be zero-filled once before its first use (the
- * library leaves it zeroed).
+ * with at most 512 tokens and max_L <= 131072, per-token score histograms);
+ * it must be zero-filled once before its first use (the library leaves it
+ * zeroed).
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t T, B, n_q, H_I, d_I, topk, max_L;

@@ -460,37 +460,64 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
 
 // Merges the split chunks of every (token, head): out = sum_c w_c O_c /
 // sum_c w_c with w_c = l_c 2^(m_c - M) (O_c already divided by l_c).
+// One warp per (token, head).  Chunks are taken kBatch at a time and every
+// load of a batch (its (m, l) pairs and its 1 KB partial rows) is issued
+// before any of them is used, so a batch costs one memory round trip.  The
+// running maximum is rescaled between batches like the online softmax.
+constexpr int kCombineBatch = 8;
+
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int th = blockIdx.x * 8 + warp;  // (token, head)
   if (th >= P.T * P.H) return;
   const int t = th / P.H, h = th % P.H;
-  float M = -__int_as_float(0x7f800000);
-  for (int c = 0; c < P.n_chunks; ++c) {
-    const float2 ml = P.part_ml[(static_cast<size_t>(t) * P.n_chunks + c) * P.H + h];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
+  const float ninf = -__int_as_float(0x7f800000);
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  float wsum = 0.f;
-  for (int c = 0; c < P.n_chunks; ++c) {
-    const float2 ml = P.part_ml[(static_cast<size_t>(t) * P.n_chunks + c) * P.H + h];
-    if (!(ml.y > 0.f)) continue;
-    const float wc = ml.y * exp2f(ml.x - M);
-    wsum += wc;
-    const uint2* src = reinterpret_cast<const uint2*>(
-        P.part_o + ((static_cast<size_t>(t) * P.n_chunks + c) * P.H + h) * kDv);
+  float M = ninf, wsum = 0.f;
+  for (int c0 = 0; c0 < P.n_chunks; c0 += kCombineBatch) {
+    float2 ml[kCombineBatch];
+    uint2 raw[kCombineBatch][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint2 raw = __ldcg(src + lane + 32 * k);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-      const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-      acc[4 * k] = fmaf(wc, a.x, acc[4 * k]);
-      acc[4 * k + 1] = fmaf(wc, a.y, acc[4 * k + 1]);
-      acc[4 * k + 2] = fmaf(wc, b2.x, acc[4 * k + 2]);
-      acc[4 * k + 3] = fmaf(wc, b2.y, acc[4 * k + 3]);
+    for (int i = 0; i < kCombineBatch; ++i) {
+      const int c = c0 + i;
+      const size_t row = (static_cast<size_t>(t) * P.n_chunks + c) * P.H + h;
+      if (c < P.n_chunks) {
+        ml[i] = __ldcg(P.part_ml + row);
+        const uint2* src = reinterpret_cast<const uint2*>(P.part_o + row * kDv);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) raw[i][k] = __ldcg(src + lane + 32 * k);
+      } else {
+        ml[i] = make_float2(ninf, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) raw[i][k] = make_uint2(0u, 0u);
+      }
+    }
+    float Mb = M;
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i)
+      if (ml[i].y > 0.f) Mb = fmaxf(Mb, ml[i].x);
+    if (Mb == ninf) continue;  // nothing visible yet
+    const float r = (M == ninf) ? 0.f : exp2f(M - Mb);
+    wsum *= r;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] *= r;
+    M = Mb;
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) {
+      const float wc = ml[i].y > 0.f ? ml[i].y * exp2f(ml[i].x - M) : 0.f;
+      wsum += wc;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i][k].x));
+        const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i][k].y));
+        acc[4 * k] = fmaf(wc, a.x, acc[4 * k]);
+        acc[4 * k + 1] = fmaf(wc, a.y, acc[4 * k + 1]);
+        acc[4 * k + 2] = fmaf(wc, b2.x, acc[4 * k + 2]);
+        acc[4 * k + 3] = fmaf(wc, b2.y, acc[4 * k + 3]);
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -503,8 +530,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
     *reinterpret_cast<uint2*>(orow + 4 * (lane + 32 * k)) = pk;
   }
   if (lane == 0 && P.lse != nullptr)
-    P.lse[static_cast<size_t>(t) * P.H + h] =
-        wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+    P.lse[static_cast<size_t>(t) * P.H + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : ninf;
 }
 
 void plan(const dsa_attn_args& a, int& head_blocks, int& n_chunks, int& chunk_rows) {

@@ -151,7 +151,7 @@ size_t topk_scores_bytes(const dsa_topk_args* a) {
 }
 
 // Workspace of dsa_indexer_topk: score rows (unless scores_out is given),
-// then, on the fused path, the histogram / counters / candidates region.
+// then, on the fused path, the per-token score histograms.
 size_t topk_total_bytes(const dsa_topk_args* a) {
   return topk_scores_bytes(a) + (topk_hist_eligible(*a) ? topk_hist_workspace(*a) : 0);
 }

@@ -36,9 +36,8 @@ int launch_indexer(const dsa_topk_args& a, float* scores, uint32_t* hist, cudaSt
 // Fused top-k path: the indexer also counts each token's scores by their
 // leading 12 key bits; the top-k pass then needs one read of the row.
 constexpr int kTopkHistBins = 4096;
-constexpr int kTopkCandCap = 16384;
 bool topk_hist_eligible(const dsa_topk_args& a);
-size_t topk_hist_workspace(const dsa_topk_args& a);  // hist + counters + candidates
+size_t topk_hist_workspace(const dsa_topk_args& a);  // the per-token histograms
 int launch_topk_hist(const dsa_topk_args& a, const float* scores, int64_t ld, void* ws, cudaStream_t s);
 int launch_indexer_dots(const dsa_topk_args& a, int32_t* dots, cudaStream_t s);
 int launch_topk(const dsa_topk_args& a, const float* scores, int64_t scores_ld, cudaStream_t s);

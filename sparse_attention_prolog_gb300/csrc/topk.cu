@@ -265,215 +265,223 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
 // Top-k with the leading digit known in advance.  The indexer has counted
 // every row's visible scores by the leading 12 bits of their order key, so
 // the k-th largest key's leading digit B and the number of keys above it
-// follow from the histogram alone.  S CTAs share a row (<= 8192 keys each,
-// held in registers): keys above B go straight to the output, keys inside B
-// become candidates; the last CTA of the row (atomic ticket) selects the
-// remaining ones among the candidates by the low 20 bits, then clears the
-// row's histogram and counters for the next call.
+// follow from that histogram alone.  One cluster of CS CTAs (<= 8) takes a
+// row; CTA r holds keys [r * kThreads * PER, (r + 1) * kThreads * PER) in
+// registers (one read of the row).  Keys above B go straight to the output;
+// the missing `need` keys of bin B are found by a radix select on the low 20
+// bits (two 10-bit passes) over the same registers, whose per-CTA histograms
+// are summed in CTA 0's shared memory with cluster atomics.  Output slots are
+// reserved the same way, one atomic per warp.  The row's histogram is left
+// zeroed for the next call.
 constexpr int kHB = kTopkHistBins;
+constexpr int kLowBins = 1024;  // 10-bit digits of the second and third pass
 
 struct TopkHistParams {
   const float* scores;
   int64_t ld;
   const int32_t* pos;
-  int max_L, topk, slices;
+  int max_L, topk;
   int32_t* out;
   uint32_t* hist;  // [T][kHB]
-  uint32_t* ctr;   // [T][4]: keys above B emitted, candidates, CTAs done
-  uint2* cand;     // [T][kTopkCandCap]: (key, index)
   uint32_t* err;
 };
 
-// Exclusive block scan of (a, b) pairs; returns totals through ta, tb.
-__device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb, uint32_t& ta,
-                                            uint32_t& tb, uint32_t* sh /*[2 * 33]*/) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t ia = a, ib = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t na = __shfl_up_sync(0xffffffffu, ia, o);
-    const uint32_t nb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) { ia += na; ib += nb; }
-  }
-  if (lane == 31) { sh[warp] = ia; sh[33 + warp] = ib; }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t wa = sh[lane], wb = sh[33 + lane];
-    uint32_t xa = wa, xb = wb;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t na = __shfl_up_sync(0xffffffffu, xa, o);
-      const uint32_t nb = __shfl_up_sync(0xffffffffu, xb, o);
-      if (lane >= o) { xa += na; xb += nb; }
-    }
-    sh[lane] = xa - wa;
-    sh[33 + lane] = xb - wb;
-    if (lane == 31) { sh[32] = xa; sh[65] = xb; }
-  }
-  __syncthreads();
-  ea = sh[warp] + ia - a;
-  eb = sh[33 + warp] + ib - b;
-  ta = sh[32];
-  tb = sh[65];
-  __syncthreads();
+__device__ __forceinline__ uint32_t atom_add_cluster(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Finds, scanning bins from the top, the bin where the running count
-// reaches `need`; per = bins per thread (nbins = per * kThreads).
+// Reserves n consecutive output slots for this thread from the counter at
+// cluster address `ctr` (one atomic per warp); returns the first slot.
+__device__ __forceinline__ uint32_t warp_reserve_n(uint32_t ctr, uint32_t n) {
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+  uint32_t base = 0;
+  if (lane == 31 && total) base = atom_add_cluster(ctr, total);
+  base = __shfl_sync(0xffffffffu, base, 31);
+  return base + incl - n;
+}
+
+// Block-wide search from the top bin: thread tid holds the counts of bins
+// nbins-1-(tid*PER+i); returns the bin where the running count (from the
+// top) first reaches `need`, the count strictly above it, and its own count.
+// bin = -1 if the counts never reach `need`.
 template <int PER>
-__device__ __forceinline__ void find_from_top(const uint32_t* hist, uint32_t need, int& bin, uint32_t& above,
-                                              uint32_t* sh) {
+__device__ __forceinline__ void find_from_top(const uint32_t (&mine)[PER], uint32_t need, int& bin,
+                                              uint32_t& above, uint32_t& count, uint32_t* sh /*[36]*/) {
   constexpr int nbins = PER * kThreads;
-  const int tid = threadIdx.x;
-  uint32_t mine[PER];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t s = 0;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    mine[i] = hist[nbins - 1 - (tid * PER + i)];
-    s += mine[i];
+  for (int i = 0; i < PER; ++i) s += mine[i];
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  uint32_t ex, dummy, tot, t2;
-  block_scan2(s, 0u, ex, dummy, tot, t2, sh);
-  uint32_t before = ex;
+  if (lane == 31) sh[warp] = incl;
+  if (tid == 0) sh[32] = 0xffffffffu;
+  __syncthreads();
+  uint32_t before = incl - s;
+  for (int w2 = 0; w2 < warp; ++w2) before += sh[w2];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     if (before < need && before + mine[i] >= need) {
-      sh[66] = nbins - 1 - (tid * PER + i);
-      sh[67] = before;
+      sh[32] = nbins - 1 - (tid * PER + i);
+      sh[33] = before;
+      sh[34] = mine[i];
     }
     before += mine[i];
   }
   __syncthreads();
-  bin = static_cast<int>(sh[66]);
-  above = sh[67];
+  bin = sh[32] == 0xffffffffu ? -1 : static_cast<int>(sh[32]);
+  above = sh[33];
+  count = sh[34];
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const TopkHistParams P) {
-  __shared__ uint32_t sh[80];
-  __shared__ uint32_t lh[1024];
-  __shared__ uint32_t base[2];
+template <int PER>
+__global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistParams P) {
+  __shared__ uint32_t sh[40];
+  __shared__ uint32_t lh[2][kLowBins];  // this CTA's counts, passes 1 and 2
+  __shared__ uint32_t gh[2][kLowBins];  // CTA 0: the cluster's counts
+  __shared__ uint32_t cnt[4];           // CTA 0: output slot counters
   const int tid = threadIdx.x;
-  const int row = blockIdx.x / P.slices, sl = blockIdx.x % P.slices;
+  const uint32_t rank = cluster_ctarank();
+  uint32_t ncta;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+  const int row = blockIdx.x / static_cast<int>(ncta);
+  for (int i = tid; i < kLowBins; i += kThreads) {
+    lh[0][i] = 0; lh[1][i] = 0; gh[0][i] = 0; gh[1][i] = 0;
+  }
+  if (tid < 4) cnt[tid] = 0;
   griddep_launch_dependents();
-  griddep_wait();
-  const int n_valid = min(P.pos[row] + 1, P.max_L);
+  griddep_wait();  // scores and histogram come from the indexer
+
+  // Issue every global load at once: the row's histogram, this CTA's keys
+  // (up to max_L; masked by the row's causal limit once pos arrives).
+  const float* src = P.scores + static_cast<size_t>(row) * P.ld;
+  uint32_t* hist = P.hist + static_cast<size_t>(row) * kHB;
+  const int lo = static_cast<int>(rank) * kThreads * PER;
+  constexpr int kHPer = kHB / kThreads;
+  uint32_t hv[kHPer];
+#pragma unroll
+  for (int i = 0; i < kHPer; ++i) hv[i] = __ldcg(hist + kHB - 1 - (tid * kHPer + i));
+  uint32_t keys[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int i = lo + tid + e * kThreads;
+    keys[e] = i < P.max_L ? order_key(__ldcg(src + i)) : 0u;
+  }
+  const int n_valid = min(__ldg(P.pos + row) + 1, P.max_L);
   const int k = P.topk;
   int32_t* out = P.out + static_cast<size_t>(row) * k;
-  uint32_t* hist = P.hist + static_cast<size_t>(row) * kHB;
-  uint32_t* ctr = P.ctr + static_cast<size_t>(row) * 4;
-  uint2* cand = P.cand + static_cast<size_t>(row) * kTopkCandCap;
-  if (n_valid <= k) {
-    if (sl == 0) {
+  if (n_valid <= k) {  // every visible key, then -1 (same branch in every CTA)
+    if (rank == 0) {
       for (int i = tid; i < k; i += kThreads) out[i] = (i < n_valid) ? i : -1;
       for (int i = tid; i < kHB; i += kThreads) hist[i] = 0;
     }
     return;
   }
-  // Leading digit of the k-th largest key, keys above it, keys in it.
-  int B;
-  uint32_t c_above;
-  find_from_top<kHB / kThreads>(hist, static_cast<uint32_t>(k), B, c_above, sh);
-  const uint32_t c_bin = hist[B];
-  const uint32_t need = static_cast<uint32_t>(k) - c_above;
+  auto valid = [&](int e) { return lo + tid + e * kThreads < n_valid; };
 
-  // This CTA's slice of the row, in registers.
-  const int chunk = (n_valid + P.slices - 1) / P.slices;
-  const int lo = sl * chunk, hi = min(n_valid, lo + chunk);
-  const float* src = P.scores + static_cast<size_t>(row) * P.ld;
-  uint32_t keys[kPer];
-  uint32_t n_gt = 0, n_eq = 0;
+  // Leading digit B of the k-th largest key and the keys above it.
+  int B;
+  uint32_t c_above, c_bin;
+  find_from_top<kHPer>(hv, static_cast<uint32_t>(k), B, c_above, c_bin, sh);
+  if (B < 0) {  // histogram and row disagree: the workspace was not zeroed
+    if (tid == 0) atomicOr(P.err, kErrBadIndex);
+    return;
+  }
+  const uint32_t ub = static_cast<uint32_t>(B);
+  cluster_sync();  // CTA 0's counters are zero; every CTA has read the histogram
+  {
+    const int h0 = static_cast<int>(rank) * kHB / static_cast<int>(ncta);
+    const int h1 = static_cast<int>(rank + 1) * kHB / static_cast<int>(ncta);
+    for (int i = h0 + tid; i < h1; i += kThreads) hist[i] = 0;
+  }
+  const uint32_t cnt0 = mapa(smem_u32(cnt), 0);
+
+  // Keys above the leading digit: output slots [0, c_above).
+  {
+    uint32_t n = 0;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const int i = lo + tid + e * kThreads;
-    keys[e] = (i < hi) ? order_key(src[i]) : 0u;
-    if (i < hi) {
-      n_gt += (keys[e] >> 20) > static_cast<uint32_t>(B);
-      n_eq += (keys[e] >> 20) == static_cast<uint32_t>(B);
+    for (int e = 0; e < PER; ++e) n += (valid(e) && (keys[e] >> 20) > ub) ? 1u : 0u;
+    uint32_t p = warp_reserve_n(cnt0, n);
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+      if (valid(e) && (keys[e] >> 20) > ub) {
+        if (p < c_above) out[p] = lo + tid + e * kThreads;
+        ++p;
+      }
+  }
+
+  // Radix select of the `need` largest keys inside bin B (bits 19..10, then
+  // 9..0).
+  uint32_t need = static_cast<uint32_t>(k) - c_above;
+  uint32_t prefix = ub << 20, mask = 0xFFF00000u;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+      if (valid(e) && (keys[e] & mask) == prefix) atomicAdd(&lh[pass][(keys[e] >> shift) & (kLowBins - 1)], 1u);
+    __syncthreads();
+    {
+      const uint32_t v = lh[pass][tid];
+      if (v) red_add_cluster(mapa(smem_u32(&gh[pass][tid]), 0), v);
     }
+    cluster_sync();
+    uint32_t g1[1] = {ld_cluster_u32(mapa(smem_u32(&gh[pass][kLowBins - 1 - tid]), 0))};
+    int bn;
+    uint32_t ab, cb;
+    find_from_top<1>(g1, need, bn, ab, cb, sh);
+    if (bn < 0) {  // cannot happen when the histogram matches the row
+      if (tid == 0) atomicOr(P.err, kErrBadIndex);
+      bn = 0;
+    }
+    need -= ab;
+    prefix |= static_cast<uint32_t>(bn) << shift;
+    mask |= static_cast<uint32_t>(kLowBins - 1) << shift;
   }
-  uint32_t off_gt, off_eq, tot_gt, tot_eq;
-  block_scan2(n_gt, n_eq, off_gt, off_eq, tot_gt, tot_eq, sh);
-  if (tid == 0) {
-    base[0] = tot_gt ? atomicAdd(&ctr[0], tot_gt) : 0u;
-    base[1] = tot_eq ? atomicAdd(&ctr[1], tot_eq) : 0u;
-  }
-  __syncthreads();
-  uint32_t pg = base[0] + off_gt, pe = base[1] + off_eq;
+  // prefix is now the k-th largest key; `need` of its copies are taken after
+  // the (k - c_above - need) keys of bin B above it.
+  const uint32_t thr = prefix;
+  const uint32_t base_gt = c_above, base_eq = static_cast<uint32_t>(k) - need;
+  {
+    uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const int i = lo + tid + e * kThreads;
-    if (i < hi) {
-      const uint32_t d = keys[e] >> 20;
-      if (d > static_cast<uint32_t>(B)) {
-        if (pg < c_above) out[pg] = i;
+    for (int e = 0; e < PER; ++e) {
+      const bool inb = valid(e) && (keys[e] >> 20) == ub;
+      n_gt += (inb && keys[e] > thr) ? 1u : 0u;
+      n_eq += (inb && keys[e] == thr) ? 1u : 0u;
+    }
+    uint32_t pg = base_gt + warp_reserve_n(cnt0 + 4, n_gt);
+    uint32_t pe = warp_reserve_n(cnt0 + 8, n_eq);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const bool inb = valid(e) && (keys[e] >> 20) == ub;
+      if (inb && keys[e] > thr) {
+        if (pg < base_eq) out[pg] = lo + tid + e * kThreads;
         ++pg;
-      } else if (d == static_cast<uint32_t>(B)) {
-        if (pe < kTopkCandCap) cand[pe] = make_uint2(keys[e], static_cast<uint32_t>(i));
+      } else if (inb && keys[e] == thr) {
+        if (pe < need) out[base_eq + pe] = lo + tid + e * kThreads;
         ++pe;
       }
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh[70] = (atomicAdd(&ctr[2], 1u) == static_cast<uint32_t>(P.slices - 1));
-  __syncthreads();
-  if (!sh[70]) return;
-  __threadfence();
-
-  // Last CTA of the row: the `need` largest candidates by the low 20 bits.
-  if (c_bin > static_cast<uint32_t>(kTopkCandCap)) {
-    if (tid == 0) atomicOr(P.err, kErrBadIndex);  // leading digit too crowded
-  } else {
-    constexpr int kC = kTopkCandCap / kThreads;
-    uint32_t ck[kC], ci[kC];
-#pragma unroll
-    for (int e = 0; e < kC; ++e) {
-      const int i = tid + e * kThreads;
-      if (i < static_cast<int>(c_bin)) {
-        const uint2 v = __ldcg(cand + i);
-        ck[e] = v.x;
-        ci[e] = v.y;
-      } else {
-        ck[e] = 0u;
-        ci[e] = 0xffffffffu;
-      }
-    }
-    uint32_t prefix = static_cast<uint32_t>(B) << 20, mask = 0xFFF00000u, nd = need;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int sh_ = pass == 0 ? 10 : 0;
-      lh[tid] = 0;
-      __syncthreads();
-#pragma unroll
-      for (int e = 0; e < kC; ++e)
-        if (ci[e] != 0xffffffffu && (ck[e] & mask) == prefix) atomicAdd(&lh[(ck[e] >> sh_) & 1023u], 1u);
-      __syncthreads();
-      int bn;
-      uint32_t ab;
-      find_from_top<1>(lh, nd, bn, ab, sh);
-      nd -= ab;
-      prefix |= static_cast<uint32_t>(bn) << sh_;
-      mask |= 1023u << sh_;
-    }
-    const uint32_t thr = prefix;  // the k-th largest key; nd of its copies are taken
-    if (tid == 0) { base[0] = 0; base[1] = 0; }
-    __syncthreads();
-    const uint32_t n_gt_c = need - nd;
-#pragma unroll
-    for (int e = 0; e < kC; ++e) {
-      if (ci[e] == 0xffffffffu) continue;
-      if (ck[e] > thr) {
-        out[c_above + atomicAdd(&base[0], 1u)] = static_cast<int32_t>(ci[e]);
-      } else if (ck[e] == thr) {
-        const uint32_t q = atomicAdd(&base[1], 1u);
-        if (q < nd) out[c_above + n_gt_c + q] = static_cast<int32_t>(ci[e]);
-      }
-    }
-  }
-  // Leave the row's histogram and counters zeroed for the next call.
-  for (int i = tid; i < kHB; i += kThreads) hist[i] = 0;
-  if (tid < 3) ctr[tid] = 0;
+  cluster_sync();  // CTA 0's shared memory stays alive until every atomic is done
 }
 
 template <int CS>
@@ -503,40 +511,41 @@ cudaError_t launch_cs(const TopkParams& P, int T, cudaStream_t s) {
 }  // namespace
 
 bool topk_hist_eligible(const dsa_topk_args& a) {
-  // groups of at most two tokens (the indexer's histogram), and a bounded
-  // candidate workspace
+  // groups of at most two tokens (the indexer's histogram); a row fits one
+  // cluster of at most 8 CTAs with 16 keys per thread
   const int G = a.H_I >= 128 ? 1 : (128 / a.H_I < a.n_q ? 128 / a.H_I : a.n_q);
-  return G <= 2 && a.H_I >= 64 && a.T <= 512 && a.max_L <= kThreads * kPer * 64;
+  return G <= 2 && a.H_I >= 64 && a.T <= 512 && a.max_L <= kThreads * 16 * 8;
 }
 
 size_t topk_hist_workspace(const dsa_topk_args& a) {
-  return round_up(static_cast<size_t>(a.T) * kTopkHistBins * 4, 256) + round_up(static_cast<size_t>(a.T) * 16, 256) +
-         round_up(static_cast<size_t>(a.T) * kTopkCandCap * 8, 256);
+  return round_up(static_cast<size_t>(a.T) * kTopkHistBins * 4, 256);
 }
 
 int launch_topk_hist(const dsa_topk_args& a, const float* scores, int64_t ld, void* ws, cudaStream_t s) {
   TopkHistParams P{};
   P.scores = scores; P.ld = ld; P.pos = a.pos; P.max_L = a.max_L; P.topk = a.topk; P.out = a.topk_idx;
-  P.slices = (a.max_L + kThreads * 8 - 1) / (kThreads * 8);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  P.hist = reinterpret_cast<uint32_t*>(w);
-  w += round_up(static_cast<size_t>(a.T) * kTopkHistBins * 4, 256);
-  P.ctr = reinterpret_cast<uint32_t*>(w);
-  w += round_up(static_cast<size_t>(a.T) * 16, 256);
-  P.cand = reinterpret_cast<uint2*>(w);
+  P.hist = static_cast<uint32_t*>(ws);
   P.err = error_word();
   if (!P.err) return DSA_ERR_CUDA;
+  const int per = a.max_L <= kThreads * 8 * 8 ? 8 : 16;
+  const int cs = (a.max_L + kThreads * per - 1) / (kThreads * per);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(a.T * P.slices);
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cs;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(a.T * cs);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, topk_hist_kernel, P));
+  cfg.numAttrs = 2;
+  cudaError_t e = per == 8 ? cudaLaunchKernelEx(&cfg, topk_hist_kernel<8>, P)
+                           : cudaLaunchKernelEx(&cfg, topk_hist_kernel<16>, P);
+  return cuda_status(e);
 }
 
 int launch_topk(const dsa_topk_args& a, const float* scores, int64_t ld, cudaStream_t s) {

@@ -66,6 +66,48 @@ def test_short_rows_pad_with_minus_one(cuda_lib):
     _check_all(inp, buf, tokens=[0, 1, 63, 199, 200, 201, 255, 383])
 
 
+@pytest.mark.parametrize("seq_lens,max_L", [([24576, 20000], 24576), ([98304, 70000], 98304)])
+def test_fused_topk_row_splits(seq_lens, max_L, cuda_lib):
+    """Rows of 24576 keys (a 3-CTA cluster of 8 keys per thread) and 98304
+    keys (6 CTAs of 16 keys per thread) on the histogram top-k path."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=seq_lens, H_I=64, d_I=128, topk=2048, H=8, seed=16,
+                               max_L=max_L, with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
+def test_fused_topk_all_scores_equal(cuda_lib):
+    """Zero queries make every visible score 0: any k distinct visible keys
+    are a correct answer."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[5000, 9000], H_I=64, d_I=128, topk=1024, H=8, seed=17, max_L=9088,
+                               with_attention=False)
+    inp.q_idx[:] = 0
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
+def test_fused_topk_many_ties_at_threshold(cuda_lib):
+    """Keys of 0/1 bytes against all-ones queries with equal key scales give
+    at most 129 distinct scores, so the k-th score is shared by many keys
+    and only some of its copies may be taken."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[12000, 16384], H_I=64, d_I=128, topk=2048, H=8, seed=18,
+                               with_attention=False)
+    rng = np.random.default_rng(118)
+    inp.k_cache[:] = (rng.random(inp.k_cache.shape) < 0.5).astype(np.int8)
+    inp.k_scale[:] = np.float16(0.03125)
+    inp.q_idx[:] = 1
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+    sc = buf.scores.cpu().numpy()
+    for t in range(inp.T):  # the tie case really occurs
+        n = int(inp.pos[t]) + 1
+        kth = np.sort(sc[t, :n])[::-1][inp.topk - 1]
+        assert (sc[t, :n] == kth).sum() > 1
+
+
 @pytest.mark.parametrize("sign", [1, -1])
 def test_tensor_core_dots_bit_exact(sign, cuda_lib):
     """One-hot head weights with unit scales make I[t,s] = ReLU(dot[t,h0,s])
