@@ -18,20 +18,26 @@
 // dots equal the int32 ones bit for bit.
 //
 // Warp roles of the persistent CTA (one per SM):
-//   warp 8     producer: 2-D TMA loads (128B swizzle) of the raw int8 key
+//   warp 12    producer: 2-D TMA loads (128B swizzle) of the raw int8 key
 //              tile into an 8-deep shared-memory ring
 //   warps 4-7  converters: one thread per key row reads its 128 bytes
 //              (bank-conflict free thanks to the swizzle), converts them to
 //              f16 and stores the row into TMEM, where it is the A operand
 //              of the MMA; they also stage Q (the B operand, shared memory)
 //              for each new group
-//   warp 9     one thread issues tcgen05.mma (A from TMEM, B from shared
-//              memory) into a double-buffered TMEM accumulator
+//   warp 13    one thread issues tcgen05.mma (A from TMEM, B from shared
+//              memory) into two or three rotating TMEM accumulators
 // Keeping the keys out of shared memory after the TMA halves the shared
 // memory traffic per tile, which otherwise bounds the kernel.
-//   warps 0-3  epilogue: tcgen05.ld of the accumulator row of its key,
-//              ReLU + head-weighted sum per token, times ks[s], causal mask,
-//              and the fp32 score row store (coalesced over keys)
+//   warps 0-3, 8-11  epilogue, two groups of four warps over the same TMEM
+//              lanes (warp w reads lanes 32 (w % 4) ..): group e takes the
+//              tokens e, e + 2, ... of the tile.  tcgen05.ld of the
+//              accumulator row of its key, ReLU + head-weighted sum per
+//              token, times ks[s], causal mask, and the fp32 score row store
+//              (coalesced over keys)
+// Each role waits for the previous kernel (programmatic launch) only before
+// its first read of that kernel's outputs (q, w, qs, new cache rows), so the
+// work list is built while the producing kernel is still finishing.
 // The per-head scores [T, H_I, L] never leave the SM; only I[t, s] (fp32,
 // [T, max_L]) is written, for the top-k pass.
 #include <cuda.h>
@@ -46,7 +52,7 @@ namespace {
 constexpr int kTileKeys = 128;
 constexpr int kStages8 = 8;   // raw int8 key tiles in flight
 constexpr int kStages16 = 2;  // converted f16 key tiles (in TMEM)
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;  // 14 warps, see the role map above
 constexpr int kMaxG = 32;     // tokens per group
 constexpr int kCoef = 256;    // max query rows (N) of a group
 constexpr int kHistBins = 4096;  // leading 12 bits of the score's order key
@@ -122,7 +128,8 @@ struct __align__(8) Bars {
   uint64_t full8[kStages8], empty8[kStages8];
   uint64_t full16[kStages16], empty16[kStages16];
   uint64_t qfull, qempty;
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull[3], tempty[3];
+  uint64_t epsync;  // barrier of the 8 epilogue warps (bounded wait)
 };
 
 template <int HI, int DI>
@@ -153,10 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Accumulator buffers start on 32-column boundaries so that every 32-column
   // load stays inside its own buffer.
-  // TMEM: two fp32 accumulators, then two f16 key tiles (DI/2 columns each).
+  // TMEM: n_acc fp32 accumulators (three when they fit in the 512 columns,
+  // so the MMA can run two tiles ahead of the epilogue), then two f16 key
+  // tiles (DI/2 columns each).
   const int acc_stride = (N + 31) & ~31;
-  const uint32_t a_col0 = 2 * acc_stride;
-  const int need_cols = 2 * acc_stride + DI;
+  const int n_acc = 3 * acc_stride + DI <= 512 ? 3 : 2;
+  const uint32_t a_col0 = n_acc * acc_stride;
+  const int need_cols = n_acc * acc_stride + DI;
   const uint32_t tmem_cols = need_cols <= 64 ? 64 : need_cols <= 128 ? 128 : need_cols <= 256 ? 256 : 512;
 
   if (tid == 0) {
@@ -164,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages16; ++i) { mbar_init(&bars.full16[i], 4); mbar_init(&bars.empty16[i], 1); }
     mbar_init(&bars.qfull, 4);
     mbar_init(&bars.qempty, 1);
-    for (int i = 0; i < 2; ++i) { mbar_init(&bars.tfull[i], 1); mbar_init(&bars.tempty[i], 4); }
+    for (int i = 0; i < 3; ++i) { mbar_init(&bars.tfull[i], 1); mbar_init(&bars.tempty[i], 8); }
+    mbar_init(&bars.epsync, 256);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -173,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   griddep_launch_dependents();
-  griddep_wait();  // q, w, qs and the new cache rows come from the prolog
   const uint32_t tmem = tmem_base;
   volatile int* abort_v = &abort_flag;
 
@@ -218,12 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     w0.j = item_lo - tiles_prefix[lo];
   }
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
       int st = 0;
       uint32_t ph = 0;
       int cur_g = -1, maxpos_cache = -1;
+      if (w0.left > 0) { cur_g = w0.g; maxpos_cache = group_of(P, w0.g).maxpos; }
+      griddep_wait();  // the key cache holds rows the previous kernel wrote
       Walker w = w0;
       for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w)) {
         const int g = w.g, j = w.j;
@@ -233,23 +246,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = s8 + st * tile8_bytes;
         const int s0 = j * kTileKeys;
         const int bh = P.box_rows;  // 128 (contiguous) or the page size (< 128)
-        int ys[kTileKeys / 8];
-        int n_loads = 0;
-        for (int k = 0; k < kTileKeys && s0 + k <= maxpos_cache; k += bh) {
-          const int64_t row = key_row(P, b, s0 + k);
-          if (row < 0) { atomicOr(P.err, kErrBadIndex); ys[n_loads++] = -1; continue; }
-          ys[n_loads++] = static_cast<int>(row);
+        // Boxes of bh rows that cover the tile's visible keys (>= 1: the
+        // walk only visits tiles with a visible key).
+        const int n_loads = min(kTileKeys / bh, (maxpos_cache - s0) / bh + 1);
+        mbar_arrive_expect_tx(&bars.full8[st], static_cast<uint32_t>(n_loads * bh * DI));
+        for (int c = 0; c < n_loads; ++c) {
+          int64_t row = key_row(P, b, s0 + c * bh);
+          if (row < 0) {  // unmapped page: flag it and load row 0 so the stage still completes
+            atomicOr(P.err, kErrBadIndex);
+            row = 0;
+          }
+          tma_load_2d(dst + c * bh * DI, &tmap, 0, static_cast<int>(row), &bars.full8[st]);
         }
-        uint32_t bytes = 0;
-        for (int c = 0; c < n_loads; ++c) bytes += ys[c] >= 0 ? static_cast<uint32_t>(bh * DI) : 0u;
-        mbar_arrive_expect_tx(&bars.full8[st], bytes);
-        for (int c = 0; c < n_loads; ++c)
-          if (ys[c] >= 0) tma_load_2d(dst + c * bh * DI, &tmap, 0, ys[c], &bars.full8[st]);
         if (++st == kStages8) { st = 0; ph ^= 1; }
       }
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- converters
+    griddep_wait();  // q comes from the previous kernel
     const int ct = tid - 128;  // 0..127
     int st8 = 0, st16 = 0;
     uint32_t ph8 = 0, ph16 = 0, qph = 0;
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++st8 == kStages8) { st8 = 0; ph8 ^= 1; }
       if (++st16 == kStages16) { st16 = 0; ph16 ^= 1; }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, N, kFmtF16, 0, 0);
@@ -359,61 +373,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool group_ends = !more || w.g != g;
         if (group_ends) mma_commit(&bars.qempty);
         if (++st16 == kStages16) { st16 = 0; ph16 ^= 1; }
-        if (++acc == 2) { acc = 0; aph ^= 1; }
+        if (++acc == n_acc) { acc = 0; aph ^= 1; }
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || (warp >= 8 && warp < 12)) {
     // ---------------------------------------------------------- epilogue
+    const int eg = warp >= 8 ? 1 : 0;  // token parity this group scores
+    const int q4 = warp & 3;           // TMEM lane quarter
+    const int et = eg * 128 + q4 * 32 + lane;  // 0..255 over both groups
+    const int r = q4 * 32 + lane;      // key within the tile = TMEM lane
+    // Barrier of the 256 epilogue threads on an mbarrier, so that a thread
+    // that gave up (abort) makes the others time out instead of hanging.
+    uint32_t ep_ph = 0;
+    auto ep_sync = [&]() -> bool {
+      mbar_arrive(&bars.epsync);
+      const bool ok = mbar_wait(&bars.epsync, ep_ph, P.err, abort_v);
+      ep_ph ^= 1;
+      return ok;
+    };
     int acc = 0;
     uint32_t aph = 0;
     int cur_g = -1;
     Group G{};
-    const int r = warp * 32 + lane;  // key within the tile = TMEM lane
     const float ninf = -__int_as_float(0x7f800000);
-    // ks of the key this thread scores in a given item (0 past the group's
-    // last visible key); loaded one item ahead to hide its latency.  The
-    // group's (b, maxpos) are re-derived only when the walk enters a new
-    // group, so no per-tile branch waits on a global load.
+    // ks of the key this thread scores in a given item, as raw fp16 bits
+    // (ok = false past the group's last visible key).  Items are prefetched
+    // two ahead into two alternating registers, so no instruction waits on
+    // a scale load issued less than two items earlier.  The group's
+    // (b, maxpos) are re-derived only when the walk enters a new group.
     Group Gload{};
     int gload = -1;
-    auto load_ks = [&](const Walker& it) -> float {
+    auto load_ks = [&](const Walker& it, bool& ok) -> unsigned short {
       if (it.g != gload) {
         gload = it.g;
         Gload = group_of(P, it.g);
       }
       const int sx = it.j * kTileKeys + r;
-      if (sx > Gload.maxpos) return 0.f;
-      const int64_t row = key_row(P, Gload.b, sx);
-      return row >= 0 ? __half2float(__ldg(P.k_scale + row)) : 0.f;
+      const int64_t row = sx > Gload.maxpos ? -1 : key_row(P, Gload.b, sx);
+      ok = row >= 0;
+      return __ldg(reinterpret_cast<const unsigned short*>(P.k_scale) + (ok ? row : 0));
     };
     const bool do_hist = kHist && P.hist != nullptr;
-    auto flush_hist = [&]() {  // G is the group whose counts are flushed
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+    auto flush_hist = [&]() -> bool {  // G is the group whose counts are flushed
+      if (!ep_sync()) return false;
       for (int gi = 0; gi < G.ntok && gi < 2; ++gi)
-        for (int bin = tid; bin < kHistBins; bin += 128) {
+        for (int bin = et; bin < kHistBins; bin += 256) {
           const uint32_t v = hist_s[gi * kHistBins + bin];
           if (v) {
             atomicAdd(P.hist + static_cast<size_t>(G.t0 + gi) * kHistBins + bin, v);
             hist_s[gi * kHistBins + bin] = 0;
           }
         }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      return ep_sync();
     };
-    Walker w = w0;
-    bool more = w.left > 0;
-    float ks_next = more ? load_ks(w) : 0.f;
-    while (more) {
-      const int g = w.g, j = w.j;
-      const float ks = ks_next;
-      Walker wn = w;
-      const bool more_n = walk_next(tiles_prefix, P.n_groups, wn);
-      if (more_n) ks_next = load_ks(wn);
+    auto release = [&]() {  // this warp has read the accumulator
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.tempty[acc]);
+    };
+    // Scores one item; false if a wait gave up.
+    auto score_item = [&](const Walker& it, unsigned short ks_raw, bool ks_ok) -> bool {
+      const int g = it.g, j = it.j;
       if (g != cur_g) {
-        if (do_hist && cur_g >= 0) flush_hist();
+        if (do_hist && cur_g >= 0 && !flush_hist()) return false;
         cur_g = g;
         G = group_of(P, g);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        for (int n = tid; n < kCoef; n += 128) {
+        if (!ep_sync()) return false;
+        for (int n = et; n < kCoef; n += 256) {
           const int gi = n / HI, h = n % HI;
           float c = 0.f;
           if (gi < G.ntok && h < P.H_I) {
@@ -423,16 +449,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           coef[n] = c;
         }
-        for (int gi = tid; gi < kMaxG; gi += 128) tok_pos[gi] = (gi < G.ntok) ? __ldg(P.pos + G.t0 + gi) : -1;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int gi = et; gi < kMaxG; gi += 256) tok_pos[gi] = (gi < G.ntok) ? __ldg(P.pos + G.t0 + gi) : -1;
+        if (!ep_sync()) return false;
       }
-      if (!mbar_wait(&bars.tfull[acc], aph, P.err, abort_v)) break;
+      if (!mbar_wait(&bars.tfull[acc], aph, P.err, abort_v)) return false;
       tc_fence_after();
+      const float ks = ks_ok ? __half2float(__ushort_as_half(ks_raw)) : 0.f;
       const int s = j * kTileKeys + r;
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * acc_stride;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + acc * acc_stride;
+      bool released = false;
       // Column n = gi * HI + h of the accumulator is token gi, head h.
       if (HI >= 32) {
-        for (int gi = 0; gi < G.ntok; ++gi) {
+        for (int gi = eg; gi < G.ntok; gi += 2) {
           float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c = 0; c < HI / 32; c += 2) {
@@ -440,10 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(lane_addr + gi * HI + c * 32, v0);
             if (c + 1 < HI / 32) tmem_ld32(lane_addr + gi * HI + (c + 1) * 32, v1);
             tmem_ld_wait();
-            if (gi == G.ntok - 1 && c + 2 >= HI / 32) {  // last columns read: free the buffer
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars.tempty[acc]);
+            if (gi + 2 >= G.ntok && c + 2 >= HI / 32) {  // last columns this warp reads
+              release();
+              released = true;
             }
             const float* cf = coef + gi * HI + c * 32;
 #pragma unroll
@@ -460,22 +487,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           P.scores[static_cast<size_t>(G.t0 + gi) * P.ld + s] = val;
           if (kHist && do_hist && vis && gi < 2) atomicAdd(&hist_s[gi * kHistBins + (order_key(val) >> 20)], 1u);
         }
-        if (G.ntok == 0) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.tempty[acc]);
-        }
       } else {
         constexpr int kTokPerChunk = HI >= 32 ? 1 : 32 / HI;
         const int n_chunks = (G.ntok * HI + 31) / 32;
-        for (int cc = 0; cc < n_chunks; ++cc) {
+        for (int cc = eg; cc < n_chunks; cc += 2) {
           uint32_t v[32];
           tmem_ld32(lane_addr + cc * 32, v);
           tmem_ld_wait();
-          if (cc == n_chunks - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.tempty[acc]);
+          if (cc + 2 >= n_chunks) {
+            release();
+            released = true;
           }
 #pragma unroll
           for (int u = 0; u < kTokPerChunk; ++u) {
@@ -489,17 +510,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                   (s <= tok_pos[gi]) ? (part[0] + part[1]) * ks : ninf;
           }
         }
-        if (n_chunks == 0) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.tempty[acc]);
-        }
       }
-      if (++acc == 2) { acc = 0; aph ^= 1; }
-      w = wn;
-      more = more_n;
+      if (!released) release();  // nothing of this tile for this group
+      if (++acc == n_acc) { acc = 0; aph ^= 1; }
+      return true;
+    };
+
+    griddep_wait();  // w, qs and the new rows' ks come from the previous kernel
+    // Walk with two prefetch registers: at the top of the loop ks_a holds
+    // the current item (wc) and ks_b the next one (wa).
+    Walker wc = w0;
+    bool more = wc.left > 0;
+    Walker wa = wc;
+    bool more_a = more && walk_next(tiles_prefix, P.n_groups, wa);
+    bool ok_a = false, ok_b = false;
+    unsigned short ks_a = more ? load_ks(wc, ok_a) : 0;
+    unsigned short ks_b = more_a ? load_ks(wa, ok_b) : 0;
+    bool aborted = false;
+    while (more) {
+      Walker wb = wa;
+      bool more_b = more_a && walk_next(tiles_prefix, P.n_groups, wb);
+      if (!score_item(wc, ks_a, ok_a)) { aborted = true; break; }
+      if (more_b) ks_a = load_ks(wb, ok_a);
+      wc = wa; more = more_a; wa = wb; more_a = more_b;
+      if (!more) break;
+      wb = wa;
+      more_b = more_a && walk_next(tiles_prefix, P.n_groups, wb);
+      if (!score_item(wc, ks_b, ok_b)) { aborted = true; break; }
+      if (more_b) ks_b = load_ks(wb, ok_b);
+      wc = wa; more = more_a; wa = wb; more_a = more_b;
     }
-    if (do_hist && cur_g >= 0 && !*abort_v) flush_hist();
+    if (do_hist && cur_g >= 0 && !aborted) flush_hist();
   }
   tc_fence_before();
   __syncthreads();
