@@ -168,7 +168,8 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * k_scale fp16 [B, max_L].  Paged: k_cache int8 [n_rows, d_I], k_scale fp16
  * [n_rows], key s of sequence b at row block_table[b, s / block_size] *
  * block_size + s % block_size, block_table int32 [B, max_blocks],
- * max_L = max_blocks * block_size.
+ * max_L = max_blocks * block_size.  k_cache and k_scale are 16-byte
+ * aligned (each tile's scales are copied with its keys in bulk).
  * Supported: d_I in {64, 128}; H_I in {4, 8, 16, 32, 64, 128}; topk >= 1;
  * B * ceil(n_q / G) <= 4096 token groups, G = min(n_q, 128 / H_I, 32);
  * max_L a multiple of 128; block_size a multiple of 8 that divides 128 or

@@ -118,7 +118,7 @@ int check_topk(const dsa_topk_args* a) {
   if (a->topk < 1) return DSA_ERR_INVALID_ARG;
   if (a->max_L < 128 || a->max_L % 128 != 0) return DSA_ERR_UNSUPPORTED;
   if (bad_ptr(a->q, 16) || bad_ptr(a->q_scale, 2) || bad_ptr(a->w, 4) || bad_ptr(a->k_cache, 16) ||
-      bad_ptr(a->k_scale, 2) || bad_ptr(a->pos, 4) || bad_ptr(a->topk_idx, 4))
+      bad_ptr(a->k_scale, 16) || bad_ptr(a->pos, 4) || bad_ptr(a->topk_idx, 4))
     return DSA_ERR_INVALID_ARG;
   if (a->scores_out && !aligned(a->scores_out, 16)) return DSA_ERR_INVALID_ARG;
   if (a->block_table) {

@@ -51,7 +51,7 @@ namespace {
 
 constexpr int kTileKeys = 128;
 constexpr int kStages8 = 8;   // raw int8 key tiles in flight
-constexpr int kStages16 = 2;  // converted f16 key tiles (in TMEM)
+constexpr int kStages16 = 3;  // converted f16 key tiles (in TMEM)
 constexpr int kThreads = 448;  // 14 warps, see the role map above
 constexpr int kMaxG = 32;     // tokens per group
 constexpr int kCoef = 256;    // max query rows (N) of a group
@@ -76,6 +76,20 @@ struct IdxParams {
 struct Group {
   int b, t0, ntok, maxpos;
 };
+
+// Packed fp32 pair helpers: d = a * b + c on both halves (one instruction),
+// max(x, 0) of two floats packed into one 64-bit register.
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t relu_pair(uint32_t x, uint32_t y) {
+  const float a = fmaxf(__uint_as_float(x), 0.f), b = fmaxf(__uint_as_float(y), 0.f);
+  return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
 
 __device__ __forceinline__ Group group_of(const IdxParams& P, int g) {
   Group G;
@@ -143,9 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* s8 = smem;                                  // [kStages8][tile8]
   uint8_t* sQ = s8 + kStages8 * tile8_bytes;           // [d_I/64 atoms][N rows][128 B]
   __shared__ Bars bars;
+  // fp16 key scales of each ring stage, copied with its key tile.
+  __shared__ __align__(16) unsigned short ks_s[kStages8][kTileKeys];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ float coef[kCoef];
+  __shared__ __align__(16) float coef[kCoef];
   __shared__ int tok_pos[kMaxG];
   __shared__ int tiles_prefix[kMaxGroupsScheduled + 1];
   __shared__ int scan_tmp[kThreads / 32];
@@ -160,17 +176,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Accumulator buffers start on 32-column boundaries so that every 32-column
   // load stays inside its own buffer.
-  // TMEM: n_acc fp32 accumulators (three when they fit in the 512 columns,
-  // so the MMA can run two tiles ahead of the epilogue), then two f16 key
-  // tiles (DI/2 columns each).
+  // TMEM: n_acc fp32 accumulators (three when they fit in the 512 columns),
+  // then three f16 key tiles (DI/2 columns each), so that the converters
+  // can run two tiles ahead of the MMA.
   const int acc_stride = (N + 31) & ~31;
-  const int n_acc = 3 * acc_stride + DI <= 512 ? 3 : 2;
+  const int n_acc = 3 * acc_stride + kStages16 * DI / 2 <= 512 ? 3 : 2;
   const uint32_t a_col0 = n_acc * acc_stride;
-  const int need_cols = n_acc * acc_stride + DI;
+  const int need_cols = n_acc * acc_stride + kStages16 * DI / 2;
   const uint32_t tmem_cols = need_cols <= 64 ? 64 : need_cols <= 128 ? 128 : need_cols <= 256 ? 256 : 512;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages8; ++i) { mbar_init(&bars.full8[i], 1); mbar_init(&bars.empty8[i], 4); }
+    // A ring stage is free once the 4 converter warps have read its keys
+    // and the 8 epilogue warps its key scales.
+    for (int i = 0; i < kStages8; ++i) { mbar_init(&bars.full8[i], 1); mbar_init(&bars.empty8[i], 12); }
     for (int i = 0; i < kStages16; ++i) { mbar_init(&bars.full16[i], 4); mbar_init(&bars.empty16[i], 1); }
     mbar_init(&bars.qfull, 4);
     mbar_init(&bars.qempty, 1);
@@ -249,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Boxes of bh rows that cover the tile's visible keys (>= 1: the
         // walk only visits tiles with a visible key).
         const int n_loads = min(kTileKeys / bh, (maxpos_cache - s0) / bh + 1);
-        mbar_arrive_expect_tx(&bars.full8[st], static_cast<uint32_t>(n_loads * bh * DI));
+        mbar_arrive_expect_tx(&bars.full8[st], static_cast<uint32_t>(n_loads * bh * (DI + 2)));
         for (int c = 0; c < n_loads; ++c) {
           int64_t row = key_row(P, b, s0 + c * bh);
           if (row < 0) {  // unmapped page: flag it and load row 0 so the stage still completes
@@ -257,6 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             row = 0;
           }
           tma_load_2d(dst + c * bh * DI, &tmap, 0, static_cast<int>(row), &bars.full8[st]);
+          // The box's key scales: bh * 2 bytes, 16-byte aligned (rows of a
+          // box start at a multiple of 8, k_scale is 16-byte aligned).
+          bulk_g2s(&ks_s[st][c * bh], P.k_scale + row, static_cast<uint32_t>(bh * 2), &bars.full8[st]);
         }
         if (++st == kStages8) { st = 0; ph ^= 1; }
       }
@@ -396,23 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_g = -1;
     Group G{};
     const float ninf = -__int_as_float(0x7f800000);
-    // ks of the key this thread scores in a given item, as raw fp16 bits
-    // (ok = false past the group's last visible key).  Items are prefetched
-    // two ahead into two alternating registers, so no instruction waits on
-    // a scale load issued less than two items earlier.  The group's
-    // (b, maxpos) are re-derived only when the walk enters a new group.
-    Group Gload{};
-    int gload = -1;
-    auto load_ks = [&](const Walker& it, bool& ok) -> unsigned short {
-      if (it.g != gload) {
-        gload = it.g;
-        Gload = group_of(P, it.g);
-      }
-      const int sx = it.j * kTileKeys + r;
-      const int64_t row = sx > Gload.maxpos ? -1 : key_row(P, Gload.b, sx);
-      ok = row >= 0;
-      return __ldg(reinterpret_cast<const unsigned short*>(P.k_scale) + (ok ? row : 0));
-    };
+    int st8 = 0;  // ring stage of the current item (same order as the producer)
+    uint32_t ph8 = 0;
     const bool do_hist = kHist && P.hist != nullptr;
     auto flush_hist = [&]() -> bool {  // G is the group whose counts are flushed
       if (!ep_sync()) return false;
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.tempty[acc]);
     };
     // Scores one item; false if a wait gave up.
-    auto score_item = [&](const Walker& it, unsigned short ks_raw, bool ks_ok) -> bool {
+    auto score_item = [&](const Walker& it) -> bool {
       const int g = it.g, j = it.j;
       if (g != cur_g) {
         if (do_hist && cur_g >= 0 && !flush_hist()) return false;
@@ -454,14 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait(&bars.tfull[acc], aph, P.err, abort_v)) return false;
       tc_fence_after();
-      const float ks = ks_ok ? __half2float(__ushort_as_half(ks_raw)) : 0.f;
+      // This key's scale from the ring stage (complete long ago: the
+      // converters consumed it before the MMA); then free the stage.
+      if (!mbar_wait(&bars.full8[st8], ph8, P.err, abort_v)) return false;
+      const float ks = __half2float(__ushort_as_half(ks_s[st8][r]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.empty8[st8]);
+      if (++st8 == kStages8) { st8 = 0; ph8 ^= 1; }
       const int s = j * kTileKeys + r;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + acc * acc_stride;
       bool released = false;
       // Column n = gi * HI + h of the accumulator is token gi, head h.
       if (HI >= 32) {
         for (int gi = eg; gi < G.ntok; gi += 2) {
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
+          // Head-weighted ReLU sum with packed fp32x2 FMAs over head pairs.
+          uint64_t part[2] = {0ull, 0ull};
 #pragma unroll
           for (int c = 0; c < HI / 32; c += 2) {
             uint32_t v0[32], v1[32];
@@ -472,16 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               release();
               released = true;
             }
-            const float* cf = coef + gi * HI + c * 32;
+            const uint64_t* cf = reinterpret_cast<const uint64_t*>(coef + gi * HI + c * 32);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) part[k & 3] = fmaf(cf[k], fmaxf(__uint_as_float(v0[k]), 0.f), part[k & 3]);
+            for (int k = 0; k < 16; ++k)
+              part[k & 1] = fma_f32x2(cf[k], relu_pair(v0[2 * k], v0[2 * k + 1]), part[k & 1]);
             if (c + 1 < HI / 32) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k)
-                part[k & 3] = fmaf(cf[32 + k], fmaxf(__uint_as_float(v1[k]), 0.f), part[k & 3]);
+              for (int k = 0; k < 16; ++k)
+                part[k & 1] = fma_f32x2(cf[16 + k], relu_pair(v1[2 * k], v1[2 * k + 1]), part[k & 1]);
             }
           }
-          const float sacc = (part[0] + part[1]) + (part[2] + part[3]);
+          const float sacc = (lo_f32(part[0]) + hi_f32(part[0])) + (lo_f32(part[1]) + hi_f32(part[1]));
           const bool vis = s <= tok_pos[gi];
           const float val = vis ? sacc * ks : ninf;
           P.scores[static_cast<size_t>(G.t0 + gi) * P.ld + s] = val;
@@ -516,30 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    griddep_wait();  // w, qs and the new rows' ks come from the previous kernel
-    // Walk with two prefetch registers: at the top of the loop ks_a holds
-    // the current item (wc) and ks_b the next one (wa).
-    Walker wc = w0;
-    bool more = wc.left > 0;
-    Walker wa = wc;
-    bool more_a = more && walk_next(tiles_prefix, P.n_groups, wa);
-    bool ok_a = false, ok_b = false;
-    unsigned short ks_a = more ? load_ks(wc, ok_a) : 0;
-    unsigned short ks_b = more_a ? load_ks(wa, ok_b) : 0;
+    griddep_wait();  // w and qs come from the previous kernel
     bool aborted = false;
-    while (more) {
-      Walker wb = wa;
-      bool more_b = more_a && walk_next(tiles_prefix, P.n_groups, wb);
-      if (!score_item(wc, ks_a, ok_a)) { aborted = true; break; }
-      if (more_b) ks_a = load_ks(wb, ok_a);
-      wc = wa; more = more_a; wa = wb; more_a = more_b;
-      if (!more) break;
-      wb = wa;
-      more_b = more_a && walk_next(tiles_prefix, P.n_groups, wb);
-      if (!score_item(wc, ks_b, ok_b)) { aborted = true; break; }
-      if (more_b) ks_b = load_ks(wb, ok_b);
-      wc = wa; more = more_a; wa = wb; more_a = more_b;
-    }
+    Walker w = w0;
+    for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w))
+      if (!score_item(w)) { aborted = true; break; }
     if (do_hist && cur_g >= 0 && !aborted) flush_hist();
   }
   tc_fence_before();

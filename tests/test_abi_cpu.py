@@ -93,6 +93,13 @@ def test_host_validation_rejects_before_launch(lib):
     t.H_I = 64
     assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 1        # null tensors
     assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) == 0            # invalid -> 0
+    base = 1 << 20  # fake, suitably aligned device addresses: only validated, never read
+    for i, f in enumerate(("q", "q_scale", "w", "k_cache", "k_scale", "pos", "topk_idx")):
+        setattr(t, f, base + i * 4096)
+    assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) > 0             # valid -> scores + histograms
+    t.k_scale = base + 4 * 4096 + 2
+    assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) == 0            # k_scale must be 16-byte aligned
+    assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 1
     at = B.AttnArgs()
     at.T, at.B, at.n_q, at.H, at.d_qk, at.d_v, at.topk, at.max_L, at.scale = 8, 4, 2, 128, 512, 512, 2048, 65536, 0.07
     assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 2        # d_qk 512
