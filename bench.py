@@ -7,7 +7,11 @@ top-k -> sparse MLA attention, B=4 sequences, MTP1 (2 query tokens each),
 
 Prints one JSON line (rank 0).  `value` is whole-job query tokens per
 second measured on the device (CUDA events on the launching stream, one CUDA
-graph per step, L2 flushed before every step, max over ranks); `e2e` repeats
+graph per step, max over ranks).  By default the steps rotate over 4
+independent device copies of every input (caches, weights, queries; about
+1.4 GB), so no step finds its inputs in the 126 MB L2 left by the steps
+before it; `--l2 flush` instead writes 256 MiB before every step (which also
+evicts the kernels' code from L2).  `e2e` repeats
 the step through the C ABI with host buffers (pinned H2D of the step's new
 inputs, D2H of the attention output) timed on the host; `roofline` is the
 dominant kernel's algorithmic bytes / its event-timed duration against the
@@ -178,53 +182,62 @@ def profiled_traffic(parts):
     return total
 
 
-def stage_times_in_graph(stage_fns, stream, flush, reps):
-    """Mean ms of each stage inside one graph of the whole step, from event
-    nodes recorded between the stages.  None if events cannot be captured."""
+def stage_times_in_graph(stage_fns_per_set, stream, prep, reps):
+    """Mean ms of each stage inside one graph of the whole step (one graph
+    per input set, replayed in rotation), from event nodes recorded between
+    the stages.  None if events cannot be captured."""
     try:
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stage_fns) + 1)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            evs[0].record(stream)
-            for i, (_, fn) in enumerate(stage_fns):
-                fn(stream)
-                evs[i + 1].record(stream)
-        acc = [[] for _ in stage_fns]
-        for r in range(reps + 2):
+        names = [n for n, _ in stage_fns_per_set[0]]
+        graphs = []
+        for fns in stage_fns_per_set:
+            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(fns) + 1)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                evs[0].record(stream)
+                for i, (_, fn) in enumerate(fns):
+                    fn(stream)
+                    evs[i + 1].record(stream)
+            graphs.append((g, evs))
+        acc = [[] for _ in names]
+        for r in range(reps + 2 * len(graphs)):
+            g, evs = graphs[r % len(graphs)]
             with torch.cuda.stream(stream):
-                flush.zero_()
+                prep()
                 g.replay()
             stream.synchronize()
-            if r >= 2:
-                for i in range(len(stage_fns)):
+            if r >= 2 * len(graphs):
+                for i in range(len(names)):
                     acc[i].append(evs[i].elapsed_time(evs[i + 1]))
     except (TypeError, RuntimeError):
         return None, None
-    return ({name: statistics.mean(a) for (name, _), a in zip(stage_fns, acc)},
-            "event nodes between the C calls inside one step graph (L2 flushed before each replay)")
+    return ({n: statistics.mean(a) for n, a in zip(names, acc)},
+            "event nodes between the C calls inside one step graph (same L2 policy as the timed steps)")
 
 
-def stage_times_separate(stage_fns, stream, flush, reps):
-    """Fallback: each stage in its own graph, replayed alone after a flush."""
+def stage_times_separate(stage_fns_per_set, stream, prep, reps):
+    """Fallback: each stage in its own graph, replayed alone."""
     out = {}
-    for name, fn in stage_fns:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            fn(stream)
+    for si, (name, _) in enumerate(stage_fns_per_set[0]):
+        graphs = []
+        for fns in stage_fns_per_set:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                fns[si][1](stream)
+            graphs.append(g)
         t = []
-        for r in range(reps + 2):
+        for r in range(reps + 2 * len(graphs)):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
-                flush.zero_()
+                prep()
                 a.record(stream)
-                g.replay()
+                graphs[r % len(graphs)].replay()
                 b.record(stream)
             stream.synchronize()
-            if r >= 2:
+            if r >= 2 * len(graphs):
                 t.append(a.elapsed_time(b))
         out[name] = statistics.mean(t)
-    return out, "one graph per stage, replayed alone after an L2 flush"
+    return out, "one graph per stage, replayed alone (same L2 policy as the timed steps)"
 
 
 def run_ours(args, rank, world, local):
@@ -236,32 +249,48 @@ def run_ours(args, rank, world, local):
     B.load()
     inp = W.decode_64k(seed=D.replica_seed(1002, rank))
     p = W.decode_64k_prolog(seed=D.replica_seed(2002, rank))
-    kc = torch.from_numpy(inp.k_cache).to(dev)
-    ks = torch.from_numpy(inp.k_scale).to(dev)
-    pro = PrologBuffers(p, dev, kc, ks)
-    buf = DecodeBuffers(inp, dev, q_idx=pro.q_out, q_idx_scale=pro.q_scale_out, w_idx=pro.w_out, k_cache=kc,
-                        k_scale=ks, keep_scores=True)
+    n_sets = max(1, args.rotate) if args.l2 == "rotate" else 1
+    sets = []
+    for _ in range(n_sets):  # independent device copies of every input
+        kc = torch.from_numpy(inp.k_cache).to(dev)
+        ks = torch.from_numpy(inp.k_scale).to(dev)
+        pro = PrologBuffers(p, dev, kc, ks)
+        buf = DecodeBuffers(inp, dev, q_idx=pro.q_out, q_idx_scale=pro.q_scale_out, w_idx=pro.w_out, k_cache=kc,
+                            k_scale=ks, keep_scores=True)
+        sets.append((pro, buf))
+    pro, buf = sets[0]
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.l2 == "flush" else None
 
-    def step(s):
-        pro.run(s)
-        buf.run(s)
+    def prep():  # before every timed step, outside the events
+        if flush is not None:
+            flush.zero_()
 
+    def step_of(pr, bu):
+        def step(s):
+            pr.run(s)
+            bu.run(s)
+        return step
+
+    steps = [step_of(pr, bu) for pr, bu in sets]
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            step(stream)
+            for st in steps:
+                st(stream)
     stream.synchronize()
     if B.device_error() != 0:
         raise RuntimeError("device-side error during warm-up")
 
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
-        step(stream)
+    graphs = []
+    for st in steps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            st(stream)
+        graphs.append(g)
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            flush.zero_()
-            graph.replay()
+        for w in range(max(args.warmup, 3) * len(graphs)):
+            prep()
+            graphs[w % len(graphs)].replay()
     stream.synchronize()
 
     K = args.steps
@@ -272,9 +301,9 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for k in range(K):
-                flush.zero_()
+                prep()
                 starts[k].record(stream)
-                graph.replay()
+                graphs[k % len(graphs)].replay()
                 ends[k].record(stream)
         torch.cuda.synchronize()
         D.barrier()
@@ -287,12 +316,12 @@ def run_ours(args, rank, world, local):
     # Per-stage times inside the step: a second copy of the step graph with
     # event nodes at the boundaries of the three C calls (event nodes split
     # the programmatic-launch overlap, so this copy is not the timed one).
-    stage_fns = [("prolog", lambda s: pro.run(s)), ("indexer+topk", lambda s: buf.run_topk(s)),
-                 ("attention+combine", lambda s: buf.run_attn(s))]
+    stage_fns = [[("prolog", lambda s, pr=pr: pr.run(s)), ("indexer+topk", lambda s, bu=bu: bu.run_topk(s)),
+                  ("attention+combine", lambda s, bu=bu: bu.run_attn(s))] for pr, bu in sets]
     reps = min(max(K, 5), 50)
-    st_ms, stage_timing = stage_times_in_graph(stage_fns, stream, flush, reps)
+    st_ms, stage_timing = stage_times_in_graph(stage_fns, stream, prep, reps)
     if st_ms is None:
-        st_ms, stage_timing = stage_times_separate(stage_fns, stream, flush, reps)
+        st_ms, stage_timing = stage_times_separate(stage_fns, stream, prep, reps)
     idx = buf.topk_idx.cpu().numpy()
     peak, peak_kind = measured_peaks()
     alg = {"prolog": prolog_bytes(p), "indexer+topk": indexer_bytes(inp) + topk_bytes(inp),
@@ -304,26 +333,35 @@ def run_ours(args, rank, world, local):
     achieved = alg[dom] / (st_ms[dom] / 1e3) / 1e9
     step_bytes = sum(alg.values())
 
-    # end to end through the C ABI with host buffers
-    h2d = {"q_lora": pro.q_lora, "q_lora_scale": pro.q_lora_scale, "x": pro.x, "pos_prolog": pro.pos,
-           "slot": pro.slot, "pos": buf.pos, "q_attn": buf.q_attn}
-    pinned = {k: v.detach().cpu().pin_memory() for k, v in h2d.items()}
+    # end to end through the C ABI with host buffers: every step copies its
+    # new inputs (queries, positions, slots, hidden states) from pinned host
+    # memory into the input set it runs on and reads the attention output back
+    names = ["q_lora", "q_lora_scale", "x", "pos_prolog", "slot", "pos", "q_attn"]
+
+    def dev_inputs(pr, bu):
+        return {"q_lora": pr.q_lora, "q_lora_scale": pr.q_lora_scale, "x": pr.x, "pos_prolog": pr.pos,
+                "slot": pr.slot, "pos": bu.pos, "q_attn": bu.q_attn}
+
+    pinned = {k: v.detach().cpu().pin_memory() for k, v in dev_inputs(pro, buf).items()}
     out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
-    h2d_bytes = sum(v.numel() * v.element_size() for v in pinned.values())
+    h2d_bytes = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
     d2h_bytes = out_host.numel() * out_host.element_size()
     e2e_t = []
-    for k in range(min(K, 50) + 2):
+    n_e2e = min(K, 50) + 2 * len(sets)
+    for k in range(n_e2e):
+        pr, bu = sets[k % len(sets)]
+        dst = dev_inputs(pr, bu)
         with torch.cuda.stream(stream):
-            flush.zero_()
+            prep()
         stream.synchronize()
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
-            for name, host in pinned.items():
-                h2d[name].copy_(host, non_blocking=True)
-            step(stream)
-            out_host.copy_(buf.out, non_blocking=True)
+            for name in names:
+                dst[name].copy_(pinned[name], non_blocking=True)
+            steps[k % len(sets)](stream)
+            out_host.copy_(bu.out, non_blocking=True)
         stream.synchronize()
-        if k >= 2:
+        if k >= 2 * len(sets):
             e2e_t.append(time.perf_counter() - t0)
     e2e_s = D.max_over_ranks(statistics.mean(e2e_t), dev)
     e2e_value = tokens_total / e2e_s
@@ -334,7 +372,9 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "int8 indexer (exact f16 MMA), bf16 attention, fp32 accumulate",
         "data": "synthetic (seeded; replica r uses seed + 100 r)",
         "config": {"workload": WORKLOAD, "global_batch": inp.B * world, "query_tokens_per_step": int(tokens_total),
-                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "l2": (f"inputs larger than L2: {len(sets)} rotating device copies of every input "
+                          f"({len(sets) * 0.36:.1f} GB), no flush" if args.l2 == "rotate"
+                          else "flushed before every timed step (256 MiB write, outside the events)"),
                    "timing": "one CUDA graph per step, CUDA events on its stream", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
@@ -434,6 +474,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
+                    help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
+    ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -47,8 +47,8 @@ int sm_count() {
   return g_sms[d];
 }
 
-bool encode_tmap_u8_2d(void* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
-                       uint32_t box_rows, int swizzle_bytes) {
+bool encode_tmap(void* out, int dtype, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
+                 const uint32_t* box, int swizzle_bytes) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -62,17 +62,31 @@ bool encode_tmap_u8_2d(void* out, const void* base, uint64_t inner, uint64_t row
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
   }
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {row_stride};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
+  if (rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
   const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
-  const CUresult r = fn(static_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = fn(static_cast<CUtensorMap*>(out), static_cast<CUtensorMapDataType>(dtype),
+                        static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_u8_2d(void* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                       uint32_t box_rows, int swizzle_bytes) {
+  const uint64_t dims[2] = {inner, rows};
+  const uint64_t strides[1] = {row_stride};
+  const uint32_t box[2] = {static_cast<uint32_t>(inner), box_rows};
+  return encode_tmap(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, swizzle_bytes);
 }
 
 }  // namespace dsa

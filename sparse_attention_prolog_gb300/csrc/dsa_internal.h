@@ -18,6 +18,13 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Encodes a tiled tensor map (rank <= 5) into `out` (128 bytes, 64-aligned):
+// dtype is a CUtensorMapDataType, dims innermost first, strides in bytes of
+// dims 1..rank-1, box in elements; OOB elements read as zero.  Returns false
+// if the driver entry point is unavailable or rejects the map.
+bool encode_tmap(void* out, int dtype, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
+                 const uint32_t* box, int swizzle_bytes);
+
 // Encodes a 2-D tiled tensor map of uint8 rows (inner extent `inner` bytes,
 // `rows` rows, `row_stride` bytes apart) with box {inner, box_rows} and the
 // given swizzle (0 none, 64 or 128 bytes) into `out` (128 bytes, 64-aligned).
