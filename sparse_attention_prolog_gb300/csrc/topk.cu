@@ -267,14 +267,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
 // the k-th largest key's leading digit B and the number of keys above it
 // follow from that histogram alone.  One cluster of CS CTAs (<= 8) takes a
 // row; CTA r holds keys [r * kThreads * PER, (r + 1) * kThreads * PER) in
-// registers (one read of the row).  Keys above B go straight to the output;
-// the missing `need` keys of bin B are found by a radix select on the low 20
-// bits (two 10-bit passes) over the same registers, whose per-CTA histograms
-// are summed in CTA 0's shared memory with cluster atomics.  Output slots are
-// reserved the same way, one atomic per warp.  The row's histogram is left
-// zeroed for the next call.
+// registers (one read of the row).  Keys above B go straight to the output
+// (slots reserved with one cluster atomic per warp on CTA 0).  The missing
+// `need` keys are the largest of bin B, found by a radix select on the low
+// 20 bits (two 10-bit passes):
+//   - bin B holds at most kCandMax keys (the usual case): every CTA stores
+//     its bin-B keys into CTA 0's shared memory, the other CTAs leave after
+//     one cluster barrier, and CTA 0 selects among the candidates alone;
+//   - otherwise (heavy ties) the passes run over the registers of every CTA,
+//     with per-CTA histograms summed in CTA 0 by cluster atomics.
+// The row's histogram is left zeroed for the next call.
 constexpr int kHB = kTopkHistBins;
 constexpr int kLowBins = 1024;  // 10-bit digits of the second and third pass
+constexpr int kCandMax = 8192;  // bin-B keys CTA 0 can hold (dynamic shared memory)
 
 struct TopkHistParams {
   const float* scores;
@@ -333,8 +338,14 @@ __device__ __forceinline__ void find_from_top(const uint32_t (&mine)[PER], uint3
   if (lane == 31) sh[warp] = incl;
   if (tid == 0) sh[32] = 0xffffffffu;
   __syncthreads();
-  uint32_t before = incl - s;
-  for (int w2 = 0; w2 < warp; ++w2) before += sh[w2];
+  // exclusive offset of this warp: a shuffle scan of the warp totals
+  uint32_t wt = lane < kThreads / 32 ? sh[lane] : 0u, wincl = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += v;
+  }
+  uint32_t before = incl - s + __shfl_sync(0xffffffffu, wincl - wt, warp);
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     if (before < need && before + mine[i] >= need) {
@@ -351,12 +362,43 @@ __device__ __forceinline__ void find_from_top(const uint32_t (&mine)[PER], uint3
   __syncthreads();
 }
 
+// Reserves n_a slots from the 32-bit counter at cluster address ctr and n_b
+// from the one after it, with one 64-bit atomic per warp; returns each
+// thread's first slot of both.
+__device__ __forceinline__ void warp_reserve_pair(uint32_t ctr, uint32_t n_a, uint32_t n_b, uint32_t& p_a,
+                                                  uint32_t& p_b) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ia = n_a, ib = n_b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t va = __shfl_up_sync(0xffffffffu, ia, o);
+    const uint32_t vb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) { ia += va; ib += vb; }
+  }
+  const uint32_t ta = __shfl_sync(0xffffffffu, ia, 31), tb = __shfl_sync(0xffffffffu, ib, 31);
+  unsigned long long base = 0;
+  if (lane == 31 && (ta | tb)) {
+    const unsigned long long add = static_cast<unsigned long long>(ta) | (static_cast<unsigned long long>(tb) << 32);
+    asm volatile("atom.shared::cluster.add.u64 %0, [%1], %2;" : "=l"(base) : "r"(ctr), "l"(add) : "memory");
+  }
+  base = __shfl_sync(0xffffffffu, base, 31);
+  p_a = static_cast<uint32_t>(base) + ia - n_a;
+  p_b = static_cast<uint32_t>(base >> 32) + ib - n_b;
+}
+
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 template <int PER>
 __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistParams P) {
+  extern __shared__ __align__(16) uint2 cand[];  // CTA 0: [kCandMax] (key, index) of bin B
   __shared__ uint32_t sh[40];
   __shared__ uint32_t lh[2][kLowBins];  // this CTA's counts, passes 1 and 2
-  __shared__ uint32_t gh[2][kLowBins];  // CTA 0: the cluster's counts
-  __shared__ uint32_t cnt[4];           // CTA 0: output slot counters
+  __shared__ uint32_t gh[2][kLowBins];  // CTA 0: the cluster's counts (tie path)
+  __shared__ __align__(8) uint32_t cnt[4];  // CTA 0: slots above B, candidates (one u64), emission
   const int tid = threadIdx.x;
   const uint32_t rank = cluster_ctarank();
   uint32_t ncta;
@@ -366,6 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
     lh[0][i] = 0; lh[1][i] = 0; gh[0][i] = 0; gh[1][i] = 0;
   }
   if (tid < 4) cnt[tid] = 0;
+  // CTA 0's counters are zero before any peer's atomics: the arrive is here,
+  // the matching wait just before the first remote access, so the barrier
+  // overlaps the loads below.
+  cluster_arrive();
   griddep_launch_dependents();
   griddep_wait();  // scores and histogram come from the indexer
 
@@ -405,31 +451,94 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
     return;
   }
   const uint32_t ub = static_cast<uint32_t>(B);
-  cluster_sync();  // CTA 0's counters are zero; every CTA has read the histogram
-  {
+  const uint32_t cnt0 = mapa(smem_u32(cnt), 0);
+  auto zero_hist_slice = [&]() {  // once every CTA has read the histogram
     const int h0 = static_cast<int>(rank) * kHB / static_cast<int>(ncta);
     const int h1 = static_cast<int>(rank + 1) * kHB / static_cast<int>(ncta);
     for (int i = h0 + tid; i < h1; i += kThreads) hist[i] = 0;
-  }
-  const uint32_t cnt0 = mapa(smem_u32(cnt), 0);
+  };
+  cluster_wait();
 
-  // Keys above the leading digit: output slots [0, c_above).
+  // Keys above the leading digit take output slots [0, c_above); keys of
+  // bin B become candidates in CTA 0 (fast path).  One 64-bit cluster
+  // atomic per warp reserves both kinds (cnt[0] counts the first, cnt[1]
+  // the second).
+  const bool fast = c_bin <= static_cast<uint32_t>(kCandMax);
+  uint32_t p_above, p_cand;
   {
-    uint32_t n = 0;
+    uint32_t n_a = 0, n_c = 0;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) n += (valid(e) && (keys[e] >> 20) > ub) ? 1u : 0u;
-    uint32_t p = warp_reserve_n(cnt0, n);
+    for (int e = 0; e < PER; ++e) {
+      n_a += (valid(e) && (keys[e] >> 20) > ub) ? 1u : 0u;
+      n_c += (fast && valid(e) && (keys[e] >> 20) == ub) ? 1u : 0u;
+    }
+    warp_reserve_pair(cnt0, n_a, n_c, p_above, p_cand);
+  }
 #pragma unroll
-    for (int e = 0; e < PER; ++e)
-      if (valid(e) && (keys[e] >> 20) > ub) {
-        if (p < c_above) out[p] = lo + tid + e * kThreads;
-        ++p;
+  for (int e = 0; e < PER; ++e)
+    if (valid(e) && (keys[e] >> 20) > ub) {
+      if (p_above < c_above) out[p_above] = lo + tid + e * kThreads;
+      ++p_above;
+    }
+  uint32_t need = static_cast<uint32_t>(k) - c_above;
+
+  if (fast) {
+    // ---------------- bin B to CTA 0, which selects among the candidates
+    {
+      const uint32_t cand0 = mapa(smem_u32(cand), 0);
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        if (valid(e) && (keys[e] >> 20) == ub) {
+          if (p_cand < static_cast<uint32_t>(kCandMax))
+            st_cluster_v2(cand0 + p_cand * 8, keys[e], static_cast<uint32_t>(lo + tid + e * kThreads));
+          ++p_cand;
+        }
+    }
+    cluster_arrive();  // candidates stored; every CTA has read the histogram
+    cluster_wait();
+    zero_hist_slice();
+    if (rank != 0) return;
+    const uint32_t n_cand = min(cnt[1], static_cast<uint32_t>(kCandMax));
+    if (tid == 0 && n_cand != c_bin) atomicOr(P.err, kErrBadIndex);
+    uint32_t prefix = ub << 20, mask = 0xFFF00000u;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 10 : 0;
+      for (uint32_t i = tid; i < n_cand; i += kThreads) {
+        const uint32_t key = cand[i].x;
+        if ((key & mask) == prefix) atomicAdd(&lh[pass][(key >> shift) & (kLowBins - 1)], 1u);
       }
+      __syncthreads();
+      uint32_t g1[1] = {lh[pass][kLowBins - 1 - tid]};
+      int bn;
+      uint32_t ab, cb;
+      find_from_top<1>(g1, need, bn, ab, cb, sh);
+      if (bn < 0) {  // cannot happen when the histogram matches the row
+        if (tid == 0) atomicOr(P.err, kErrBadIndex);
+        bn = 0;
+      }
+      need -= ab;
+      prefix |= static_cast<uint32_t>(bn) << shift;
+      mask |= static_cast<uint32_t>(kLowBins - 1) << shift;
+    }
+    // prefix is the k-th largest key; `need` of its copies are taken after
+    // the keys of bin B above it.
+    const uint32_t thr = prefix;
+    const uint32_t base_eq = static_cast<uint32_t>(k) - need;
+    for (uint32_t i = tid; i < n_cand; i += kThreads) {
+      const uint2 c = cand[i];
+      if (c.x > thr) {
+        const uint32_t q = atomicAdd(&cnt[2], 1u);
+        if (c_above + q < base_eq) out[c_above + q] = static_cast<int32_t>(c.y);
+      } else if (c.x == thr) {
+        const uint32_t q = atomicAdd(&cnt[3], 1u);
+        if (q < need) out[base_eq + q] = static_cast<int32_t>(c.y);
+      }
+    }
+    return;
   }
 
-  // Radix select of the `need` largest keys inside bin B (bits 19..10, then
-  // 9..0).
-  uint32_t need = static_cast<uint32_t>(k) - c_above;
+  // ---------------- heavy ties: radix passes over every CTA's registers
   uint32_t prefix = ub << 20, mask = 0xFFF00000u;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
@@ -443,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
       if (v) red_add_cluster(mapa(smem_u32(&gh[pass][tid]), 0), v);
     }
     cluster_sync();
+    if (pass == 0) zero_hist_slice();
     uint32_t g1[1] = {ld_cluster_u32(mapa(smem_u32(&gh[pass][kLowBins - 1 - tid]), 0))};
     int bn;
     uint32_t ab, cb;
@@ -467,8 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
       n_gt += (inb && keys[e] > thr) ? 1u : 0u;
       n_eq += (inb && keys[e] == thr) ? 1u : 0u;
     }
-    uint32_t pg = base_gt + warp_reserve_n(cnt0 + 4, n_gt);
-    uint32_t pe = warp_reserve_n(cnt0 + 8, n_eq);
+    uint32_t pg = base_gt + warp_reserve_n(cnt0 + 8, n_gt);
+    uint32_t pe = warp_reserve_n(cnt0 + 12, n_eq);
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const bool inb = valid(e) && (keys[e] >> 20) == ub;
@@ -539,12 +649,14 @@ int launch_topk_hist(const dsa_topk_args& a, const float* scores, int64_t ld, vo
   attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(a.T * cs);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kCandMax * sizeof(uint2);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = per == 8 ? cudaLaunchKernelEx(&cfg, topk_hist_kernel<8>, P)
-                           : cudaLaunchKernelEx(&cfg, topk_hist_kernel<16>, P);
+  cudaError_t e = cudaFuncSetAttribute(per == 8 ? topk_hist_kernel<8> : topk_hist_kernel<16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMax * (int)sizeof(uint2));
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  e = per == 8 ? cudaLaunchKernelEx(&cfg, topk_hist_kernel<8>, P) : cudaLaunchKernelEx(&cfg, topk_hist_kernel<16>, P);
   return cuda_status(e);
 }
 
