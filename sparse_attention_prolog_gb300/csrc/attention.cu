@@ -26,6 +26,7 @@
 //
 // Both CTAs gather the same rows (the second read is an L2 hit).  Chunks of
 // one token are merged by attn_combine_kernel with their log-sum-exp.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include "dsa_internal.h"
@@ -42,7 +43,10 @@ constexpr int kStageK = kAtomsK * kRows * 128;  // 73,728 B
 constexpr int kStageV = kAtomsV * kRows * 128;  // 65,536 B
 constexpr int kStagesK = 3, kStagesV = 2;
 constexpr int kPSlot = 128 * 128;               // P tile [128 heads x 64 rows] bf16
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;                // 14 warps, roles in the kernel
+constexpr int kGatherWarps = 8, kRowsPerWarp = 64 / kGatherWarps;  // rows of a tile per gather warp
+constexpr int kMmaWarp = 12, kRelayWarp = 13;
+constexpr int kOutAtom = 128 * 128;  // output staging atom [128 heads x 64 cols] bf16
 constexpr uint32_t kPBytes = 128 * (8 * 16 + 4);  // P row + alpha, per tile
 constexpr uint32_t kFinalBytes = 128 * 8;
 constexpr uint32_t kTmemQ = 0, kTmemS = 288;    // CTA 0 column map
@@ -70,6 +74,7 @@ struct __align__(8) Bars {
   uint64_t vfull[kStagesV], vempty[kStagesV];   // CTA 1 gather ring
   uint64_t pfull[2], pcons[2];                  // CTA 1 P slots
   uint64_t ready[2], odone, ffull;              // CTA 1 correction / MMA
+  uint64_t alldone;                             // CTA 1: every PV MMA complete
   uint64_t qready;                              // CTA 0: q is in TMEM
 };
 
@@ -80,27 +85,30 @@ __device__ __forceinline__ int64_t kv_row(const AttnParams& P, int b, int s) {
 }
 
 // Physical row of the slot this lane looks up for tile slot0 of producer
-// warp pw (lane l covers row pw*16 + l%16); -1 for masked slots.
+// warp pw (lane l covers row pw*kRowsPerWarp + l%kRowsPerWarp); -1 for
+// masked slots.
 __device__ __forceinline__ long long gather_row(const AttnParams& P, const int32_t* idx_row, int b, int slot0,
                                                 int pw, int lane) {
-  const int slot = slot0 + pw * 16 + (lane & 15);
+  const int slot = slot0 + pw * kRowsPerWarp + (lane % kRowsPerWarp);
   const int s = (slot < P.topk) ? __ldg(idx_row + slot) : -1;
   return (s >= 0 && s < P.max_L) ? kv_row(P, b, s) : -1;
 }
 
 // Gathers the 64 rows of one tile into a swizzled stage: `atoms` 64-dim
-// atoms of every row, zero rows for masked slots.  Producer warp pw (0..3)
-// owns rows pw*16 .. pw*16+15 whose physical addresses (one per lane, see
-// gather_row, looked up a tile ahead) are broadcast by shuffle.  Lanes copy
-// consecutive 16-byte chunks of a row (coalesced) with cp.async.
+// atoms of every row, zero rows for masked slots.  Producer warp pw owns
+// rows pw*kRowsPerWarp .. +kRowsPerWarp-1 whose physical addresses (one per
+// lane, see gather_row, looked up a tile ahead) are broadcast by shuffle.
+// Lanes copy consecutive 16-byte chunks of a row (coalesced) with cp.async.
+// A random-row gather is bound by the memory requests an SM keeps in
+// flight, so eight warps of every CTA gather.
 __device__ __forceinline__ void gather_tile(const AttnParams& P, long long row, uint8_t* stage, int atoms, int pw,
                                             int lane) {
   const int chunks = atoms * 8;
   const uint32_t sbase = smem_u32(stage);
 #pragma unroll 4
-  for (int rr = 0; rr < 16; ++rr) {
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
     const long long prow = __shfl_sync(0xffffffffu, row, rr);
-    const int r = pw * 16 + rr;
+    const int r = pw * kRowsPerWarp + rr;
     const __nv_bfloat16* rsrc = P.kv + (prow >= 0 ? prow : 0) * kDqk;
     const uint32_t bytes = prow >= 0 ? 16u : 0u;
     for (int c = lane; c < chunks; c += 32)
@@ -108,7 +116,8 @@ __device__ __forceinline__ void gather_tile(const AttnParams& P, long long row, 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams P) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ AttnParams P, const __grid_constant__ CUtensorMap tmap_o) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -132,13 +141,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   uint8_t* sK = smem;                                           // CTA 0: K stages
 
   if (tid == 0) {
-    for (int i = 0; i < kStagesK; ++i) { mbar_init(&bars.kfull[i], 128); mbar_init(&bars.kempty[i], 1); }
+    for (int i = 0; i < kStagesK; ++i) { mbar_init(&bars.kfull[i], kGatherWarps * 32); mbar_init(&bars.kempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.sfull[i], 1); mbar_init(&bars.sempty[i], 4); mbar_init(&bars.pfree[i], 1);
       mbar_init(&bars.pfull[i], 1); mbar_init(&bars.pcons[i], 1); mbar_init(&bars.ready[i], 4);
     }
-    for (int i = 0; i < kStagesV; ++i) { mbar_init(&bars.vfull[i], 128); mbar_init(&bars.vempty[i], 1); }
+    for (int i = 0; i < kStagesV; ++i) { mbar_init(&bars.vfull[i], kGatherWarps * 32); mbar_init(&bars.vempty[i], 1); }
     mbar_init(&bars.odone, 1);
+    mbar_init(&bars.alldone, 1);
     mbar_init(&bars.ffull, 1);
     mbar_init(&bars.qready, 4);
     abort_flag = 0;
@@ -163,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
   griddep_wait();  // topk_idx comes from the previous kernel
 
   if (rank == 0) {
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 4 && warp < 4 + kGatherWarps) {
       // ------------------------------------------------ gather K (CTA 0)
       int st = 0;
       uint32_t ph = 0;
@@ -178,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         if (++st == kStagesK) { st = 0; ph ^= 1; }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
       // ---------------------------------------------- QK^T MMA (CTA 0)
       if (lane == 0) {
         const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
@@ -300,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
       st_async_v2(remote_final + hrow * 8, __float_as_uint(m_used), __float_as_uint(l_sum), remote_ffull);
     }
   } else {
-    if (warp >= 4 && warp < 8) {
+    bool ok = true;
+    if (warp >= 4 && warp < 4 + kGatherWarps) {
       // ------------------------------------------------ gather V (CTA 1)
       int st = 0;
       uint32_t ph = 0;
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         if (++st == kStagesV) { st = 0; ph ^= 1; }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
       // ------------------------------------------------- PV MMA (CTA 1)
       if (lane == 0) {
         const uint32_t idesc = idesc_f16(128, 256, kFmtBF16, 0, 1);
@@ -342,9 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
           mma_commit(&bars.pcons[ps]);
           mma_commit(&bars.odone);
           if (++st == kStagesV) { st = 0; ph ^= 1; }
+          if (j + 1 == n_tiles) mma_commit(&bars.alldone);
         }
       }
-    } else if (warp == 9) {
+    } else if (warp == kRelayWarp) {
       // ----------------------------------- relay: P slot consumed -> CTA 0
       if (lane == 0) {
         const uint32_t remote_pfree[2] = {mapa(smem_u32(&bars.pfree[0]), 0), mapa(smem_u32(&bars.pfree[1]), 0)};
@@ -356,10 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         }
       }
     } else if (warp < 4) {
-      // --------------------------------- correction + epilogue (CTA 1)
+      // ----------------------------------------- correction (CTA 1)
       const int hrow = warp * 32 + lane;
       int consumed = 0;  // odone phases observed
-      bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int ps = j & 1;
         if (!mbar_wait_cluster(&bars.pfull[ps], (j >> 1) & 1, P.err, abort_v)) { ok = false; break; }
@@ -393,62 +404,59 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
           ++consumed;
         }
       }
-      while (ok && consumed < n_tiles) {
-        if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
-        ++consumed;
-      }
+    }
+    if (warp < 8) {
+      // ------------------------------------------ epilogue (CTA 1, 8 warps)
+      // Every PV product is in O (alldone) and (m, l) of each head has
+      // arrived: normalise, convert to bf16 into a swizzled staging tile (the
+      // free V stages) and write it with TMA stores, 64 columns x 128 heads
+      // per box (heads past H are clipped by the tensor map).
+      if (ok && n_tiles > 0) ok = mbar_wait(&bars.alldone, 0, P.err, abort_v);
       if (ok) ok = mbar_wait_cluster(&bars.ffull, 0, P.err, abort_v);
       tc_fence_after();
+      const int hrow = (warp & 3) * 32 + lane;
+      const int half = warp >> 2;  // columns [256 half, 256 half + 256)
       const float2 ml = sFinal[hrow];
-      const int h = hb * 128 + hrow;
-      const bool empty = (n_tiles == 0) || !(ml.y > 0.f);
+      const bool empty = !ok || (n_tiles == 0) || !(ml.y > 0.f);
       const float inv_l = empty ? 0.f : 1.f / ml.y;
-      if (P.n_chunks == 1) {
-        __nv_bfloat16* orow = P.out + (static_cast<size_t>(t) * P.H + h) * kDv;
-        for (int c0 = 0; c0 < kDv; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + c0, v);
-          tmem_ld_wait();
-          if (h < P.H) {
-            uint32_t pk[16];
+#pragma unroll 1
+      for (int c0 = half * 256; c0 < half * 256 + 256; c0 += 64) {  // one atom per round
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_off + c0, v0);
+        tmem_ld32(tmem + lane_off + c0 + 32, v1);
+        tmem_ld_wait();
+        uint32_t pk[32];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float a = empty ? 0.f : __uint_as_float(v[2 * k]) * inv_l;
-              const float bb = empty ? 0.f : __uint_as_float(v[2 * k + 1]) * inv_l;
-              __nv_bfloat162 pb = __floats2bfloat162_rn(a, bb);
-              pk[k] = *reinterpret_cast<uint32_t*>(&pb);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          }
+        for (int k = 0; k < 16; ++k) {
+          __nv_bfloat162 pa = __floats2bfloat162_rn(__uint_as_float(v0[2 * k]) * inv_l, __uint_as_float(v0[2 * k + 1]) * inv_l);
+          __nv_bfloat162 pb = __floats2bfloat162_rn(__uint_as_float(v1[2 * k]) * inv_l, __uint_as_float(v1[2 * k + 1]) * inv_l);
+          pk[k] = empty ? 0u : *reinterpret_cast<uint32_t*>(&pa);
+          pk[16 + k] = empty ? 0u : *reinterpret_cast<uint32_t*>(&pb);
         }
-        if (h < P.H && P.lse != nullptr)
-          P.lse[static_cast<size_t>(t) * P.H + h] =
-              empty ? -__int_as_float(0x7f800000) : (ml.x + log2f(ml.y)) * 0.69314718055994531f;
-      } else {
-        __nv_bfloat16* orow = P.part_o + ((static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h) * kDv;
-        for (int c0 = 0; c0 < kDv; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + c0, v);
-          tmem_ld_wait();
-          if (h < P.H) {
-            uint32_t pk[16];
+        uint8_t* atom = sV + (c0 / 64) * kOutAtom;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float a = empty ? 0.f : __uint_as_float(v[2 * k]) * inv_l;
-              const float bb = empty ? 0.f : __uint_as_float(v[2 * k + 1]) * inv_l;
-              __nv_bfloat162 pb = __floats2bfloat162_rn(a, bb);
-              pk[k] = *reinterpret_cast<uint32_t*>(&pb);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          }
-        }
-        if (h < P.H)
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(atom + sw128_off(hrow, k)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      }
+      fence_proxy_async_smem();  // generic writes -> TMA store reads
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (warp == 0 && lane == 0) {
+        const int z = P.n_chunks == 1 ? t : t * P.n_chunks + chunk;
+        for (int a = 0; a < kAtomsV; ++a) tma_store_3d(&tmap_o, sV + a * kOutAtom, a * 64, hb * 128, z);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      const int h = hb * 128 + hrow;
+      if (warp < 4 && h < P.H) {
+        if (P.n_chunks == 1) {
+          if (P.lse != nullptr)
+            P.lse[static_cast<size_t>(t) * P.H + h] =
+                empty ? -__int_as_float(0x7f800000) : (ml.x + log2f(ml.y)) * 0.69314718055994531f;
+        } else {
           P.part_ml[(static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h] =
               empty ? make_float2(-__int_as_float(0x7f800000), 0.f) : make_float2(ml.x, ml.y);
+        }
       }
     }
   }
@@ -574,6 +582,17 @@ int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
   P.err = error_word();
   if (!P.err) return DSA_ERR_CUDA;
 
+  // output (or split-K partials): [Z, H, 512] bf16, stored as 64-column x
+  // 128-head boxes; heads past H are clipped by the map.
+  alignas(64) CUtensorMap tmap_o;
+  {
+    const uint64_t z = P.n_chunks == 1 ? static_cast<uint64_t>(a.T) : static_cast<uint64_t>(a.T) * P.n_chunks;
+    const uint64_t dims[3] = {static_cast<uint64_t>(kDv), static_cast<uint64_t>(a.H), z};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kDv) * 2, static_cast<uint64_t>(a.H) * kDv * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    void* base = P.n_chunks == 1 ? static_cast<void*>(P.out) : static_cast<void*>(P.part_o);
+    if (!encode_tmap(&tmap_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, 128)) return DSA_ERR_CUDA;
+  }
   const size_t smem = 1024 + static_cast<size_t>(kSmemA > kStagesV * kStageV + 2 * kPSlot + 2048
                                                     ? kSmemA
                                                     : kStagesV * kStageV + 2 * kPSlot + 2048);
@@ -593,7 +612,7 @@ int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, P);
+  e = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, P, tmap_o);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (P.n_chunks > 1) {
     cudaLaunchConfig_t c2 = {};

@@ -77,19 +77,10 @@ struct Group {
   int b, t0, ntok, maxpos;
 };
 
-// Packed fp32 pair helpers: d = a * b + c on both halves (one instruction),
-// max(x, 0) of two floats packed into one 64-bit register.
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
+// max(x, 0) of two floats packed into one 64-bit register (fma_f32x2 operand).
 __device__ __forceinline__ uint64_t relu_pair(uint32_t x, uint32_t y) {
-  const float a = fmaxf(__uint_as_float(x), 0.f), b = fmaxf(__uint_as_float(y), 0.f);
-  return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+  return pack_f32x2(fmaxf(__uint_as_float(x), 0.f), fmaxf(__uint_as_float(y), 0.f));
 }
-__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
 
 __device__ __forceinline__ Group group_of(const IdxParams& P, int g) {
   Group G;
