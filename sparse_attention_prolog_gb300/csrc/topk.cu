@@ -501,8 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
     const uint32_t n_cand = min(cnt[1], static_cast<uint32_t>(kCandMax));
     if (tid == 0 && n_cand != c_bin) atomicOr(P.err, kErrBadIndex);
     uint32_t prefix = ub << 20, mask = 0xFFF00000u;
+    bool whole_bin = false;  // the k-th key's digit group is taken entirely
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = 0; pass < 2 && !whole_bin; ++pass) {
       const int shift = pass == 0 ? 10 : 0;
       for (uint32_t i = tid; i < n_cand; i += kThreads) {
         const uint32_t key = cand[i].x;
@@ -520,17 +521,20 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
       need -= ab;
       prefix |= static_cast<uint32_t>(bn) << shift;
       mask |= static_cast<uint32_t>(kLowBins - 1) << shift;
+      // every key of the found group is needed: the lower bits do not matter
+      whole_bin = (cb == need);
     }
-    // prefix is the k-th largest key; `need` of its copies are taken after
-    // the keys of bin B above it.
-    const uint32_t thr = prefix;
+    // Keys of bin B above the group `prefix/mask` come first; then `need`
+    // keys of the group itself (all of it when whole_bin, else the copies of
+    // the k-th key `prefix`).
     const uint32_t base_eq = static_cast<uint32_t>(k) - need;
     for (uint32_t i = tid; i < n_cand; i += kThreads) {
       const uint2 c = cand[i];
-      if (c.x > thr) {
+      const uint32_t g = c.x & mask;
+      if (g > prefix) {
         const uint32_t q = atomicAdd(&cnt[2], 1u);
         if (c_above + q < base_eq) out[c_above + q] = static_cast<int32_t>(c.y);
-      } else if (c.x == thr) {
+      } else if (g == prefix) {
         const uint32_t q = atomicAdd(&cnt[3], 1u);
         if (q < need) out[base_eq + q] = static_cast<int32_t>(c.y);
       }
