@@ -170,11 +170,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_rows = max(0, min(128, P.H - hb * 128));  // real heads of this block
   cluster_sync();  // both CTAs' barriers are initialised before any remote use
   griddep_launch_dependents();
-  griddep_wait();  // topk_idx comes from the previous kernel
+  // Roles wait for the previous kernel (griddep_wait) only before reading
+  // what it wrote (topk_idx); q and the kv cache are this call's inputs, so
+  // q is in TMEM before the top-k has finished.
 
   if (rank == 0) {
     if (warp >= 4 && warp < 4 + kGatherWarps) {
       // ------------------------------------------------ gather K (CTA 0)
+      griddep_wait();
       int st = 0;
       uint32_t ph = 0;
       long long row_next = n_tiles > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.qready);
+      griddep_wait();  // the index rows come from the previous kernel
       const float ninf = -__int_as_float(0x7f800000);
       float m_used = ninf, l_sum = 0.f;
       int sb = 0;
@@ -313,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (warp >= 4 && warp < 4 + kGatherWarps) {
       // ------------------------------------------------ gather V (CTA 1)
+      griddep_wait();
       int st = 0;
       uint32_t ph = 0;
       long long row_next = n_tiles > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
