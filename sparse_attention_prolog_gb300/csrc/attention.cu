@@ -473,39 +473,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merges the split chunks of every (token, head): out = sum_c w_c O_c /
 // sum_c w_c with w_c = l_c 2^(m_c - M) (O_c already divided by l_c).
-// One warp per (token, head).  Chunks are taken kBatch at a time and every
-// load of a batch (its (m, l) pairs and its 1 KB partial rows) is issued
-// before any of them is used, so a batch costs one memory round trip.  The
-// running maximum is rescaled between batches like the online softmax.
+// One warp per (token, head, half of the 512 columns), 8 columns per lane.
+// Chunks are taken kBatch at a time and every load of a batch (its (m, l)
+// pairs and its partial rows) is issued before any of them is used, so a
+// batch costs one memory round trip.  The running maximum is rescaled
+// between batches like the online softmax.
 constexpr int kCombineBatch = 8;
 
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int th = blockIdx.x * 8 + warp;  // (token, head)
-  if (th >= P.T * P.H) return;
+  const int item = blockIdx.x * 8 + warp;  // (token, head, column half)
+  if (item >= P.T * P.H * 2) return;
+  const int th = item >> 1, half = item & 1;
   const int t = th / P.H, h = th % P.H;
+  const int col = half * 256 + lane * 8;  // this lane's 8 columns
   const float ninf = -__int_as_float(0x7f800000);
-  float acc[16];
+  float acc[8];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
   float M = ninf, wsum = 0.f;
   for (int c0 = 0; c0 < P.n_chunks; c0 += kCombineBatch) {
     float2 ml[kCombineBatch];
-    uint2 raw[kCombineBatch][4];
+    uint4 raw[kCombineBatch];
 #pragma unroll
     for (int i = 0; i < kCombineBatch; ++i) {
       const int c = c0 + i;
       const size_t row = (static_cast<size_t>(t) * P.n_chunks + c) * P.H + h;
       if (c < P.n_chunks) {
         ml[i] = __ldcg(P.part_ml + row);
-        const uint2* src = reinterpret_cast<const uint2*>(P.part_o + row * kDv);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) raw[i][k] = __ldcg(src + lane + 32 * k);
+        raw[i] = __ldcg(reinterpret_cast<const uint4*>(P.part_o + row * kDv + col));
       } else {
         ml[i] = make_float2(ninf, 0.f);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) raw[i][k] = make_uint2(0u, 0u);
+        raw[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     float Mb = M;
@@ -516,33 +516,30 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
     const float r = (M == ninf) ? 0.f : exp2f(M - Mb);
     wsum *= r;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] *= r;
+    for (int k = 0; k < 8; ++k) acc[k] *= r;
     M = Mb;
 #pragma unroll
     for (int i = 0; i < kCombineBatch; ++i) {
       const float wc = ml[i].y > 0.f ? ml[i].y * exp2f(ml[i].x - M) : 0.f;
       wsum += wc;
+      const uint32_t wds[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i][k].x));
-        const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i][k].y));
-        acc[4 * k] = fmaf(wc, a.x, acc[4 * k]);
-        acc[4 * k + 1] = fmaf(wc, a.y, acc[4 * k + 1]);
-        acc[4 * k + 2] = fmaf(wc, b2.x, acc[4 * k + 2]);
-        acc[4 * k + 3] = fmaf(wc, b2.y, acc[4 * k + 3]);
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wds[k]));
+        acc[2 * k] = fmaf(wc, f.x, acc[2 * k]);
+        acc[2 * k + 1] = fmaf(wc, f.y, acc[2 * k + 1]);
       }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* orow = P.out + (static_cast<size_t>(t) * P.H + h) * kDv;
+  uint32_t pk[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * k] * inv, acc[4 * k + 1] * inv);
-    __nv_bfloat162 c2 = __floats2bfloat162_rn(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
-    uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&c2));
-    *reinterpret_cast<uint2*>(orow + 4 * (lane + 32 * k)) = pk;
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+    pk[k] = *reinterpret_cast<uint32_t*>(&b2);
   }
-  if (lane == 0 && P.lse != nullptr)
+  *reinterpret_cast<uint4*>(P.out + (static_cast<size_t>(t) * P.H + h) * kDv + col) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  if (half == 0 && lane == 0 && P.lse != nullptr)
     P.lse[static_cast<size_t>(t) * P.H + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : ninf;
 }
 
@@ -621,7 +618,7 @@ int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (P.n_chunks > 1) {
     cudaLaunchConfig_t c2 = {};
-    c2.gridDim = dim3((a.T * a.H + 7) / 8);
+    c2.gridDim = dim3((a.T * a.H * 2 + 7) / 8);
     c2.blockDim = dim3(256);
     c2.dynamicSmemBytes = 0;
     c2.stream = s;
