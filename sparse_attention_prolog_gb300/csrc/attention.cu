@@ -443,15 +443,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k)
           *reinterpret_cast<uint4*>(atom + sw128_off(hrow, k)) =
               make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        // the 4 warps of this half have written the atom: store it while
+        // they convert the next one
+        fence_proxy_async_smem();  // generic writes -> TMA store reads
+        asm volatile("bar.sync %0, 128;" ::"r"(2 + half) : "memory");
+        if ((warp & 3) == 0 && lane == 0) {
+          const int z = P.n_chunks == 1 ? t : t * P.n_chunks + chunk;
+          tma_store_3d(&tmap_o, atom, c0, hb * 128, z);
+          bulk_commit_group();
+        }
       }
-      fence_proxy_async_smem();  // generic writes -> TMA store reads
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (warp == 0 && lane == 0) {
-        const int z = P.n_chunks == 1 ? t : t * P.n_chunks + chunk;
-        for (int a = 0; a < kAtomsV; ++a) tma_store_3d(&tmap_o, sV + a * kOutAtom, a * 64, hb * 128, z);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
+      if ((warp & 3) == 0 && lane == 0) bulk_wait_group_read0();
       const int h = hb * 128 + hrow;
       if (warp < 4 && h < P.H) {
         if (P.n_chunks == 1) {
