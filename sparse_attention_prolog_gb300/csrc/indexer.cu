@@ -171,9 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // then three f16 key tiles (DI/2 columns each), so that the converters
   // can run two tiles ahead of the MMA.
   const int acc_stride = (N + 31) & ~31;
-  const int n_acc = 3 * acc_stride + kStages16 * DI / 2 <= 512 ? 3 : 2;
+  // Three accumulators let the MMA of a tile run while the epilogue still
+  // reads the two before it; they take precedence over a third key stage.
+  const int n16 = 3 * acc_stride + kStages16 * DI / 2 <= 512 ? kStages16 : 2;
+  const int n_acc = 3 * acc_stride + n16 * DI / 2 <= 512 ? 3 : 2;
   const uint32_t a_col0 = n_acc * acc_stride;
-  const int need_cols = n_acc * acc_stride + kStages16 * DI / 2;
+  const int need_cols = n_acc * acc_stride + n16 * DI / 2;
   const uint32_t tmem_cols = need_cols <= 64 ? 64 : need_cols <= 128 ? 128 : need_cols <= 256 ? 256 : 512;
 
   if (tid == 0) {
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars.empty8[st8]);
       }
       if (++st8 == kStages8) { st8 = 0; ph8 ^= 1; }
-      if (++st16 == kStages16) { st16 = 0; ph16 ^= 1; }
+      if (++st16 == n16) { st16 = 0; ph16 ^= 1; }
     }
   } else if (warp == 13) {
     // -------------------------------------------------------- MMA issuer
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars.tfull[acc]);
         const bool group_ends = !more || w.g != g;
         if (group_ends) mma_commit(&bars.qempty);
-        if (++st16 == kStages16) { st16 = 0; ph16 ^= 1; }
+        if (++st16 == n16) { st16 = 0; ph16 ^= 1; }
         if (++acc == n_acc) { acc = 0; aph ^= 1; }
       }
     }
