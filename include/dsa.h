@@ -29,6 +29,15 @@
  *     bounded wait expired records it in a device error word that
  *     dsa_get_device_error() reads (DSA_ERR_DEVICE_TIMEOUT).
  *   - T = 0 (no query tokens) is a no-op returning DSA_OK.
+ *   - Kernels are launched with programmatic dependent launch: a call's
+ *     kernel may start while the kernel enqueued just before it on the
+ *     stream is still running, and waits for that kernel to complete before
+ *     it reads anything the kernel may have written.  The exceptions are
+ *     inputs that a decode step never produces in the kernel right before
+ *     the call, which are read as soon as the kernel starts: pos of
+ *     dsa_indexer_topk / dsa_indexer_scores and q of dsa_sparse_attn.  The
+ *     kernel enqueued just before such a call must not write them (an event
+ *     or a memcpy in between lifts the rule).
  */
 #ifndef DSA_H_
 #define DSA_H_
