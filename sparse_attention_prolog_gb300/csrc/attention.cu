@@ -43,9 +43,16 @@ constexpr int kStageK = kAtomsK * kRows * 128;  // 73,728 B
 constexpr int kStageV = kAtomsV * kRows * 128;  // 65,536 B
 constexpr int kStagesK = 3, kStagesV = 2;
 constexpr int kPSlot = 128 * 128;               // P tile [128 heads x 64 rows] bf16
-constexpr int kThreads = 448;                // 14 warps, roles in the kernel
-constexpr int kGatherWarps = 8, kRowsPerWarp = 64 / kGatherWarps;  // rows of a tile per gather warp
-constexpr int kMmaWarp = 12, kRelayWarp = 13;
+// 24 warps in six warpgroups: 0 softmax / correction (and half of the
+// epilogue), 1-4 gather, 5 MMA, relay and the other half of the epilogue.
+// The gather warpgroups give registers to the other two (setmaxnreg): the
+// launch grants 80 per thread, 768 x 80 = 128 x 168 + 512 x 40 + 128 x 152.
+constexpr int kThreads = 768;
+constexpr int kGatherWarps = 16, kRowsPerWarp = 64 / kGatherWarps;  // rows of a tile per gather warp
+constexpr int kMmaWarp = 20, kRelayWarp = 21;
+constexpr int kRegsLaunch = 80, kRegsSoftmax = 168, kRegsGather = 40, kRegsLast = 152;
+static_assert(128 * kRegsSoftmax + 4 * 128 * kRegsGather + 128 * kRegsLast <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr int kOutAtom = 128 * 128;  // output staging atom [128 heads x 64 cols] bf16
 constexpr uint32_t kPBytes = 128 * (8 * 16 + 4);  // P row + alpha, per tile
 constexpr uint32_t kFinalBytes = 128 * 8;
@@ -100,7 +107,7 @@ __device__ __forceinline__ long long gather_row(const AttnParams& P, const int32
 // lane, see gather_row, looked up a tile ahead) are broadcast by shuffle.
 // Lanes copy consecutive 16-byte chunks of a row (coalesced) with cp.async.
 // A random-row gather is bound by the memory requests an SM keeps in
-// flight, so eight warps of every CTA gather.
+// flight, so sixteen warps of every CTA gather.
 __device__ __forceinline__ void gather_tile(const AttnParams& P, long long row, uint8_t* stage, int atoms, int pw,
                                             int lane) {
   const int chunks = atoms * 8;
@@ -174,8 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // what it wrote (topk_idx); q and the kv cache are this call's inputs, so
   // q is in TMEM before the top-k has finished.
 
-  if (rank == 0) {
-    if (warp >= 4 && warp < 4 + kGatherWarps) {
+  if (warp >= 4 && warp < 4 + kGatherWarps) {
+    setmaxnreg_dec<kRegsGather>();
+    if (rank == 0) {
       // ------------------------------------------------ gather K (CTA 0)
       griddep_wait();
       int st = 0;
@@ -191,131 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++st == kStagesK) { st = 0; ph ^= 1; }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == kMmaWarp) {
-      // ---------------------------------------------- QK^T MMA (CTA 0)
-      if (lane == 0) {
-        const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
-        int st = 0, sb = 0;
-        uint32_t ph = 0, phs = 0;
-        if (n_tiles > 0 && mbar_wait(&bars.qready, 0, P.err, abort_v)) tc_fence_after();
-        for (int j = 0; j < n_tiles; ++j) {
-          if (!mbar_wait(&bars.kfull[st], ph, P.err, abort_v)) break;
-          if (!mbar_wait(&bars.sempty[sb], phs ^ 1, P.err, abort_v)) break;
-          fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
-          tc_fence_after();
-          const uint32_t base = smem_u32(sK + st * kStageK);
-          for (int kk = 0; kk < kDqk / 16; ++kk) {
-            const uint64_t bd = smem_desc(base + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
-            mma_ts(tmem + kTmemS + sb * kRows, tmem + kTmemQ + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars.kempty[st]);
-          mma_commit(&bars.sfull[sb]);
-          if (++st == kStagesK) { st = 0; ph ^= 1; }
-          if (++sb == 2) { sb = 0; phs ^= 1; }
-        }
-      }
-    } else if (warp < 4) {
-      // ------------------------------------------------- softmax (CTA 0)
-      const int hrow = warp * 32 + lane;
-      const uint32_t remote_p = mapa(smem_u32(sP), 1);
-      const uint32_t remote_alpha = mapa(smem_u32(sAlpha), 1);
-      const uint32_t remote_final = mapa(smem_u32(sFinal), 1);
-      const uint32_t remote_pfull[2] = {mapa(smem_u32(&bars.pfull[0]), 1), mapa(smem_u32(&bars.pfull[1]), 1)};
-      const uint32_t remote_ffull = mapa(smem_u32(&bars.ffull), 1);
-      // q row of this thread's head: global -> registers -> TMEM columns
-      // [0, 288), three atoms (24 independent 16-byte loads) per round.
-      {
-        const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (static_cast<size_t>(t) * P.H + hb * 128 + hrow) * kDqk);
-        const bool real = hrow < q_rows;
-#pragma unroll 1
-        for (int a0 = 0; a0 < kAtomsK; a0 += 3) {
-          uint4 v[24];
-#pragma unroll
-          for (int i = 0; i < 24; ++i) v[i] = real ? __ldg(qrow + a0 * 8 + i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int a = 0; a < 3; ++a) {
-            uint32_t r[32];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              r[4 * c] = v[a * 8 + c].x; r[4 * c + 1] = v[a * 8 + c].y;
-              r[4 * c + 2] = v[a * 8 + c].z; r[4 * c + 3] = v[a * 8 + c].w;
-            }
-            tmem_st32(tmem + lane_off + kTmemQ + (a0 + a) * 32, r);
-          }
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.qready);
-      griddep_wait();  // the index rows come from the previous kernel
-      const float ninf = -__int_as_float(0x7f800000);
-      float m_used = ninf, l_sum = 0.f;
-      int sb = 0;
-      uint32_t phs = 0;
-      bool ok = true;
-      // this lane's two index slots of a tile, loaded one tile ahead
-      auto load_idx = [&](int jj, int& lo, int& hi) {
-        const int slot0 = slot_begin + jj * kRows;
-        lo = (slot0 + lane < P.topk) ? __ldg(idx_row + slot0 + lane) : -1;
-        hi = (slot0 + 32 + lane < P.topk) ? __ldg(idx_row + slot0 + 32 + lane) : -1;
-      };
-      int nx_lo = -1, nx_hi = -1;
-      if (n_tiles > 0) load_idx(0, nx_lo, nx_hi);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s_lo = nx_lo, s_hi = nx_hi;
-        if (j + 1 < n_tiles) load_idx(j + 1, nx_lo, nx_hi);
-        if (!mbar_wait(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
-        const uint32_t v_lo = __ballot_sync(0xffffffffu, s_lo >= 0 && s_lo < P.max_L);
-        const uint32_t v_hi = __ballot_sync(0xffffffffu, s_hi >= 0 && s_hi < P.max_L);
-        tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tmem + lane_off + kTmemS + sb * kRows, s0);
-        tmem_ld32(tmem + lane_off + kTmemS + sb * kRows + 32, s1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.sempty[sb]);
-        float x[64];
-        float mt = ninf;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          x[k] = ((v_lo >> k) & 1u) ? __uint_as_float(s0[k]) * P.scale_log2 : ninf;
-          x[32 + k] = ((v_hi >> k) & 1u) ? __uint_as_float(s1[k]) * P.scale_log2 : ninf;
-          mt = fmaxf(mt, fmaxf(x[k], x[32 + k]));
-        }
-        float alpha = 1.f;
-        if (mt > m_used + 8.f) {  // also taken when m_used is -inf
-          alpha = ex2_approx(m_used - mt);
-          l_sum *= alpha;
-          m_used = mt;
-        }
-        uint32_t pk[32];
-        float lt = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = (x[2 * k] == ninf) ? 0.f : ex2_approx(x[2 * k] - m_used);
-          const float p1 = (x[2 * k + 1] == ninf) ? 0.f : ex2_approx(x[2 * k + 1] - m_used);
-          lt += p0 + p1;
-          __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          pk[k] = *reinterpret_cast<uint32_t*>(&pb);
-        }
-        l_sum += lt;
-        const int ps = j & 1;
-        if (!mbar_wait_cluster(&bars.pfree[ps], ((j >> 1) & 1) ^ 1, P.err, abort_v)) { ok = false; break; }
-        const uint32_t prow = remote_p + ps * kPSlot;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(prow + sw128_off(hrow, c), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]),
-                      remote_pfull[ps]);
-        st_async_b32(remote_alpha + (ps * 128 + hrow) * 4, __float_as_uint(alpha), remote_pfull[ps]);
-        if (++sb == 2) { sb = 0; phs ^= 1; }
-      }
-      st_async_v2(remote_final + hrow * 8, __float_as_uint(m_used), __float_as_uint(l_sum), remote_ffull);
-    }
-  } else {
-    bool ok = true;
-    if (warp >= 4 && warp < 4 + kGatherWarps) {
+    } else {
       // ------------------------------------------------ gather V (CTA 1)
       griddep_wait();
       int st = 0;
@@ -331,87 +215,217 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++st == kStagesV) { st = 0; ph ^= 1; }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == kMmaWarp) {
-      // ------------------------------------------------- PV MMA (CTA 1)
-      if (lane == 0) {
-        const uint32_t idesc = idesc_f16(128, 256, kFmtBF16, 0, 1);
-        int st = 0;
-        uint32_t ph = 0;
-        for (int j = 0; j < n_tiles; ++j) {
-          const int ps = j & 1;
-          if (!mbar_wait(&bars.vfull[st], ph, P.err, abort_v)) break;
-          if (!mbar_wait(&bars.ready[ps], (j >> 1) & 1, P.err, abort_v)) break;
-          fence_proxy_async_smem();  // cp.async / st.async data -> tensor core reads
-          tc_fence_after();
-          const uint32_t pbase = smem_u32(sP + ps * kPSlot);
-          const uint32_t vbase = smem_u32(sV + st * kStageV);
-          for (int kk = 0; kk < kRows / 16; ++kk) {
-            const uint64_t ad = smem_desc(pbase + kk * 32, 16, 1024, kSwizzle128B);
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-              const uint64_t bd = smem_desc(vbase + nh * 4 * (kRows * 128) + kk * 16 * 128, kRows * 128, 1024,
-                                            kSwizzle128B);
-              mma_ss(tmem + nh * 256, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+    }
+  } else {
+    bool ok = true;
+    if (warp < 4) {
+      setmaxnreg_inc<kRegsSoftmax>();
+      if (rank == 0) {
+        // ------------------------------------------------- softmax (CTA 0)
+        const int hrow = warp * 32 + lane;
+        const uint32_t remote_p = mapa(smem_u32(sP), 1);
+        const uint32_t remote_alpha = mapa(smem_u32(sAlpha), 1);
+        const uint32_t remote_final = mapa(smem_u32(sFinal), 1);
+        const uint32_t remote_pfull[2] = {mapa(smem_u32(&bars.pfull[0]), 1), mapa(smem_u32(&bars.pfull[1]), 1)};
+        const uint32_t remote_ffull = mapa(smem_u32(&bars.ffull), 1);
+        // q row of this thread's head: global -> registers -> TMEM columns
+        // [0, 288), three atoms (24 independent 16-byte loads) per round.
+        {
+          const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (static_cast<size_t>(t) * P.H + hb * 128 + hrow) * kDqk);
+          const bool real = hrow < q_rows;
+  #pragma unroll 1
+          for (int a0 = 0; a0 < kAtomsK; a0 += 3) {
+            uint4 v[24];
+  #pragma unroll
+            for (int i = 0; i < 24; ++i) v[i] = real ? __ldg(qrow + a0 * 8 + i) : make_uint4(0, 0, 0, 0);
+  #pragma unroll
+            for (int a = 0; a < 3; ++a) {
+              uint32_t r[32];
+  #pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                r[4 * c] = v[a * 8 + c].x; r[4 * c + 1] = v[a * 8 + c].y;
+                r[4 * c + 2] = v[a * 8 + c].z; r[4 * c + 3] = v[a * 8 + c].w;
+              }
+              tmem_st32(tmem + lane_off + kTmemQ + (a0 + a) * 32, r);
             }
           }
-          mma_commit(&bars.vempty[st]);
-          mma_commit(&bars.pcons[ps]);
-          mma_commit(&bars.odone);
-          if (++st == kStagesV) { st = 0; ph ^= 1; }
-          if (j + 1 == n_tiles) mma_commit(&bars.alldone);
+          tmem_st_wait();
         }
-      }
-    } else if (warp == kRelayWarp) {
-      // ----------------------------------- relay: P slot consumed -> CTA 0
-      if (lane == 0) {
-        const uint32_t remote_pfree[2] = {mapa(smem_u32(&bars.pfree[0]), 0), mapa(smem_u32(&bars.pfree[1]), 0)};
-        for (int j = 0; j + 2 < n_tiles; ++j) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.qready);
+        griddep_wait();  // the index rows come from the previous kernel
+        const float ninf = -__int_as_float(0x7f800000);
+        float m_used = ninf, l_sum = 0.f;
+        int sb = 0;
+        uint32_t phs = 0;
+        bool ok = true;
+        // this lane's two index slots of a tile, loaded one tile ahead
+        auto load_idx = [&](int jj, int& lo, int& hi) {
+          const int slot0 = slot_begin + jj * kRows;
+          lo = (slot0 + lane < P.topk) ? __ldg(idx_row + slot0 + lane) : -1;
+          hi = (slot0 + 32 + lane < P.topk) ? __ldg(idx_row + slot0 + 32 + lane) : -1;
+        };
+        int nx_lo = -1, nx_hi = -1;
+        if (n_tiles > 0) load_idx(0, nx_lo, nx_hi);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int s_lo = nx_lo, s_hi = nx_hi;
+          if (j + 1 < n_tiles) load_idx(j + 1, nx_lo, nx_hi);
+          if (!mbar_wait(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
+          const uint32_t v_lo = __ballot_sync(0xffffffffu, s_lo >= 0 && s_lo < P.max_L);
+          const uint32_t v_hi = __ballot_sync(0xffffffffu, s_hi >= 0 && s_hi < P.max_L);
+          tc_fence_after();
+          uint32_t s0[32], s1[32];
+          tmem_ld32(tmem + lane_off + kTmemS + sb * kRows, s0);
+          tmem_ld32(tmem + lane_off + kTmemS + sb * kRows + 32, s1);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.sempty[sb]);
+          float x[64];
+          float mt = ninf;
+  #pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            x[k] = ((v_lo >> k) & 1u) ? __uint_as_float(s0[k]) * P.scale_log2 : ninf;
+            x[32 + k] = ((v_hi >> k) & 1u) ? __uint_as_float(s1[k]) * P.scale_log2 : ninf;
+            mt = fmaxf(mt, fmaxf(x[k], x[32 + k]));
+          }
+          float alpha = 1.f;
+          if (mt > m_used + 8.f) {  // also taken when m_used is -inf
+            alpha = ex2_approx(m_used - mt);
+            l_sum *= alpha;
+            m_used = mt;
+          }
+          uint32_t pk[32];
+          float lt = 0.f;
+  #pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float p0 = (x[2 * k] == ninf) ? 0.f : ex2_approx(x[2 * k] - m_used);
+            const float p1 = (x[2 * k + 1] == ninf) ? 0.f : ex2_approx(x[2 * k + 1] - m_used);
+            lt += p0 + p1;
+            __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            pk[k] = *reinterpret_cast<uint32_t*>(&pb);
+          }
+          l_sum += lt;
           const int ps = j & 1;
-          if (!mbar_wait(&bars.pcons[ps], (j >> 1) & 1, P.err, abort_v)) break;
-          mbar_arrive_expect_tx(&bars.pfull[ps], kPBytes);  // arm the slot's next use
-          mbar_arrive_remote(remote_pfree[ps]);
+          if (!mbar_wait_cluster(&bars.pfree[ps], ((j >> 1) & 1) ^ 1, P.err, abort_v)) { ok = false; break; }
+          const uint32_t prow = remote_p + ps * kPSlot;
+  #pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_async_v4(prow + sw128_off(hrow, c), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]),
+                        remote_pfull[ps]);
+          st_async_b32(remote_alpha + (ps * 128 + hrow) * 4, __float_as_uint(alpha), remote_pfull[ps]);
+          if (++sb == 2) { sb = 0; phs ^= 1; }
         }
-      }
-    } else if (warp < 4) {
-      // ----------------------------------------- correction (CTA 1)
-      const int hrow = warp * 32 + lane;
-      int consumed = 0;  // odone phases observed
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int ps = j & 1;
-        if (!mbar_wait_cluster(&bars.pfull[ps], (j >> 1) & 1, P.err, abort_v)) { ok = false; break; }
-        const float alpha = sAlpha[ps * 128 + hrow];
-        const bool need = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
-        if (need) {
-          // O must hold PV of tile j-1 before it is rescaled.
+        st_async_v2(remote_final + hrow * 8, __float_as_uint(m_used), __float_as_uint(l_sum), remote_ffull);
+      } else {
+        // ----------------------------------------- correction (CTA 1)
+        const int hrow = warp * 32 + lane;
+        int consumed = 0;  // odone phases observed
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int ps = j & 1;
+          if (!mbar_wait_cluster(&bars.pfull[ps], (j >> 1) & 1, P.err, abort_v)) { ok = false; break; }
+          const float alpha = sAlpha[ps * 128 + hrow];
+          const bool need = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
+          if (need) {
+            // O must hold PV of tile j-1 before it is rescaled.
+            while (consumed < j) {
+              if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
+              ++consumed;
+            }
+            if (!ok) break;
+            tc_fence_after();
+            for (int c0 = 0; c0 < kDv; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_off + c0, v);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+              tmem_st32(tmem + lane_off + c0, v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+          }
+          fence_proxy_async_smem();  // P arrived through st.async; the MMA reads it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.ready[ps]);
+          // keep at most one PV completion unobserved
           while (consumed < j) {
             if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
             ++consumed;
           }
-          if (!ok) break;
-          tc_fence_after();
-          for (int c0 = 0; c0 < kDv; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(tmem + lane_off + c0, v);
-          }
-          tmem_st_wait();
-          tc_fence_before();
         }
-        fence_proxy_async_smem();  // P arrived through st.async; the MMA reads it
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.ready[ps]);
-        // keep at most one PV completion unobserved
-        while (consumed < j) {
-          if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
-          ++consumed;
+      }
+    } else {
+      setmaxnreg_inc<kRegsLast>();
+      if (warp == kMmaWarp && rank == 0) {
+        // ---------------------------------------------- QK^T MMA (CTA 0)
+        if (lane == 0) {
+          const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
+          int st = 0, sb = 0;
+          uint32_t ph = 0, phs = 0;
+          if (n_tiles > 0 && mbar_wait(&bars.qready, 0, P.err, abort_v)) tc_fence_after();
+          for (int j = 0; j < n_tiles; ++j) {
+            if (!mbar_wait(&bars.kfull[st], ph, P.err, abort_v)) break;
+            if (!mbar_wait(&bars.sempty[sb], phs ^ 1, P.err, abort_v)) break;
+            fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
+            tc_fence_after();
+            const uint32_t base = smem_u32(sK + st * kStageK);
+            for (int kk = 0; kk < kDqk / 16; ++kk) {
+              const uint64_t bd = smem_desc(base + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
+              mma_ts(tmem + kTmemS + sb * kRows, tmem + kTmemQ + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars.kempty[st]);
+            mma_commit(&bars.sfull[sb]);
+            if (++st == kStagesK) { st = 0; ph ^= 1; }
+            if (++sb == 2) { sb = 0; phs ^= 1; }
+          }
+        }
+      } else if (warp == kMmaWarp) {
+        // ------------------------------------------------- PV MMA (CTA 1)
+        if (lane == 0) {
+          const uint32_t idesc = idesc_f16(128, 256, kFmtBF16, 0, 1);
+          int st = 0;
+          uint32_t ph = 0;
+          for (int j = 0; j < n_tiles; ++j) {
+            const int ps = j & 1;
+            if (!mbar_wait(&bars.vfull[st], ph, P.err, abort_v)) break;
+            if (!mbar_wait(&bars.ready[ps], (j >> 1) & 1, P.err, abort_v)) break;
+            fence_proxy_async_smem();  // cp.async / st.async data -> tensor core reads
+            tc_fence_after();
+            const uint32_t pbase = smem_u32(sP + ps * kPSlot);
+            const uint32_t vbase = smem_u32(sV + st * kStageV);
+            for (int kk = 0; kk < kRows / 16; ++kk) {
+              const uint64_t ad = smem_desc(pbase + kk * 32, 16, 1024, kSwizzle128B);
+  #pragma unroll
+              for (int nh = 0; nh < 2; ++nh) {
+                const uint64_t bd = smem_desc(vbase + nh * 4 * (kRows * 128) + kk * 16 * 128, kRows * 128, 1024,
+                                              kSwizzle128B);
+                mma_ss(tmem + nh * 256, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&bars.vempty[st]);
+            mma_commit(&bars.pcons[ps]);
+            mma_commit(&bars.odone);
+            if (++st == kStagesV) { st = 0; ph ^= 1; }
+            if (j + 1 == n_tiles) mma_commit(&bars.alldone);
+          }
+        }
+      } else if (warp == kRelayWarp && rank == 1) {
+        // ----------------------------------- relay: P slot consumed -> CTA 0
+        if (lane == 0) {
+          const uint32_t remote_pfree[2] = {mapa(smem_u32(&bars.pfree[0]), 0), mapa(smem_u32(&bars.pfree[1]), 0)};
+          for (int j = 0; j + 2 < n_tiles; ++j) {
+            const int ps = j & 1;
+            if (!mbar_wait(&bars.pcons[ps], (j >> 1) & 1, P.err, abort_v)) break;
+            mbar_arrive_expect_tx(&bars.pfull[ps], kPBytes);  // arm the slot's next use
+            mbar_arrive_remote(remote_pfree[ps]);
+          }
         }
       }
     }
-    if (warp < 8) {
-      // ------------------------------------------ epilogue (CTA 1, 8 warps)
+    if (rank == 1) {
+      // --------------------- epilogue (CTA 1, warpgroups 0 and 5: 8 warps)
       // Every PV product is in O (alldone) and (m, l) of each head has
       // arrived: normalise, convert to bf16 into a swizzled staging tile (the
       // free V stages) and write it with TMA stores, 64 columns x 128 heads
@@ -420,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = mbar_wait_cluster(&bars.ffull, 0, P.err, abort_v);
       tc_fence_after();
       const int hrow = (warp & 3) * 32 + lane;
-      const int half = warp >> 2;  // columns [256 half, 256 half + 256)
+      const int half = warp < 4 ? 0 : 1;  // columns [256 half, 256 half + 256)
       const float2 ml = sFinal[hrow];
       const bool empty = !ok || (n_tiles == 0) || !(ml.y > 0.f);
       const float inv_l = empty ? 0.f : 1.f / ml.y;

@@ -110,6 +110,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return mbar_wait_bounded<true>(bar, parity, err, abort_flag);
 }
 
+// Register reallocation between warpgroups (every thread of the warpgroup
+// executes the same instruction).
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------- cluster utilities
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
