@@ -100,8 +100,10 @@ int dsa_get_device_error(void* stream);
  * [T, H_I] (required iff w_proj != NULL).
  * Supported: 1 <= T <= 32, d_I in {64, 128}, 1 <= H_I <= 128, d_rope even
  * with d_rope <= d_I and (d_rope/2) a multiple of d_I/32, K_q <= 2048 and
- * D_x <= 12288, both multiples of 64.  Workspace: dsa_indexer_prolog_workspace() bytes; it must
- * be zero-filled once before its first use (the library leaves it zeroed).
+ * D_x <= 12288, both multiples of 64; x, w_k and w_proj 16-byte aligned.
+ * Workspace: dsa_indexer_prolog_workspace() bytes; it must be zero-filled
+ * once before its first use (each call leaves it zeroed; after a call that
+ * ended in DSA_ERR_DEVICE_TIMEOUT, zero it again).
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t T, H_I, d_I, d_rope, K_q, D_x;

@@ -56,8 +56,8 @@ extern "C" int dsa_indexer_prolog_noalloc(const dsa_prolog_args* a, void* stream
   const int st = dsa::scratch_address(&scratch);
   if (st != DSA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The kernel's completion ticket (first 256 bytes) must start at zero; the
-  // array keeps whatever the previous call left there.
-  if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return DSA_ERR_CUDA;
+  // The kernel's completion ticket and its k / weight sums must start at
+  // zero; the array keeps whatever the previous call left there.
+  if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) return DSA_ERR_CUDA;
   return dsa_indexer_prolog(a, scratch, dsa::kNoAllocScratchBytes, stream);
 }

@@ -15,13 +15,17 @@
 //     partials through distributed shared memory.  Each CTA then finishes
 //     the tokens t = rank (mod 2): dequant -> RoPE -> Hadamard (warp
 //     butterfly over shuffles) -> int8 quantisation.
-//   * k / weight streams: CTAs of 8 output channels over the full D_x (the
-//     8 weight rows are bulk-copied into shared memory); fp32 results go to
-//     the workspace and the last CTA to finish (atomic ticket) runs
+//   * k / weight streams: split over D_x.  Each CTA takes a slice of
+//     64-column atoms of w_k, w_proj and x (TMA tiles, 128-byte swizzle)
+//     and forms its partial [channels x tokens] product on the tensor core
+//     (bf16 operands, fp32 accumulation in tensor memory), so a CTA reads
+//     its weight slice and only its slice of x.  The partial sums are added
+//     into the fp32 workspace; the last CTA to finish (atomic ticket) runs
 //     LayerNorm -> RoPE -> Hadamard -> quantisation, writes the key-cache
-//     rows and the weights.
+//     rows and the weights, and clears the workspace for the next call.
 // Every scale, RoPE row, gamma/beta and position an epilogue needs is
 // prefetched into shared memory while the weight slabs are in flight.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -33,12 +37,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kQSplit = 2;       // cluster size and K_q split of the q stream
-constexpr int kKwChannels = 8;   // output channels per k/weight CTA
+constexpr int kKwMaxAtoms = 6;   // 64-column atoms of D_x per k/weight CTA (shared memory)
+constexpr uint32_t kKwAtom = 128 * 128;  // [128 rows][64 bf16] operand atom
 constexpr int kMaxT = 32;
 constexpr int kMaxRope = 64;     // max d_rope / 2 entries per RoPE row
 
 struct PrologParams {
-  int T, H_I, d_I, d_rope, K_q, D_x, interleaved, n_q_ctas, n_kw_ctas, n_kw_channels;
+  int T, H_I, d_I, d_rope, K_q, D_x, interleaved, n_q_ctas, n_kw_ctas, n_kw_channels, kw_atoms;
   const int8_t* q_lora;
   const __half* q_lora_scale;
   const int8_t* w_qb;
@@ -61,7 +66,7 @@ struct PrologParams {
   int64_t cache_rows;
   float* w_out;
   uint32_t* ticket;  // workspace: last-CTA ticket (left at 0)
-  float* kw;         // workspace: [T, n_kw_channels]
+  float* kw;         // workspace: [T, n_kw_channels] fp32 sums (left at 0)
   uint32_t* err;
 };
 
@@ -290,9 +295,15 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
 }
 
 // ------------------------------------------------------- k / weight stream
-template <int DPL>
-__device__ void kw_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
+// CTA c owns the 64-column atoms [c*kw_atoms, (c+1)*kw_atoms) of D_x.  Its
+// partial products D0 = w_k[:, slice] . x[:, slice]^T (channels x tokens)
+// and D1 = w_proj[:, slice] . x[:, slice]^T come from M=128, N=NX bf16 MMAs
+// (rows past d_I / H_I and tokens past T are zero fill of the tiles).
+template <int DPL, int NX>
+__device__ void kw_stream(const PrologParams& P, const CUtensorMap* tm_wk, const CUtensorMap* tm_wp,
+                          const CUtensorMap* tm_x, uint8_t* smem_raw, Pre& pre) {
   constexpr int D = 32 * DPL;
+  constexpr uint32_t kAtomX = NX * 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x - P.n_q_ctas;
   if (cta >= P.n_kw_ctas) {  // padding CTA of the last cluster
@@ -300,30 +311,37 @@ __device__ void kw_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
     return;
   }
   const int T = P.T;
-  const int c0 = cta * kKwChannels;
-  const int nch = min(kKwChannels, P.n_kw_channels - c0);
-  const size_t row_bytes = static_cast<size_t>(P.D_x) * 2;
-  __nv_bfloat16* sWk = reinterpret_cast<__nv_bfloat16*>(smem);  // [nch][D_x]
-  __shared__ float red[kThreads / 32][8 * kKwChannels];
+  const int nb = P.kw_atoms;
+  const int x0 = cta * nb * 64;
+  const bool has_w = P.w_proj != nullptr;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA0 = smem;                // w_k atoms    [nb][128 rows][128 B]
+  uint8_t* sA1 = sA0 + nb * kKwAtom;  // w_proj atoms [nb][128 rows][128 B]
+  uint8_t* sB = sA1 + nb * kKwAtom;   // x atoms      [nb][NX rows][128 B]
   __shared__ bool is_last;
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar, mdone;
   __shared__ int abort_flag;
+  __shared__ uint32_t tmem_base;
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&mdone, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == 0) tmem_alloc(&tmem_base, 64);  // D0 in columns [0, NX), D1 in [32, 32 + NX)
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
   griddep_launch_dependents();
   griddep_wait();
-  if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nch * row_bytes));
-    __syncwarp();
-    for (int c = lane; c < nch; c += 32) {
-      const int ch = c0 + c;
-      const __nv_bfloat16* src = (ch < D) ? P.w_k + static_cast<size_t>(ch) * P.D_x
-                                          : P.w_proj + static_cast<size_t>(ch - D) * P.D_x;
-      bulk_g2s(sWk + static_cast<size_t>(c) * P.D_x, src, static_cast<uint32_t>(row_bytes), &bar);
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nb) * ((has_w ? 2u : 1u) * kKwAtom + kAtomX));
+    for (int a = 0; a < nb; ++a) {
+      const int xc = x0 + a * 64;  // atoms past D_x read as zero
+      tma_load_2d(sA0 + a * kKwAtom, tm_wk, xc, 0, &bar);
+      if (has_w) tma_load_2d(sA1 + a * kKwAtom, tm_wp, xc, 0, &bar);
+      tma_load_2d(sB + a * kAtomX, tm_x, xc, 0, &bar);
     }
   }
   // inputs of the last CTA's epilogue
@@ -334,83 +352,52 @@ __device__ void kw_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
   if (tid >= D && tid - D < T) pre.slot[tid - D] = __ldg(P.slot + (tid - D));
   prefetch_rope(P, pre, tid);
 
-  mbar_wait(&bar, 0, P.err, &abort_flag);
-  // Tokens in blocks of 8: each thread owns 16-byte column chunks of the
-  // weight rows (read once per block from shared memory) and streams the
-  // matching x chunks of the block's tokens from L2.
-  constexpr int kTB = 8;
-  for (int tb = 0; tb < T; tb += kTB) {
-    float acc[kTB][kKwChannels];
+  if (tid == 0) {
+    if (mbar_wait(&bar, 0, P.err, &abort_flag)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_f16(128, NX, kFmtBF16, 0, 0);
+      for (int a = 0; a < nb; ++a) {
 #pragma unroll
-    for (int t = 0; t < kTB; ++t)
-#pragma unroll
-      for (int c = 0; c < kKwChannels; ++c) acc[t][c] = 0.f;
-    // x chunks of the block's tokens, one iteration ahead (rows past T repeat
-    // the last row; their sums are discarded)
-    auto load_x = [&](int k, uint4 (&xv)[kTB]) {
-#pragma unroll
-      for (int t = 0; t < kTB; ++t)
-        xv[t] = __ldg(reinterpret_cast<const uint4*>(P.x + static_cast<size_t>(min(tb + t, T - 1)) * P.D_x + k));
-    };
-    uint4 xnext[kTB];
-    if (tid * 8 < P.D_x) load_x(tid * 8, xnext);
-    for (int k = tid * 8; k < P.D_x; k += kThreads * 8) {
-      uint4 xv[kTB];
-#pragma unroll
-      for (int t = 0; t < kTB; ++t) xv[t] = xnext[t];
-      if (k + kThreads * 8 < P.D_x) load_x(k + kThreads * 8, xnext);
-      float wf[kKwChannels][8];
-#pragma unroll
-      for (int c = 0; c < kKwChannels; ++c) {
-        uint4 wv = make_uint4(0, 0, 0, 0);
-        if (c < nch) wv = *reinterpret_cast<const uint4*>(sWk + static_cast<size_t>(c) * P.D_x + k);
-        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(w2[j]);
-          wf[c][2 * j] = f.x;
-          wf[c][2 * j + 1] = f.y;
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kTB; ++t) {
-        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv[t]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(x2[j]);
-#pragma unroll
-          for (int c = 0; c < kKwChannels; ++c) {
-            acc[t][c] = fmaf(f.x, wf[c][2 * j], acc[t][c]);
-            acc[t][c] = fmaf(f.y, wf[c][2 * j + 1], acc[t][c]);
-          }
+        for (int kk = 0; kk < 4; ++kk) {  // K = 16 per MMA, 32 bytes into the swizzled atom
+          const uint32_t acc = (a > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t bd = smem_desc(smem_u32(sB + a * kAtomX) + kk * 32, 16, 1024, kSwizzle128B);
+          mma_ss(tmem, smem_desc(smem_u32(sA0 + a * kKwAtom) + kk * 32, 16, 1024, kSwizzle128B), bd, idesc, acc);
+          if (has_w)
+            mma_ss(tmem + 32, smem_desc(smem_u32(sA1 + a * kKwAtom) + kk * 32, 16, 1024, kSwizzle128B), bd, idesc,
+                   acc);
         }
       }
     }
-    // Block reduction of every (token, channel) sum of this token block.
-#pragma unroll
-    for (int t = 0; t < kTB; ++t) {
-      if (tb + t < T) {
-#pragma unroll
-        for (int c = 0; c < kKwChannels; ++c) {
-          const float sum = warp_sum(acc[t][c]);
-          if (lane == 0) red[warp][t * kKwChannels + c] = sum;
-        }
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < kTB * kKwChannels; i += kThreads) {
-      const int t = i / kKwChannels, c = i % kKwChannels;
-      if (tb + t < T && c < nch) {
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) sum += red[w][i];
-        P.kw[static_cast<size_t>(tb + t) * P.n_kw_channels + c0 + c] = sum;
-      }
-    }
-    __syncthreads();
+    mma_commit(&mdone);
   }
+  if (warp < 4) {
+    // Row r of D0 / D1 (TMEM lane r) is channel r / d_I + r; column t is token t.
+    const bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag);
+    tc_fence_after();
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    uint32_t v[32];
+    tmem_ld32(lane_base, v);
+    tmem_ld_wait();
+    if (ok && r < D) {
+#pragma unroll
+      for (int t = 0; t < NX; ++t)
+        if (t < T) atomicAdd(P.kw + static_cast<size_t>(t) * P.n_kw_channels + r, __uint_as_float(v[t]));
+    }
+    if (has_w) {
+      tmem_ld32(lane_base + 32, v);
+      tmem_ld_wait();
+      if (ok && r < P.H_I) {
+#pragma unroll
+        for (int t = 0; t < NX; ++t)
+          if (t < T) atomicAdd(P.kw + static_cast<size_t>(t) * P.n_kw_channels + D + r, __uint_as_float(v[t]));
+      }
+    }
+  }
+  tc_fence_before();
   __threadfence();
   __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
   if (tid == 0) is_last = (atomicAdd(P.ticket, 1u) == static_cast<uint32_t>(P.n_kw_ctas - 1));
   __syncthreads();
   if (!is_last) return;
@@ -456,17 +443,21 @@ __device__ void kw_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
       P.w_out[i] = __ldcg(P.kw + static_cast<size_t>(t) * P.n_kw_channels + D + h) * P.w_scale;
     }
   }
+  __syncthreads();  // every sum is read: clear them for the next call
+  for (int i = tid; i < T * P.n_kw_channels; i += kThreads) P.kw[i] = 0.f;
   if (tid == 0) *P.ticket = 0u;  // ready for the next call
 }
 
 template <int DPL, int TM>
-__global__ void __launch_bounds__(kThreads, 1) prolog_kernel(const PrologParams P) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prolog_kernel(const __grid_constant__ PrologParams P, const __grid_constant__ CUtensorMap tm_wk,
+                  const __grid_constant__ CUtensorMap tm_wp, const __grid_constant__ CUtensorMap tm_x) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ Pre pre;
   if (static_cast<int>(blockIdx.x) < P.n_q_ctas) {
     q_stream<DPL, TM>(P, smem, pre);
   } else {
-    kw_stream<DPL>(P, smem, pre);
+    kw_stream<DPL, (TM < 16 ? 16 : TM)>(P, &tm_wk, &tm_wp, &tm_x, smem, pre);
   }
 }
 
@@ -483,7 +474,14 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   P.interleaved = a.rope_interleaved;
   P.n_q_ctas = a.H_I * kQSplit;
   P.n_kw_channels = a.d_I + (a.w_proj ? a.H_I : 0);
-  P.n_kw_ctas = (P.n_kw_channels + kKwChannels - 1) / kKwChannels;
+  // The k / weight CTAs split D_x into 64-column atoms, as few per CTA as
+  // the SMs left over by the q stream allow (at most kKwMaxAtoms).
+  const int atoms = a.D_x / 64;
+  const int spare = sm_count() - P.n_q_ctas;
+  const int want = spare >= 8 ? spare : 8;
+  P.kw_atoms = (atoms + want - 1) / want;
+  if (P.kw_atoms > kKwMaxAtoms) P.kw_atoms = kKwMaxAtoms;
+  P.n_kw_ctas = (atoms + P.kw_atoms - 1) / P.kw_atoms;
   P.q_lora = a.q_lora; P.q_lora_scale = reinterpret_cast<const __half*>(a.q_lora_scale);
   P.w_qb = a.w_qb; P.w_qb_scale = reinterpret_cast<const __half*>(a.w_qb_scale);
   P.x = reinterpret_cast<const __nv_bfloat16*>(a.x);
@@ -502,8 +500,28 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   const int kchunk = a.K_q / kQSplit;
   const size_t smem_q = static_cast<size_t>(a.d_I) * (kchunk + 16) + static_cast<size_t>(kMaxT) * kchunk +
                         static_cast<size_t>(kMaxT) * a.d_I * 4;
-  const size_t smem_kw = static_cast<size_t>(kKwChannels) * a.D_x * 2;
+  const int tm = a.T <= 8 ? 8 : (a.T <= 16 ? 16 : 32);
+  const int nx = tm < 16 ? 16 : tm;  // MMA N: tokens padded with zero rows
+  const size_t smem_kw = 1024 + static_cast<size_t>(P.kw_atoms) * (2 * kKwAtom + nx * 128);
   const size_t smem = smem_q > smem_kw ? smem_q : smem_kw;
+  // bf16 tiles of 64 columns x rows; rows past the tensor (channels past
+  // d_I or H_I, tokens past T) and columns past D_x read as zero.
+  alignas(64) CUtensorMap tm_wk, tm_wp, tm_x;
+  {
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.D_x) * 2};
+    const uint64_t dk[2] = {static_cast<uint64_t>(a.D_x), static_cast<uint64_t>(a.d_I)};
+    const uint64_t dx[2] = {static_cast<uint64_t>(a.D_x), static_cast<uint64_t>(a.T)};
+    const uint32_t box_w[2] = {64, 128}, box_x[2] = {64, static_cast<uint32_t>(nx)};
+    if (!encode_tmap(&tm_wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.w_k, dk, strides, box_w, 128) ||
+        !encode_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, dx, strides, box_x, 128))
+      return DSA_ERR_CUDA;
+    tm_wp = tm_wk;
+    if (a.w_proj) {
+      const uint64_t dp[2] = {static_cast<uint64_t>(a.D_x), static_cast<uint64_t>(a.H_I)};
+      if (!encode_tmap(&tm_wp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.w_proj, dp, strides, box_w, 128))
+        return DSA_ERR_CUDA;
+    }
+  }
   const int grid = P.n_q_ctas + static_cast<int>(round_up(P.n_kw_ctas, kQSplit));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -520,9 +538,8 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   cudaError_t e;
   auto go = [&](auto kern) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return r == cudaSuccess ? cudaLaunchKernelEx(&cfg, kern, P) : r;
+    return r == cudaSuccess ? cudaLaunchKernelEx(&cfg, kern, P, tm_wk, tm_wp, tm_x) : r;
   };
-  const int tm = a.T <= 8 ? 8 : (a.T <= 16 ? 16 : 32);
   if (a.d_I == 128) {
     e = tm == 8 ? go(prolog_kernel<4, 8>) : (tm == 16 ? go(prolog_kernel<4, 16>) : go(prolog_kernel<4, 32>));
   } else {

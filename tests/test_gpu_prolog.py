@@ -66,6 +66,29 @@ def test_prolog_small_heads_interleaved(cuda_lib):
     _run_and_check(p, cuda_lib)
 
 
+def test_prolog_repeated_calls_share_the_workspace(cuda_lib):
+    """The k / weight sums accumulate in the workspace and the call leaves
+    it zeroed: three calls on one workspace give the same checked result."""
+    p = W.decode_64k_prolog()
+    rows = 4 * 65536
+    kc = torch.full((rows, p.d_I), 99, dtype=torch.int8, device=DEV)
+    ks = torch.full((rows,), 7.0, dtype=torch.float16, device=DEV)
+    buf = PrologBuffers(p, DEV, kc, ks)
+    ref_cache = np.full((rows, p.d_I), 99, np.int8)
+    ref_cs = np.full(rows, 7.0, np.float16)
+    ref = O.indexer_prolog(p, ref_cache, ref_cs)
+    from sparse_attention_prolog_gb300 import binding
+    for _ in range(3):
+        buf.run()
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        check_codes(kc.cpu().numpy()[p.slot], ks.cpu().numpy()[p.slot], ref_cache[p.slot], ref_cs[p.slot], "k")
+        wg = buf.w_out.cpu().numpy().astype(np.float64)
+        wr = ref["w"].astype(np.float64)
+        assert np.abs(wg - wr).max() <= 1e-4 * max(1.0, np.abs(wr).max())
+    assert (buf.ws == 0).all(), "workspace not left zeroed"
+
+
 def test_prolog_zero_tokens_is_noop(cuda_lib):
     from sparse_attention_prolog_gb300 import binding as B
     p = W.prolog_alone()
