@@ -372,7 +372,8 @@ __device__ void kw_stream(const PrologParams& P, const CUtensorMap* tm_wk, const
   }
   if (warp < 4) {
     // Row r of D0 / D1 (TMEM lane r) is channel r / d_I + r; column t is token t.
-    const bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag);
+    // a CTA whose weight tiles never arrived adds nothing (its error is recorded)
+    const bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag) && !*static_cast<volatile int*>(&abort_flag);
     tc_fence_after();
     const int r = warp * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
