@@ -66,6 +66,15 @@ def test_prolog_small_heads_interleaved(cuda_lib):
     _run_and_check(p, cuda_lib)
 
 
+@pytest.mark.parametrize("d_I", [64, 128])
+def test_prolog_128_heads_two_waves(d_I, cuda_lib):
+    """H_I=128: 256 q CTAs (more than one wave), 256 k/weight channels, so the
+    D_x slices per k/weight CTA hit their shared-memory cap."""
+    p = W.make_prolog_inputs(T=3, pos=np.array([5, 900, 4000]), slot=np.array([0, 2, 1]), seed=91, H_I=128,
+                             d_I=d_I, K_q=512, D_x=3072, max_pos=4096)
+    _run_and_check(p, cuda_lib)
+
+
 def test_prolog_repeated_calls_share_the_workspace(cuda_lib):
     """The k / weight sums accumulate in the workspace and the call leaves
     it zeroed: three calls on one workspace give the same checked result."""
