@@ -21,11 +21,13 @@
 //   CTA 1  (PV): O [128 x 512] fp32 fills its whole TMEM; P (shared memory,
 //          K-major) times V (the first 512 dims of the gathered rows, read
 //          MN-major from the same swizzled layout) accumulates into O.
-//          Correction warps rescale O rows in the rare case the max grew,
-//          and finally normalise O and write it (or a split-K partial).
+//          Correction warps rescale O rows in the rare case the max grew;
+//          at the end they and the MMA warpgroup normalise O and write it
+//          (or a split-K partial) with TMA stores.
 //
-// Both CTAs gather the same rows (the second read is an L2 hit).  Chunks of
-// one token are merged by attn_combine_kernel with their log-sum-exp.
+// Both CTAs gather the same rows (the second read is an L2 hit), each with
+// 16 warps.  Chunks of one token are merged by attn_combine_kernel with
+// their log-sum-exp.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
