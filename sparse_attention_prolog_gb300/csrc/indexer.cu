@@ -246,17 +246,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
       int st = 0;
       uint32_t ph = 0;
-      int cur_g = -1, maxpos_cache = -1;
-      if (w0.left > 0) { cur_g = w0.g; maxpos_cache = group_of(P, w0.g).maxpos; }
+      // Per-group values are set at each group change; a contiguous cache
+      // loads a tile as one box at row b * max_L + s0, without the per-box
+      // arithmetic of the paged layout (this thread's loop is on the
+      // critical path of every tile).
+      const bool contiguous = P.block_table == nullptr;
+      int cur_g = -1, maxpos_cache = -1, b = 0;
+      int64_t row0 = 0;
+      auto set_group = [&](int g) {
+        const Group G = group_of(P, g);
+        cur_g = g;
+        maxpos_cache = G.maxpos;
+        b = G.b;
+        row0 = static_cast<int64_t>(b) * P.max_L;
+      };
+      if (w0.left > 0) set_group(w0.g);
       griddep_wait();  // the key cache holds rows the previous kernel wrote
       Walker w = w0;
       for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w)) {
         const int g = w.g, j = w.j;
-        const int b = g / P.groups_per_seq;
-        if (g != cur_g) { cur_g = g; maxpos_cache = group_of(P, g).maxpos; }
+        if (g != cur_g) set_group(g);
         if (!mbar_wait(&bars.empty8[st], ph ^ 1, P.err, abort_v)) break;
         uint8_t* dst = s8 + st * tile8_bytes;
         const int s0 = j * kTileKeys;
+        if (contiguous) {
+          const int64_t row = row0 + s0;
+          mbar_arrive_expect_tx(&bars.full8[st], static_cast<uint32_t>(kTileKeys * (DI + 2)));
+          tma_load_2d(dst, &tmap, 0, static_cast<int>(row), &bars.full8[st]);
+          bulk_g2s(&ks_s[st][0], P.k_scale + row, static_cast<uint32_t>(kTileKeys * 2), &bars.full8[st]);
+          if (++st == kStages8) { st = 0; ph ^= 1; }
+          continue;
+        }
         const int bh = P.box_rows;  // 128 (contiguous) or the page size (< 128)
         // Boxes of bh rows that cover the tile's visible keys (>= 1: the
         // walk only visits tiles with a visible key).
