@@ -228,28 +228,40 @@ def topk_indices(scores: np.ndarray, n_valid: int, k: int) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # Sparse Flash Attention  [V4-TileLang §Sparse Flash Attention steps 2-6, 8]
 # ----------------------------------------------------------------------------
-def sparse_attention_token(q_tok: np.ndarray, rows: np.ndarray, scale: float, d_v: int):
+def sparse_attention_token(q_tok: np.ndarray, rows: np.ndarray, scale: float, d_v: int, sink=None):
     """Softmax attention of q_tok [H, d_qk] over the selected latent rows
     [n, d_qk] (value = first d_v dims).  Returns (out [H, d_v], lse [H]),
     lse = natural log of sum_j exp(scale * q.k_j).  No rows: out 0, lse -inf.
-    Reading: the online softmax of the page computes exactly this; the
-    attention sink (step 7) is not applied."""
+    Reading: the online softmax of the page computes exactly this.
+
+    sink [H] (natural-log units) or None: the attention sink of
+    [V4-TileLang §Sparse Flash Attention] step 7, whose operator the page
+    prints garbled.  Read as one extra term exp(sink[h]) in each head's
+    softmax denominator, i.e. a virtual key with logit sink[h] and a zero
+    value: out = sum_j e^{s_j} v_j / (sum_j e^{s_j} + e^{sink}), lse =
+    log(sum_j e^{s_j} + e^{sink}); with no rows, out 0 and lse = sink."""
     q = np.asarray(q_tok, dtype=F64)
     H = q.shape[0]
+    sk = None if sink is None else np.asarray(sink, dtype=F64).reshape(H)
     if rows.shape[0] == 0:
-        return np.zeros((H, d_v)), np.full(H, -np.inf)
+        return np.zeros((H, d_v)), (np.full(H, -np.inf) if sk is None else sk.copy())
     kv = np.asarray(rows, dtype=F64)
     S = scale * (q @ kv.T)
     m = S.max(axis=1, keepdims=True)
+    if sk is not None:
+        m = np.maximum(m, sk[:, None])
     p = np.exp(S - m)
     l = p.sum(axis=1, keepdims=True)
+    if sk is not None:
+        l = l + np.exp(sk[:, None] - m)
     out = (p @ kv[:, :d_v]) / l
     return out, (m + np.log(l))[:, 0]
 
 
-def sparse_attention(inp, topk_idx: np.ndarray, tokens=None):
+def sparse_attention(inp, topk_idx: np.ndarray, tokens=None, sink=None):
     """Sparse attention for the given tokens of a workloads.DecodeInputs-like
-    object; index -1 selects nothing.  Returns (out [n_tok, H, d_v], lse)."""
+    object; index -1 selects nothing; optional per-head sink [H] (see
+    sparse_attention_token).  Returns (out [n_tok, H, d_v], lse)."""
     if tokens is None:
         tokens = range(inp.T)
     outs, lses = [], []
@@ -259,7 +271,7 @@ def sparse_attention(inp, topk_idx: np.ndarray, tokens=None):
         b = int(inp.seq_of_token[t])
         phys = np.asarray(inp.physical_row(b, idx)) if idx.size else np.zeros(0, np.int64)
         rows = bf16_bits_to_f64(inp.kv_cache[phys])
-        o, l = sparse_attention_token(bf16_bits_to_f64(inp.q_attn[t]), rows, inp.scale, inp.d_v)
+        o, l = sparse_attention_token(bf16_bits_to_f64(inp.q_attn[t]), rows, inp.scale, inp.d_v, sink)
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)

@@ -337,6 +337,35 @@ def test_attention_special_cases():
     np.testing.assert_allclose(o_dup, ref, rtol=1e-12)
 
 
+def test_attention_sink_is_a_zero_value_key_with_logit_sink():
+    """The sink reading, pinned by torch's SDPA: an extra key whose score is
+    the sink (a zero key row plus an additive mask of sink[h]) and whose
+    value row is zero."""
+    H, L, d, dv, scale = 4, 30, 576, 512, 192 ** -0.5
+    q = _bf16(rng.standard_normal((H, d)))
+    kv = _bf16(rng.standard_normal((L, d)))
+    sel = np.array([2, 9, 29, 14])
+    sink = np.array([-1.5, 0.3, 4.0, -np.inf])
+    out, lse = O.sparse_attention_token(q, kv[sel], scale, dv, sink)
+    keys = np.concatenate([kv[sel], np.zeros((1, d))])
+    vals = np.concatenate([kv[sel, :dv], np.zeros((1, dv))])
+    bias = np.zeros((H, len(sel) + 1))
+    bias[:, -1] = sink
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, None], torch.from_numpy(keys)[None].expand(H, -1, -1),
+        torch.from_numpy(vals)[None].expand(H, -1, -1), attn_mask=torch.from_numpy(bias)[:, None],
+        scale=scale)[:, 0].numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    scores = np.concatenate([scale * q @ kv[sel].T, sink[:, None]], axis=1)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(scores, axis=1), rtol=1e-12)
+    # sink -inf is no sink; no rows leave out = 0 and lse = sink
+    o0, l0 = O.sparse_attention_token(q, kv[sel], scale, dv)
+    np.testing.assert_array_equal(out[3], o0[3])
+    assert lse[3] == l0[3]
+    oe, le = O.sparse_attention_token(q, kv[:0], scale, dv, sink)
+    assert (oe == 0).all() and np.array_equal(le, sink)
+
+
 def test_attention_all_causal_keys_is_causal_attention():
     H, L, d, dv, scale = 2, 16, 576, 512, 192 ** -0.5
     q = _bf16(rng.standard_normal((L, H, d)))
