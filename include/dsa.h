@@ -233,7 +233,16 @@ int dsa_indexer_dots_debug(const dsa_topk_args* args, int32_t* dots, void* strea
  * over the rows r_j of token t's sequence named by topk_idx[t, j] >= 0
  * (logical positions; -1 selects nothing).  lse[t,h] = natural log of
  * sum_j exp(scale * q . k_j); a token with no selected row gets out = 0 and
- * lse = -inf.  The attention sink (step 7) is not applied.
+ * lse = -inf.
+ *
+ * sink: fp32 [H] or NULL.  The attention sink of step 7 (the page prints
+ * its operator garbled), read as one more term exp(sink[h]) in head h's
+ * softmax denominator - a key with logit sink[h] (natural-log units, like
+ * scale * q . k) and a zero value:
+ *   out[t,h,:] = sum_j e^{s_j} KV[r_j, :d_v] / (sum_j e^{s_j} + e^{sink[h]})
+ *   lse[t,h]   = log(sum_j e^{s_j} + e^{sink[h]})
+ * so a token with no selected row gets out = 0 and lse = sink[h].  Entries
+ * are finite or -inf (-inf = no sink for that head).
  *
  * Token layout: T = B * n_q, token t in sequence t / n_q.
  * Shapes: q bf16 [T, H, d_qk]; kv bf16 contiguous [B, max_L, d_qk] or paged
@@ -253,6 +262,7 @@ typedef struct {
   const int32_t* topk_idx;
   uint16_t* out;
   float* lse;
+  const float* sink;
 } dsa_attn_args;
 
 size_t dsa_sparse_attn_workspace(const dsa_attn_args* args);

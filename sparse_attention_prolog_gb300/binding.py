@@ -46,6 +46,7 @@ class AttnArgs(ctypes.Structure):
         ("T", c_int), ("B", c_int), ("n_q", c_int), ("H", c_int), ("d_qk", c_int), ("d_v", c_int), ("topk", c_int),
         ("max_L", c_int), ("scale", ctypes.c_float), ("q", c_ptr), ("kv", c_ptr), ("block_table", c_ptr),
         ("block_size", c_int), ("max_blocks", c_int), ("topk_idx", c_ptr), ("out", c_ptr), ("lse", c_ptr),
+        ("sink", c_ptr),
     ]
 
 
@@ -182,10 +183,10 @@ def dsa_topk_from_scores(args: TopkArgs, scores: torch.Tensor, stream=None):
 
 # -------------------------------------------------------------- attention
 def attn_args(T, B, n_q, H, topk, max_L, scale, q, kv, topk_idx, out, lse=None, block_table=None,
-              block_size=0, d_qk=576, d_v=512) -> AttnArgs:
+              block_size=0, d_qk=576, d_v=512, sink=None) -> AttnArgs:
     max_blocks = 0 if block_table is None else block_table.shape[1]
     return AttnArgs(T, B, n_q, H, d_qk, d_v, topk, max_L, float(scale), _p(q), _p(kv), _p(block_table),
-                    block_size, max_blocks, _p(topk_idx), _p(out), _p(lse))
+                    block_size, max_blocks, _p(topk_idx), _p(out), _p(lse), _p(sink))
 
 
 def dsa_sparse_attn(args: AttnArgs, workspace: Optional[torch.Tensor] = None, stream=None, device=None):

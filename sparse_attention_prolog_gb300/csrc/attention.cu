@@ -71,6 +71,7 @@ struct AttnParams {
   const int32_t* idx;
   __nv_bfloat16* out;
   float* lse;
+  const float* sink;      // [H] attention sink logits (natural-log units), or null
   __nv_bfloat16* part_o;  // [T][n_chunks][H][512], O_c / l_c, when n_chunks > 1
   float2* part_ml; // [T][n_chunks][H]: (max, sum) in log2 units
   uint32_t* err;
@@ -439,7 +440,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int half = warp < 4 ? 0 : 1;  // columns [256 half, 256 half + 256)
       const float2 ml = sFinal[hrow];
       const bool empty = !ok || (n_tiles == 0) || !(ml.y > 0.f);
-      const float inv_l = empty ? 0.f : 1.f / ml.y;
+      const int h = hb * 128 + hrow;
+      float inv_l = empty ? 0.f : 1.f / ml.y;
+      float lse2 = empty ? -__int_as_float(0x7f800000) : ml.x + log2f(ml.y);  // log2 units
+      if (P.sink != nullptr && P.n_chunks == 1) {
+        // The sink adds 2^s2 to the denominator; taken relative to
+        // max(m, s2) so that neither term overflows.  (Split chunks get
+        // it in attn_combine_kernel.)
+        const float s2 = (h < P.H ? __ldg(P.sink + h) : -__int_as_float(0x7f800000)) * 1.4426950408889634f;
+        if (!empty) {
+          const float mx = fmaxf(ml.x, s2);
+          const float den = ml.y * exp2f(ml.x - mx) + exp2f(s2 - mx);
+          inv_l = exp2f(ml.x - mx) / den;
+          lse2 = mx + log2f(den);
+        } else {
+          lse2 = s2;
+        }
+      }
 #pragma unroll 1
       for (int c0 = half * 256; c0 < half * 256 + 256; c0 += 64) {  // one atom per round
         uint32_t v0[32], v1[32];
@@ -470,12 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if ((warp & 3) == 0 && lane == 0) bulk_wait_group_read0();
-      const int h = hb * 128 + hrow;
       if (warp < 4 && h < P.H) {
         if (P.n_chunks == 1) {
-          if (P.lse != nullptr)
-            P.lse[static_cast<size_t>(t) * P.H + h] =
-                empty ? -__int_as_float(0x7f800000) : (ml.x + log2f(ml.y)) * 0.69314718055994531f;
+          if (P.lse != nullptr) P.lse[static_cast<size_t>(t) * P.H + h] = lse2 * 0.69314718055994531f;
         } else {
           P.part_ml[(static_cast<size_t>(t) * P.n_chunks + chunk) * P.H + h] =
               empty ? make_float2(-__int_as_float(0x7f800000), 0.f) : make_float2(ml.x, ml.y);
@@ -490,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merges the split chunks of every (token, head): out = sum_c w_c O_c /
-// sum_c w_c with w_c = l_c 2^(m_c - M) (O_c already divided by l_c).
+// (sum_c w_c [+ 2^(sink - M)]) with w_c = l_c 2^(m_c - M) (O_c already
+// divided by l_c); the optional attention sink is one more denominator term.
 // One warp per (token, head, half of the 512 columns), 8 columns per lane.
 // Chunks are taken kBatch at a time and every load of a batch (its (m, l)
 // pairs and its partial rows) is issued before any of them is used, so a
@@ -549,6 +564,23 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams P) {
       }
     }
   }
+  if (P.sink != nullptr) {
+    // one more term 2^s2 in the denominator (a zero-value key); -inf: none
+    const float s2 = __ldg(P.sink + h) * 1.4426950408889634f;
+    if (s2 != ninf) {
+      if (wsum > 0.f) {
+        const float mx = fmaxf(M, s2);
+        const float r = exp2f(M - mx);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] *= r;
+        wsum = wsum * r + exp2f(s2 - mx);
+        M = mx;
+      } else {  // nothing selected: out 0, lse = sink
+        M = s2;
+        wsum = 1.f;
+      }
+    }
+  }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   uint32_t pk[4];
 #pragma unroll
@@ -594,6 +626,7 @@ int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
   P.idx = a.topk_idx;
   P.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   P.lse = a.lse;
+  P.sink = a.sink;
   if (P.n_chunks > 1) {
     P.part_o = static_cast<__nv_bfloat16*>(ws);
     P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +

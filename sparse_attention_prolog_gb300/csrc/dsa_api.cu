@@ -153,6 +153,7 @@ int check_attn(const dsa_attn_args* a) {
   if (bad_ptr(a->q, 16) || bad_ptr(a->kv, 16) || bad_ptr(a->topk_idx, 4) || bad_ptr(a->out, 16))
     return DSA_ERR_INVALID_ARG;
   if (a->lse && !aligned(a->lse, 4)) return DSA_ERR_INVALID_ARG;
+  if (a->sink && !aligned(a->sink, 4)) return DSA_ERR_INVALID_ARG;
   if (a->block_table) {
     if (!aligned(a->block_table, 4) || a->block_size < 1) return DSA_ERR_INVALID_ARG;
     if (static_cast<long long>(a->max_blocks) * a->block_size != a->max_L) return DSA_ERR_INVALID_ARG;
@@ -186,7 +187,7 @@ const char* dsa_status_string(int status) {
   }
 }
 
-int dsa_abi_version(void) { return 100; }
+int dsa_abi_version(void) { return 101; }
 
 int dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;

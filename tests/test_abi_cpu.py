@@ -65,7 +65,7 @@ def test_status_strings(lib):
     from sparse_attention_prolog_gb300 import binding as B
     assert B.status_string(0) == "ok"
     assert "workspace" in B.status_string(3)
-    assert lib.dsa_abi_version() == 100
+    assert lib.dsa_abi_version() == 101
 
 
 def test_host_validation_rejects_before_launch(lib):

@@ -13,14 +13,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _attn_with_idx(inp, idx_np, tokens=None):
+def _attn_with_idx(inp, idx_np, tokens=None, sink=None):
     buf = DecodeBuffers(inp, DEV, with_attention=True)
     buf.topk_idx.copy_(torch.from_numpy(idx_np.astype(np.int32)))
+    if sink is not None:
+        sink_dev = torch.from_numpy(np.asarray(sink, np.float32)).to(DEV)
+        buf.aargs.sink = sink_dev.data_ptr()
     buf.run_attn()
     torch.cuda.synchronize()
     assert B.device_error() == 0
     tokens = list(range(inp.T)) if tokens is None else tokens
-    ref_o, ref_l = O.sparse_attention(inp, idx_np, tokens)
+    ref_o, ref_l = O.sparse_attention(inp, idx_np, tokens, sink)
     out = buf.out.float().cpu().numpy()[tokens]
     lse = buf.lse.cpu().numpy()[tokens]
     return check_attention(out, ref_o, lse, ref_l, "attn")
@@ -84,3 +87,34 @@ def test_heads_above_128(cuda_lib):
     inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[512], H_I=4, d_I=64, topk=128, H=160, seed=25)
     rng = np.random.default_rng(6)
     _attn_with_idx(inp, _random_idx(rng, inp))
+
+
+def _sinks(H, seed):
+    """Per-head sinks around the score range, with a head switched off
+    (-inf) and one that dominates its softmax."""
+    r = np.random.default_rng(seed)
+    sink = r.normal(0.0, 2.0, H)
+    sink[0] = -np.inf
+    sink[H - 1] = 40.0
+    return sink
+
+
+def test_attention_sink_single_chunk(cuda_lib):
+    """The sink applied in the attention epilogue (one chunk per token), a
+    token with nothing selected (out 0, lse = sink)."""
+    inp = W.tiny_decode()
+    rng = np.random.default_rng(31)
+    idx = _random_idx(rng, inp)
+    idx[1] = -1
+    _attn_with_idx(inp, idx, sink=_sinks(inp.H, 32))
+
+
+@pytest.mark.parametrize("topk", [200, 1000])
+def test_attention_sink_split_chunks(topk, cuda_lib):
+    """The sink applied once, in the merge of the split chunks."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[3001, 4096], H_I=4, d_I=64, topk=topk, H=128, seed=33)
+    rng = np.random.default_rng(34 + topk)
+    idx = _random_idx(rng, inp, frac_invalid=0.1)
+    idx[2] = -1
+    _attn_with_idx(inp, idx, sink=_sinks(inp.H, 35))
+
