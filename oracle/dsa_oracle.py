@@ -26,7 +26,7 @@ F64 = np.float64
 
 __all__ = [
     "bf16_bits_to_f64", "sylvester_hadamard", "hadamard_rows", "dynamic_quant",
-    "int8_gemm_dequant", "rope", "layer_norm", "indexer_prolog",
+    "int8_gemm_dequant", "act_quant", "rope", "layer_norm", "indexer_prolog",
     "indexer_dots", "indexer_scores_token", "topk_indices",
     "sparse_attention_token", "sparse_attention", "logical_rows",
 ]
@@ -85,6 +85,35 @@ def dynamic_quant(x: np.ndarray):
     y = np.clip(y, np.float32(-127.0), np.float32(127.0))
     codes = np.where(sdiv > 0, np.rint(y), np.float32(0.0))
     return codes.astype(np.int8), s16
+
+
+def act_quant(x_bits: np.ndarray, round_scale: bool = False):
+    """The standalone Activation Quantization operator of [V4-TileLang
+    §Activation Quantization] steps 1-4, on bf16 input (raw bits [M, N]).
+
+    (1) |x| in fp32 and its maximum per row (reading: "per column" in the
+    text, but the scale is indexed by row; one scale per row of N values,
+    as for the prolog's per-(token, head) rows); (2) scale = max / 127 in
+    fp32, and with round_scale the power of two at or above it (reading:
+    rounding up keeps |x / scale| <= 127); (3) y = round(clamp(x / scale,
+    -127, 127)), half to even, the division in fp32 (the page's precision,
+    and the one the quantiser's decision is taken in); the fp16 -> int8
+    casts of the page are exact for these integers; (4) both written back,
+    the scale as fp32.  A row of zeros gets scale 0 and codes 0.
+    Returns (codes int8 [M, N], scale fp32 [M])."""
+    x32 = bf16_bits_to_f64(x_bits).astype(np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s = amax / np.float32(127.0)
+    if round_scale:
+        m, e = np.frexp(s)  # s = m * 2^e, m in [0.5, 1) (s > 0)
+        up = np.where(m == 0.5, e - 1, e).astype(np.int32)
+        s = np.where(s > 0, np.ldexp(np.float32(1.0), up), np.float32(0.0)).astype(np.float32)
+    sd = s[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = x32 / sd
+    y = np.clip(y, np.float32(-127.0), np.float32(127.0))
+    codes = np.where(sd > 0, np.rint(y), np.float32(0.0))
+    return codes.astype(np.int8), s.astype(np.float32)
 
 
 # ----------------------------------------------------------------------------

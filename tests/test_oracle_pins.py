@@ -377,3 +377,53 @@ def test_attention_all_causal_keys_is_causal_attention():
     for t in range(L):
         out, _ = O.sparse_attention_token(q[t], kv[: t + 1], scale, dv)
         np.testing.assert_allclose(out, ref[t], rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------- Activation Quantization
+def _bits(x):
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    return f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def test_act_quant_hand_worked_rows():
+    """x = [1, -2.5, 0.5, 0]: scale 2.5/127, codes 51 -127 25 0 (1/s = 50.8,
+    0.5/s = 25.4); with round_scale the scale is 2^-5 (2.5/127 = 0.0197 lies
+    in (2^-6, 2^-5]) and the codes are 32 -80 16 0."""
+    x = _bits([[1.0, -2.5, 0.5, 0.0]])
+    y, s = O.act_quant(x)
+    assert s[0] == np.float32(2.5) / np.float32(127.0)
+    assert y.tolist() == [[51, -127, 25, 0]]
+    y2, s2 = O.act_quant(x, round_scale=True)
+    assert s2[0] == np.float32(2.0 ** -5)
+    assert y2.tolist() == [[32, -80, 16, 0]]
+
+
+def test_act_quant_properties():
+    r = np.random.default_rng(7)
+    x = r.standard_normal((64, 256)) * np.exp(r.uniform(-8, 8, (64, 1)))
+    x[3] = 0.0
+    xb = _bits(x)
+    xf = O.bf16_bits_to_f64(xb)
+    for rs in (False, True):
+        y, s = O.act_quant(xb, round_scale=rs)
+        amax = np.abs(xf).max(axis=1)
+        assert s[3] == 0 and (y[3] == 0).all()                      # zero row
+        nz = amax > 0
+        if rs:
+            m, _ = np.frexp(s[nz])
+            assert (m == 0.5).all()                                 # powers of two
+            assert (s[nz] >= amax[nz] / 127).all() and (s[nz] < 2 * amax[nz] / 127).all()
+            big = np.abs(y[nz].astype(int)).max(axis=1)
+            assert (big >= 63).all() and (big <= 127).all()
+        else:
+            assert (np.abs(y[nz].astype(int)).max(axis=1) == 127).all()  # the row max maps to +-127
+        err = np.abs(y.astype(np.float64) * s[:, None].astype(np.float64) - xf)
+        # half a step, plus the fp32 rounding of the quotient (<= 127 * 2^-24 steps)
+        assert (err <= (0.5 + 1e-5) * s[:, None].astype(np.float64)).all()
+    # where max/127 is exactly an fp16 value, the prolog's quantiser agrees
+    row = np.linspace(-15.875, 15.875, 128)
+    yp, sp = O.dynamic_quant(O.bf16_bits_to_f64(_bits(row))[None])
+    ya, sa = O.act_quant(_bits(row)[None])
+    assert float(sp[0]) == float(sa[0]) == 0.125
+    assert np.array_equal(yp, ya)
+
