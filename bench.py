@@ -495,6 +495,58 @@ def run_reference(args, rank, world):
     }
 
 
+def run_act_quant(args):
+    """The standalone activation quantiser on a [16384, 7168] bf16 matrix
+    (235 MB in, 118 MB out: larger than L2, so no flush is needed), timed
+    launch by launch with CUDA events; its roofline is the copy bandwidth
+    (2 bytes read + 1 written per element + 4 per row scale)."""
+    from sparse_attention_prolog_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, N = 16384, 7168
+    rng = np.random.default_rng(4242)
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    bits = f32_to_bf16_bits((rng.standard_normal((M, N)) * np.exp(rng.uniform(-4, 4, (M, 1)))).astype(np.float32))
+    x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.int8, device=dev)
+    sc = torch.empty((M,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            B.dsa_act_quant(x, y, sc, False, stream)
+    stream.synchronize()
+    K = min(args.steps, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(device_uuid(dev)) as clk:
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                a.record(stream)
+                B.dsa_act_quant(x, y, sc, False, stream)
+                b.record(stream)
+        stream.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    nbytes = M * N * 3 + M * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    res = {"metric": "act_quant GB/s (bf16 [16384,7168] -> int8 + fp32 row scales)", "value": round(gbs, 1),
+           "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+           "higher_is_better": True, "dtype": "bf16 in, fp32 scale, int8 out", "data": "synthetic (seeded)",
+           "config": {"workload": "act_quant M=16384 N=7168 round_scale=0",
+                      "l2": "inputs larger than L2 (235 MB read per launch)"},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+           "gpu_launches": K, "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        sample = bits[:512]
+        t0 = time.perf_counter()
+        O.act_quant(sample)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round((512 * N * 3 + 512 * 4) / dt / 1e9, 3), "unit": "GB/s",
+                               "cores": 1, "kind": "oracle", "sample": "512 rows of the same matrix, numpy"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,9 +559,14 @@ def main():
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
+    ap.add_argument("--op", choices=["step", "act_quant"], default="step",
+                    help="the decode step (default), or the standalone activation quantiser")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op == "act_quant":
+        print(json.dumps(run_act_quant(args)), flush=True)
+        return
     rank, world, local = D.init()
     if args.impl == "reference":
         if rank == 0:

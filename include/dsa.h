@@ -5,6 +5,7 @@
  *   dsa_indexer_prolog  : Indexer Prolog (q / k / weight streams)
  *   dsa_indexer_topk    : Lightning Indexer scores + per-query top-k
  *   dsa_sparse_attn     : Sparse (MLA) flash attention over the top-k rows
+ *   dsa_act_quant       : standalone activation quantisation (int8, per row)
  *
  * Page citations:
  *   [V3.2-PyPTO]  "NPU DeepSeek-V3.2-Exp PyPTO 融合算子开发优化实践",
@@ -267,6 +268,30 @@ typedef struct {
 
 size_t dsa_sparse_attn_workspace(const dsa_attn_args* args);
 int dsa_sparse_attn(const dsa_attn_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Activation Quantization  [V4-TileLang §Activation Quantization, steps
+ * 1-4] - a standalone export of the quantiser (the prolog fuses its own).
+ *
+ *   scale[m] = max_n |x[m,n]| / 127           (fp32; round_scale != 0: the
+ *                                               power of two at or above it)
+ *   y[m,n]   = rint(clamp(x[m,n] / scale[m], -127, 127))   (int8)
+ *
+ * One scale per row of N values; the quotient is an fp32 division and ties
+ * round to even; a row of zeros gets scale 0 and codes 0.
+ * Shapes: x bf16 [M, N] (16-byte aligned); y int8 [M, N] (8-byte aligned);
+ * scale fp32 [M].  Supported: 8 <= N <= 32768, N a multiple of 8.  No
+ * workspace.  M = 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t M, N;
+  const uint16_t* x;
+  int8_t* y;
+  float* scale;
+  int32_t round_scale;
+} dsa_act_quant_args;
+
+int dsa_act_quant(const dsa_act_quant_args* args, void* stream);
 
 #ifdef __cplusplus
 }

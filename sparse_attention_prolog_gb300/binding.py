@@ -50,12 +50,16 @@ class AttnArgs(ctypes.Structure):
     ]
 
 
+class ActQuantArgs(ctypes.Structure):
+    _fields_ = [("M", c_int), ("N", c_int), ("x", c_ptr), ("y", c_ptr), ("scale", c_ptr), ("round_scale", c_int)]
+
+
 EXPORTS = [
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error",
     "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
     "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
     "dsa_indexer_scores", "dsa_topk_from_scores",
-    "dsa_sparse_attn_workspace", "dsa_sparse_attn", "dsa_indexer_prolog_noalloc",
+    "dsa_sparse_attn_workspace", "dsa_sparse_attn", "dsa_indexer_prolog_noalloc", "dsa_act_quant",
 ]
 
 _lib = None
@@ -94,6 +98,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_indexer_scores.restype = c_int
     lib.dsa_topk_from_scores.argtypes = [ctypes.POINTER(TopkArgs), c_ptr, ctypes.c_int64, c_ptr]
     lib.dsa_topk_from_scores.restype = c_int
+    lib.dsa_act_quant.argtypes = [ctypes.POINTER(ActQuantArgs), c_ptr]
+    lib.dsa_act_quant.restype = c_int
     _lib = lib
     return lib
 
@@ -206,3 +212,11 @@ def workspace_bytes(kind: str, args) -> int:
 
 def device_error(stream=None) -> int:
     return int(load().dsa_get_device_error(_stream(stream)))
+
+
+def dsa_act_quant(x: torch.Tensor, y: torch.Tensor, scale: torch.Tensor, round_scale: bool = False, stream=None):
+    """x bf16 [M, N] -> y int8 [M, N], scale fp32 [M] (see dsa.h)."""
+    M, N = x.shape
+    args = ActQuantArgs(M, N, _p(x), _p(y), _p(scale), int(bool(round_scale)))
+    _check(load().dsa_act_quant(ctypes.byref(args), _stream(stream)), "dsa_act_quant")
+

@@ -270,4 +270,12 @@ int dsa_sparse_attn(const dsa_attn_args* a, void* ws, size_t ws_bytes, void* str
   return launch_attn(*a, ws, static_cast<cudaStream_t>(stream));
 }
 
+int dsa_act_quant(const dsa_act_quant_args* a, void* stream) {
+  if (!a || a->M < 0) return DSA_ERR_INVALID_ARG;
+  if (a->N < 8 || a->N % 8 != 0 || a->N > 32768) return DSA_ERR_UNSUPPORTED;
+  if (a->M == 0) return DSA_OK;
+  if (bad_ptr(a->x, 16) || bad_ptr(a->y, 8) || bad_ptr(a->scale, 4)) return DSA_ERR_INVALID_ARG;
+  return launch_act_quant(*a, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -44,7 +44,7 @@ def test_struct_layout_matches_header(lib, tmp_path):
     src = tmp_path / "layout.c"
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dsa.h"', "int main(void) {"]
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
-                      ("dsa_attn_args", B.AttnArgs)):
+                      ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs)):
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
         for f, _ in py._fields_:
             lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
@@ -55,7 +55,7 @@ def test_struct_layout_matches_header(lib, tmp_path):
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
     got = dict(line.split() for line in out if line)
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
-                      ("dsa_attn_args", B.AttnArgs)):
+                      ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs)):
         assert int(got[cname]) == ctypes.sizeof(py)
         for f, _ in py._fields_:
             assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, f"{cname}.{f}"
@@ -107,6 +107,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 1        # null tensors
     at.T = 0
     assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 0
+    assert lib.dsa_act_quant(None, null) == 1
+    aq = B.ActQuantArgs(4, 100, 1 << 20, 1 << 21, 1 << 22, 0)
+    assert lib.dsa_act_quant(ctypes.byref(aq), null) == 2                  # N % 8
+    aq.N = 64
+    aq.x = (1 << 20) + 8
+    assert lib.dsa_act_quant(ctypes.byref(aq), null) == 1                  # x not 16-byte aligned
+    aq.M = 0
+    assert lib.dsa_act_quant(ctypes.byref(aq), null) == 0                  # empty: no-op
 
 
 def test_missing_library_fails_loudly(tmp_path):
