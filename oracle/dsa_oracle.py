@@ -26,7 +26,7 @@ F64 = np.float64
 
 __all__ = [
     "bf16_bits_to_f64", "sylvester_hadamard", "hadamard_rows", "dynamic_quant",
-    "int8_gemm_dequant", "act_quant", "rope", "layer_norm", "indexer_prolog",
+    "int8_gemm_dequant", "int8_gemm", "act_quant", "rope", "layer_norm", "indexer_prolog",
     "indexer_dots", "indexer_scores_token", "topk_indices",
     "sparse_attention_token", "sparse_attention", "logical_rows",
 ]
@@ -130,6 +130,14 @@ def int8_gemm_dequant(a: np.ndarray, a_scale: np.ndarray, b: np.ndarray,
     precision up to the quantiser, no fp16 output cast)."""
     acc = np.asarray(a, dtype=F64) @ np.asarray(b, dtype=F64).T
     return acc * np.asarray(a_scale, dtype=F64)[:, None] * np.asarray(b_scale, dtype=F64)[None, :]
+
+
+def int8_gemm(a: np.ndarray, a_scale: np.ndarray, b: np.ndarray, b_scale: np.ndarray) -> np.ndarray:
+    """The standalone Int8 GEMM operator of [V4-TileLang §Int8 General Matrix
+    Multiplication] steps 1-4: the exact int32 product, dequantised by the
+    row scale of a and of b, and cast to the target type (fp16, the page's
+    example), rounding to nearest even.  Returns fp16 [M, N]."""
+    return int8_gemm_dequant(a, a_scale, b, b_scale).astype(np.float16)
 
 
 # ----------------------------------------------------------------------------

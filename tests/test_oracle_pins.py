@@ -427,3 +427,17 @@ def test_act_quant_properties():
     assert float(sp[0]) == float(sa[0]) == 0.125
     assert np.array_equal(yp, ya)
 
+
+def test_int8_gemm_fp16_output():
+    """The standalone operator is the exact product, dequantised, rounded
+    once to fp16: a hand-worked 1x1 case and the fp16 cast of the pinned
+    dequantised product."""
+    c = O.int8_gemm(np.array([[3, -2]], np.int8), np.array([0.5]), np.array([[4, 1]], np.int8), np.array([0.25]))
+    assert c.dtype == np.float16 and float(c[0, 0]) == (3 * 4 - 2 * 1) * 0.5 * 0.25
+    r = np.random.default_rng(11)
+    a = r.integers(-128, 128, (5, 96)).astype(np.int8)
+    b = r.integers(-128, 128, (7, 96)).astype(np.int8)
+    sa, sb = r.uniform(0.001, 0.1, 5), r.uniform(0.001, 0.1, 7)
+    exact = a.astype(np.int64) @ b.astype(np.int64).T
+    assert np.array_equal(O.int8_gemm(a, sa, b, sb), (exact * sa[:, None] * sb[None, :]).astype(np.float16))
+
