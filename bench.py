@@ -547,6 +547,57 @@ def run_act_quant(args):
     return res
 
 
+def run_int8_gemm(args):
+    """The standalone int8 GEMM for 8 decode rows against a [24576, 7168]
+    int8 weight (176 MB, larger than L2), timed launch by launch with CUDA
+    events; a weight stream, so its roofline is the copy bandwidth."""
+    from sparse_attention_prolog_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, N, K = 8, 24576, 7168
+    gen = torch.Generator(device=dev).manual_seed(77)
+    a = torch.randint(-128, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+    b = torch.randint(-128, 128, (N, K), dtype=torch.int8, device=dev, generator=gen)
+    sa = torch.full((M,), 1.0 / 128, dtype=torch.float32, device=dev)
+    sb = torch.full((N,), 1.0 / (128 * K ** 0.5), dtype=torch.float32, device=dev)
+    c = torch.empty((M, N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            B.dsa_int8_gemm(a, sa, b, sb, c, stream)
+    stream.synchronize()
+    K_steps = min(args.steps, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    with ClockSampler(device_uuid(dev)) as clk:
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                e0.record(stream)
+                B.dsa_int8_gemm(a, sa, b, sb, c, stream)
+                e1.record(stream)
+        stream.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    nbytes = N * K + M * K + M * N * 2 + (M + N) * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    res = {"metric": "int8_gemm GB/s (a int8 [8,7168] x b int8 [24576,7168] -> fp16)", "value": round(gbs, 1),
+           "unit": "GB/s", "n_gpus": 1, "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+           "higher_is_better": True, "dtype": "int8 in, int32 accumulate, fp32 dequant, fp16 out",
+           "data": "synthetic (seeded)", "config": {"workload": "int8_gemm M=8 N=24576 K=7168",
+                                                   "l2": "weight larger than L2 (176 MB per launch)"},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+           "gpu_launches": K_steps, "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        an, bn = a.cpu().numpy(), b[:512].cpu().numpy()
+        t0 = time.perf_counter()
+        O.int8_gemm(an, sa.cpu().numpy(), bn, sb[:512].cpu().numpy())
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(512 * K / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                               "sample": "512 weight rows of the same problem, numpy float64"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,13 +610,13 @@ def main():
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
-    ap.add_argument("--op", choices=["step", "act_quant"], default="step",
-                    help="the decode step (default), or the standalone activation quantiser")
+    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm"], default="step",
+                    help="the decode step (default), or a standalone export: the activation quantiser, the int8 GEMM")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.op == "act_quant":
-        print(json.dumps(run_act_quant(args)), flush=True)
+    if args.op in ("act_quant", "int8_gemm"):
+        print(json.dumps(run_act_quant(args) if args.op == "act_quant" else run_int8_gemm(args)), flush=True)
         return
     rank, world, local = D.init()
     if args.impl == "reference":

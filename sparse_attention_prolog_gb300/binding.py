@@ -54,12 +54,18 @@ class ActQuantArgs(ctypes.Structure):
     _fields_ = [("M", c_int), ("N", c_int), ("x", c_ptr), ("y", c_ptr), ("scale", c_ptr), ("round_scale", c_int)]
 
 
+class Int8GemmArgs(ctypes.Structure):
+    _fields_ = [("M", c_int), ("N", c_int), ("K", c_int), ("a", c_ptr), ("a_scale", c_ptr), ("b", c_ptr),
+                ("b_scale", c_ptr), ("c", c_ptr)]
+
+
 EXPORTS = [
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error",
     "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
     "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
     "dsa_indexer_scores", "dsa_topk_from_scores",
     "dsa_sparse_attn_workspace", "dsa_sparse_attn", "dsa_indexer_prolog_noalloc", "dsa_act_quant",
+    "dsa_int8_gemm",
 ]
 
 _lib = None
@@ -100,6 +106,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_topk_from_scores.restype = c_int
     lib.dsa_act_quant.argtypes = [ctypes.POINTER(ActQuantArgs), c_ptr]
     lib.dsa_act_quant.restype = c_int
+    lib.dsa_int8_gemm.argtypes = [ctypes.POINTER(Int8GemmArgs), c_ptr]
+    lib.dsa_int8_gemm.restype = c_int
     _lib = lib
     return lib
 
@@ -219,4 +227,13 @@ def dsa_act_quant(x: torch.Tensor, y: torch.Tensor, scale: torch.Tensor, round_s
     M, N = x.shape
     args = ActQuantArgs(M, N, _p(x), _p(y), _p(scale), int(bool(round_scale)))
     _check(load().dsa_act_quant(ctypes.byref(args), _stream(stream)), "dsa_act_quant")
+
+
+def dsa_int8_gemm(a: torch.Tensor, a_scale: torch.Tensor, b: torch.Tensor, b_scale: torch.Tensor,
+                  c: torch.Tensor, stream=None):
+    """a int8 [M, K], b int8 [N, K], fp32 scales -> c fp16 [M, N] (see dsa.h)."""
+    M, K = a.shape
+    N = b.shape[0]
+    args = Int8GemmArgs(M, N, K, _p(a), _p(a_scale), _p(b), _p(b_scale), _p(c))
+    _check(load().dsa_int8_gemm(ctypes.byref(args), _stream(stream)), "dsa_int8_gemm")
 

@@ -278,4 +278,14 @@ int dsa_act_quant(const dsa_act_quant_args* a, void* stream) {
   return launch_act_quant(*a, static_cast<cudaStream_t>(stream));
 }
 
+int dsa_int8_gemm(const dsa_int8_gemm_args* a, void* stream) {
+  if (!a || a->M < 0 || a->N < 0 || a->K < 0) return DSA_ERR_INVALID_ARG;
+  if (a->M > 32 || a->K < 16 || a->K % 16 != 0 || a->K > 65536) return DSA_ERR_UNSUPPORTED;
+  if (a->M == 0 || a->N == 0) return DSA_OK;
+  if (bad_ptr(a->a, 16) || bad_ptr(a->b, 16) || bad_ptr(a->a_scale, 4) || bad_ptr(a->b_scale, 4) ||
+      bad_ptr(a->c, 2))
+    return DSA_ERR_INVALID_ARG;
+  return launch_int8_gemm(*a, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

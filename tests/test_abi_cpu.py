@@ -44,7 +44,8 @@ def test_struct_layout_matches_header(lib, tmp_path):
     src = tmp_path / "layout.c"
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dsa.h"', "int main(void) {"]
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
-                      ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs)):
+                      ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs),
+                      ("dsa_int8_gemm_args", B.Int8GemmArgs)):
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
         for f, _ in py._fields_:
             lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
@@ -55,7 +56,8 @@ def test_struct_layout_matches_header(lib, tmp_path):
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
     got = dict(line.split() for line in out if line)
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
-                      ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs)):
+                      ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs),
+                      ("dsa_int8_gemm_args", B.Int8GemmArgs)):
         assert int(got[cname]) == ctypes.sizeof(py)
         for f, _ in py._fields_:
             assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, f"{cname}.{f}"
@@ -115,6 +117,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_act_quant(ctypes.byref(aq), null) == 1                  # x not 16-byte aligned
     aq.M = 0
     assert lib.dsa_act_quant(ctypes.byref(aq), null) == 0                  # empty: no-op
+    g = B.Int8GemmArgs(33, 64, 128, 1 << 20, 1 << 21, 1 << 22, 1 << 23, 1 << 24)
+    assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 2                   # M > 32
+    g.M, g.K = 8, 100
+    assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 2                   # K % 16
+    g.K, g.b = 128, (1 << 22) + 4
+    assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 1                   # b not 16-byte aligned
+    g.N = 0
+    assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 0                   # empty: no-op
 
 
 def test_missing_library_fails_loudly(tmp_path):

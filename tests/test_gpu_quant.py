@@ -37,3 +37,24 @@ def test_act_quant_bit_exact(M, N, round_scale, cuda_lib):
     ry, rs = O.act_quant(bits, round_scale=round_scale)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32)), "scales differ"
     assert np.array_equal(y.cpu().numpy(), ry), "codes differ"
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 8192, 1536), (1, 100, 16), (5, 300, 1008), (32, 256, 7168), (17, 129, 64)])
+def test_int8_gemm_matches_oracle(M, N, K, cuda_lib):
+    """Exact int32 sums, so the fp16 outputs agree to the last place up to
+    the fp32 rounding of the dequantisation (at most one fp16 ulp)."""
+    r = np.random.default_rng(M * 131 + N + K)
+    a = r.integers(-128, 128, (M, K)).astype(np.int8)
+    b = r.integers(-128, 128, (N, K)).astype(np.int8)
+    sa = r.uniform(0.5, 2.0, M).astype(np.float32) * np.float32(1.0 / 128)
+    sb = r.uniform(0.5, 2.0, N).astype(np.float32) / np.float32(128 * max(K, 64) ** 0.5)
+    c = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    B.dsa_int8_gemm(torch.from_numpy(a).to(DEV), torch.from_numpy(sa).to(DEV), torch.from_numpy(b).to(DEV),
+                    torch.from_numpy(sb).to(DEV), c)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    ref = O.int8_gemm(a, sa.astype(np.float64), b, sb.astype(np.float64)).astype(np.float64)
+    got = c.cpu().numpy().astype(np.float64)
+    ulp = np.maximum(np.abs(ref) * 2.0 ** -10, 2.0 ** -24)
+    assert np.isfinite(got).all()
+    assert (np.abs(got - ref) <= ulp).all(), f"max excess {np.max(np.abs(got - ref) / ulp):.2f} ulp"
