@@ -28,7 +28,7 @@ __all__ = [
     "bf16_bits_to_f64", "sylvester_hadamard", "hadamard_rows", "dynamic_quant",
     "int8_gemm_dequant", "int8_gemm", "act_quant", "rope", "layer_norm", "indexer_prolog",
     "indexer_dots", "indexer_scores_token", "topk_indices",
-    "sparse_attention_token", "sparse_attention", "logical_rows",
+    "sparse_attention_token", "sparse_attention", "logical_rows", "mhc",
 ]
 
 
@@ -312,3 +312,37 @@ def sparse_attention(inp, topk_idx: np.ndarray, tokens=None, sink=None):
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)
+
+
+# ----------------------------------------------------------------------------
+# Manifold-Constrained Hyper-Connections  [V4-TileLang §Manifold-Constrained
+# Hyper-Connections, steps 1-5]
+# ----------------------------------------------------------------------------
+def mhc(mixes: np.ndarray, hc_scale: np.ndarray, hc_base: np.ndarray, hc: int, iters: int, eps: float):
+    """pre [n, hc], post [n, hc], comb [n, hc, hc] from mixes [n, hc*(2+hc)].
+
+    Readings where the page is garbled or silent: a row of mixes holds the
+    pre part (hc values), the post part (hc) and the comb matrix (hc x hc,
+    row-major) - the only split that makes the page's row and column
+    normalisations of comb meaningful (it prints comb as [n, hc]); hc_scale
+    [3] scales the three parts in that order (step 1: mixes * scale +
+    hc_base); pre = sigmoid(.) + eps and post = 2 sigmoid(.) (steps 2-3,
+    whose printed operands are garbled); comb = softmax over each row + eps
+    (step 4), then divided by its column sums + eps, then `iters` rounds of
+    row sums + eps and column sums + eps (step 5, in the page's order)."""
+    x = np.asarray(mixes, dtype=F64)
+    n = x.shape[0]
+    sc = np.concatenate([np.full(hc, hc_scale[0]), np.full(hc, hc_scale[1]), np.full(hc * hc, hc_scale[2])])
+    z = x * sc + np.asarray(hc_base, dtype=F64)
+    sig = lambda v: 1.0 / (1.0 + np.exp(-v))
+    pre = sig(z[:, :hc]) + eps
+    post = 2.0 * sig(z[:, hc:2 * hc])
+    c = z[:, 2 * hc:].reshape(n, hc, hc)
+    c = np.exp(c - c.max(axis=-1, keepdims=True))
+    c = c / c.sum(axis=-1, keepdims=True) + eps
+    c = c / (c.sum(axis=-2, keepdims=True) + eps)
+    for _ in range(iters):
+        c = c / (c.sum(axis=-1, keepdims=True) + eps)
+        c = c / (c.sum(axis=-2, keepdims=True) + eps)
+    return pre, post, c
+

@@ -441,3 +441,36 @@ def test_int8_gemm_fp16_output():
     exact = a.astype(np.int64) @ b.astype(np.int64).T
     assert np.array_equal(O.int8_gemm(a, sa, b, sb), (exact * sa[:, None] * sb[None, :]).astype(np.float16))
 
+
+# ------------------------------------------- Manifold-constrained HC (mHC)
+def test_mhc_pins():
+    """Closed forms and the Sinkhorn fixed point: zero mixes and zero base
+    give pre = 1/2 + eps, post = 1, comb = the uniform doubly stochastic
+    matrix; with many iterations every comb is doubly stochastic (rows and
+    columns sum to 1 within eps); a scaled-up comb block becomes a
+    permutation when its rows pick distinct columns; softmax invariance to
+    a per-row shift of the comb logits."""
+    hc, eps = 4, 1e-6
+    n = 6
+    z0 = np.zeros((n, hc * (2 + hc)))
+    pre, post, comb = O.mhc(z0, np.ones(3), np.zeros(hc * (2 + hc)), hc, 20, eps)
+    np.testing.assert_allclose(pre, 0.5 + eps)
+    np.testing.assert_allclose(post, 1.0)
+    np.testing.assert_allclose(comb, np.full((n, hc, hc), 1.0 / hc), rtol=1e-5)
+    r = np.random.default_rng(5)
+    mixes = r.standard_normal((n, hc * (2 + hc)))
+    base = r.standard_normal(hc * (2 + hc)) * 0.1
+    _, _, c = O.mhc(mixes, np.array([1.0, 1.0, 1.0]), base, hc, 50, eps)
+    np.testing.assert_allclose(c.sum(axis=-1), 1.0, atol=1e-4)
+    np.testing.assert_allclose(c.sum(axis=-2), 1.0, atol=1e-4)
+    perm = np.array([2, 0, 3, 1])
+    logits = np.zeros((1, hc * (2 + hc)))
+    logits[0, 2 * hc:] = (np.eye(hc)[perm] * 40.0).reshape(-1)
+    _, _, cp = O.mhc(logits, np.ones(3), np.zeros(hc * (2 + hc)), hc, 5, 0.0)
+    np.testing.assert_allclose(cp[0], np.eye(hc)[perm], atol=1e-9)
+    shifted = mixes.copy()
+    shifted[:, 2 * hc:] += np.repeat(r.standard_normal((n, hc)), hc, axis=1)  # + a constant per comb row
+    _, _, c1 = O.mhc(mixes, np.ones(3), base, hc, 3, eps)
+    _, _, c2 = O.mhc(shifted, np.ones(3), base, hc, 3, eps)
+    np.testing.assert_allclose(c1, c2, rtol=1e-12)
+
