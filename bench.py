@@ -598,6 +598,56 @@ def run_int8_gemm(args):
     return res
 
 
+def run_mhc(args):
+    """The mHC mappings for 2^20 tokens with 4 streams (96 bytes in and 96
+    out per token, 201 MB: larger than L2), timed launch by launch."""
+    from sparse_attention_prolog_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n, hc, iters = 1 << 20, 4, 20
+    w = hc * (2 + hc)
+    gen = torch.Generator(device=dev).manual_seed(5)
+    mixes = torch.randn((n, w), device=dev, generator=gen)
+    scale = torch.tensor([0.8, 1.3, 1.7], device=dev)
+    base = torch.randn((w,), device=dev, generator=gen) * 0.5
+    pre, post = torch.empty((n, hc), device=dev), torch.empty((n, hc), device=dev)
+    comb = torch.empty((n, hc, hc), device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            B.dsa_mhc(mixes, scale, base, hc, iters, 1e-6, pre, post, comb, stream)
+    stream.synchronize()
+    K_steps = min(args.steps, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    with ClockSampler(device_uuid(dev)) as clk:
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                e0.record(stream)
+                B.dsa_mhc(mixes, scale, base, hc, iters, 1e-6, pre, post, comb, stream)
+                e1.record(stream)
+        stream.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    nbytes = n * w * 4 * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    res = {"metric": "mhc GB/s (n=2^20 tokens, hc=4, 20 Sinkhorn rounds)", "value": round(gbs, 1), "unit": "GB/s",
+           "n_gpus": 1, "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+           "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded)",
+           "config": {"workload": "mhc n=1048576 hc=4 iters=20", "l2": "inputs larger than L2 (201 MB per launch)"},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+           "gpu_launches": K_steps, "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        mx = mixes[:65536].cpu().numpy()
+        t0 = time.perf_counter()
+        O.mhc(mx, scale.cpu().numpy(), base.cpu().numpy(), hc, iters, 1e-6)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(65536 * w * 8 / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
+                               "kind": "oracle", "sample": "65536 tokens of the same input, numpy float64"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -610,13 +660,15 @@ def main():
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
-    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm"], default="step",
-                    help="the decode step (default), or a standalone export: the activation quantiser, the int8 GEMM")
+    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm", "mhc"], default="step",
+                    help="the decode step (default), or a standalone export: the activation quantiser, the int8 "
+                         "GEMM, the mHC mappings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.op in ("act_quant", "int8_gemm"):
-        print(json.dumps(run_act_quant(args) if args.op == "act_quant" else run_int8_gemm(args)), flush=True)
+    if args.op != "step":
+        run = {"act_quant": run_act_quant, "int8_gemm": run_int8_gemm, "mhc": run_mhc}[args.op]
+        print(json.dumps(run(args)), flush=True)
         return
     rank, world, local = D.init()
     if args.impl == "reference":

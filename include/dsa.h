@@ -7,6 +7,7 @@
  *   dsa_sparse_attn     : Sparse (MLA) flash attention over the top-k rows
  *   dsa_act_quant       : standalone activation quantisation (int8, per row)
  *   dsa_int8_gemm       : standalone int8 GEMM + dequant to fp16 (M <= 32)
+ *   dsa_mhc             : manifold-constrained hyper-connection mappings
  *
  * Page citations:
  *   [V3.2-PyPTO]  "NPU DeepSeek-V3.2-Exp PyPTO 融合算子开发优化实践",
@@ -318,6 +319,37 @@ typedef struct {
 } dsa_int8_gemm_args;
 
 int dsa_int8_gemm(const dsa_int8_gemm_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Manifold-Constrained Hyper-Connections  [V4-TileLang §Manifold-
+ * Constrained Hyper-Connections, steps 1-5] - per token, hc streams:
+ *
+ *   z    = mixes * hc_scale[part] + hc_base      (parts: pre, post, comb)
+ *   pre  = sigmoid(z_pre) + eps                  [n, hc]
+ *   post = 2 sigmoid(z_post)                     [n, hc]
+ *   comb = softmax_rows(z_comb) + eps, then / (column sums + eps), then
+ *          `iters` times / (row sums + eps) and / (column sums + eps)
+ *                                                [n, hc, hc]
+ *
+ * A row of mixes (fp32 [n, hc (2 + hc)]) holds z_pre (hc), z_post (hc) and
+ * z_comb (hc x hc, row-major); hc_scale fp32 [3]; hc_base fp32
+ * [hc (2 + hc)].  All fp32; mixes, pre, post and comb 16-byte aligned,
+ * hc_scale and hc_base 4-byte aligned (else DSA_ERR_INVALID_ARG).
+ * Supported: hc in {4, 8}, 0 <= iters <= 100.  n = 0 is a no-op.  No
+ * workspace.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t n, hc, iters;
+  float eps;
+  const float* mixes;
+  const float* hc_scale;
+  const float* hc_base;
+  float* pre;
+  float* post;
+  float* comb;
+} dsa_mhc_args;
+
+int dsa_mhc(const dsa_mhc_args* args, void* stream);
 
 #ifdef __cplusplus
 }

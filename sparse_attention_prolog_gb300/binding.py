@@ -59,13 +59,18 @@ class Int8GemmArgs(ctypes.Structure):
                 ("b_scale", c_ptr), ("c", c_ptr)]
 
 
+class MhcArgs(ctypes.Structure):
+    _fields_ = [("n", c_int), ("hc", c_int), ("iters", c_int), ("eps", ctypes.c_float), ("mixes", c_ptr),
+                ("hc_scale", c_ptr), ("hc_base", c_ptr), ("pre", c_ptr), ("post", c_ptr), ("comb", c_ptr)]
+
+
 EXPORTS = [
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error",
     "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
     "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
     "dsa_indexer_scores", "dsa_topk_from_scores",
     "dsa_sparse_attn_workspace", "dsa_sparse_attn", "dsa_indexer_prolog_noalloc", "dsa_act_quant",
-    "dsa_int8_gemm",
+    "dsa_int8_gemm", "dsa_mhc",
 ]
 
 _lib = None
@@ -108,6 +113,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_act_quant.restype = c_int
     lib.dsa_int8_gemm.argtypes = [ctypes.POINTER(Int8GemmArgs), c_ptr]
     lib.dsa_int8_gemm.restype = c_int
+    lib.dsa_mhc.argtypes = [ctypes.POINTER(MhcArgs), c_ptr]
+    lib.dsa_mhc.restype = c_int
     _lib = lib
     return lib
 
@@ -236,4 +243,12 @@ def dsa_int8_gemm(a: torch.Tensor, a_scale: torch.Tensor, b: torch.Tensor, b_sca
     N = b.shape[0]
     args = Int8GemmArgs(M, N, K, _p(a), _p(a_scale), _p(b), _p(b_scale), _p(c))
     _check(load().dsa_int8_gemm(ctypes.byref(args), _stream(stream)), "dsa_int8_gemm")
+
+
+def dsa_mhc(mixes: torch.Tensor, hc_scale: torch.Tensor, hc_base: torch.Tensor, hc: int, iters: int, eps: float,
+            pre: torch.Tensor, post: torch.Tensor, comb: torch.Tensor, stream=None):
+    """mixes fp32 [n, hc (2 + hc)] -> pre [n, hc], post [n, hc], comb [n, hc, hc] (see dsa.h)."""
+    args = MhcArgs(mixes.shape[0], hc, iters, float(eps), _p(mixes), _p(hc_scale), _p(hc_base), _p(pre), _p(post),
+                   _p(comb))
+    _check(load().dsa_mhc(ctypes.byref(args), _stream(stream)), "dsa_mhc")
 

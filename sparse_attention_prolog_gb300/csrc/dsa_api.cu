@@ -288,4 +288,14 @@ int dsa_int8_gemm(const dsa_int8_gemm_args* a, void* stream) {
   return launch_int8_gemm(*a, static_cast<cudaStream_t>(stream));
 }
 
+int dsa_mhc(const dsa_mhc_args* a, void* stream) {
+  if (!a || a->n < 0 || a->iters < 0 || !(a->eps >= 0.f)) return DSA_ERR_INVALID_ARG;
+  if ((a->hc != 4 && a->hc != 8) || a->iters > 100) return DSA_ERR_UNSUPPORTED;
+  if (a->n == 0) return DSA_OK;
+  if (bad_ptr(a->mixes, 16) || bad_ptr(a->hc_scale, 4) || bad_ptr(a->hc_base, 4) || bad_ptr(a->pre, 16) ||
+      bad_ptr(a->post, 16) || bad_ptr(a->comb, 16))
+    return DSA_ERR_INVALID_ARG;
+  return launch_mhc(*a, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -159,7 +159,115 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------- mHC
+// [V4-TileLang §Manifold-Constrained Hyper-Connections] steps 1-5 for hc
+// streams: per token, mixes [hc (2 + hc)] -> pre [hc], post [hc], comb
+// [hc, hc] (row-major).  One thread per token, everything in registers in
+// fp32: scale + base, the sigmoids, the row softmax + eps, then the column /
+// row / column Sinkhorn-Knopp normalisations.  The 20-round normalisation
+// makes the kernel issue-bound, so the memory side is kept to the fewest
+// instructions: each thread moves its own rows with 16-byte accesses (a row
+// is a whole number of float4) and L1 absorbs the 96- / 320-byte stride
+// between the lanes of a warp.
+constexpr int kMhcTokens = 128;
+
+template <int HC>
+__global__ void __launch_bounds__(kMhcTokens) mhc_kernel(const float* __restrict__ mixes, const float* __restrict__ hc_scale,
+                                                         const float* __restrict__ hc_base, float* __restrict__ pre,
+                                                         float* __restrict__ post, float* __restrict__ comb, int n,
+                                                         int iters, float eps) {
+  constexpr int W = HC * (2 + HC);
+  static_assert(W % 4 == 0 && HC % 4 == 0, "rows must be whole float4");
+  const int t = blockIdx.x * kMhcTokens + threadIdx.x;
+  if (t >= n) return;
+  float z[W];
+  const float4* src = reinterpret_cast<const float4*>(mixes + static_cast<size_t>(t) * W);
+#pragma unroll
+  for (int v = 0; v < W / 4; ++v) {
+    const float4 q = __ldg(src + v);
+    z[4 * v] = q.x;
+    z[4 * v + 1] = q.y;
+    z[4 * v + 2] = q.z;
+    z[4 * v + 3] = q.w;
+  }
+  const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1), s2 = __ldg(hc_scale + 2);
+  float pr[HC], po[HC], c[HC][HC];
+#pragma unroll
+  for (int i = 0; i < HC; ++i) {
+    const float zp = z[i] * s0 + __ldg(hc_base + i);
+    const float zq = z[HC + i] * s1 + __ldg(hc_base + HC + i);
+    pr[i] = 1.f / (1.f + expf(-zp)) + eps;
+    po[i] = 2.f / (1.f + expf(-zq));
+  }
+#pragma unroll
+  for (int i = 0; i < HC; ++i) {
+    float m = -3.402823466e38f;
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+      c[i][j] = z[2 * HC + i * HC + j] * s2 + __ldg(hc_base + 2 * HC + i * HC + j);
+      m = fmaxf(m, c[i][j]);
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+      c[i][j] = expf(c[i][j] - m);
+      sum += c[i][j];
+    }
+    const float inv = 1.f / sum;
+#pragma unroll
+    for (int j = 0; j < HC; ++j) c[i][j] = c[i][j] * inv + eps;
+  }
+  auto col_norm = [&]() {
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < HC; ++i) sum += c[i][j];
+      const float inv = 1.f / (sum + eps);
+#pragma unroll
+      for (int i = 0; i < HC; ++i) c[i][j] *= inv;
+    }
+  };
+  col_norm();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < HC; ++i) {
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < HC; ++j) sum += c[i][j];
+      const float inv = 1.f / (sum + eps);
+#pragma unroll
+      for (int j = 0; j < HC; ++j) c[i][j] *= inv;
+    }
+    col_norm();
+  }
+  float4* dpre = reinterpret_cast<float4*>(pre + static_cast<size_t>(t) * HC);
+  float4* dpost = reinterpret_cast<float4*>(post + static_cast<size_t>(t) * HC);
+  float4* dcomb = reinterpret_cast<float4*>(comb + static_cast<size_t>(t) * HC * HC);
+#pragma unroll
+  for (int v = 0; v < HC / 4; ++v) {
+    dpre[v] = make_float4(pr[4 * v], pr[4 * v + 1], pr[4 * v + 2], pr[4 * v + 3]);
+    dpost[v] = make_float4(po[4 * v], po[4 * v + 1], po[4 * v + 2], po[4 * v + 3]);
+  }
+#pragma unroll
+  for (int i = 0; i < HC; ++i)
+#pragma unroll
+    for (int v = 0; v < HC / 4; ++v)
+      dcomb[i * (HC / 4) + v] = make_float4(c[i][4 * v], c[i][4 * v + 1], c[i][4 * v + 2], c[i][4 * v + 3]);
+}
+
 }  // namespace
+
+int launch_mhc(const dsa_mhc_args& a, cudaStream_t s) {
+  const dim3 grid((a.n + kMhcTokens - 1) / kMhcTokens);
+  if (a.hc == 4)
+    mhc_kernel<4><<<grid, kMhcTokens, 0, s>>>(a.mixes, a.hc_scale, a.hc_base, a.pre, a.post, a.comb, a.n, a.iters,
+                                              a.eps);
+  else
+    mhc_kernel<8><<<grid, kMhcTokens, 0, s>>>(a.mixes, a.hc_scale, a.hc_base, a.pre, a.post, a.comb, a.n, a.iters,
+                                              a.eps);
+  return cuda_status(cudaGetLastError());
+}
 
 int launch_int8_gemm(const dsa_int8_gemm_args& a, cudaStream_t s) {
   uint32_t* err = error_word();

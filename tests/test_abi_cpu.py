@@ -45,7 +45,7 @@ def test_struct_layout_matches_header(lib, tmp_path):
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dsa.h"', "int main(void) {"]
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
                       ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs),
-                      ("dsa_int8_gemm_args", B.Int8GemmArgs)):
+                      ("dsa_int8_gemm_args", B.Int8GemmArgs), ("dsa_mhc_args", B.MhcArgs)):
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
         for f, _ in py._fields_:
             lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
@@ -57,7 +57,7 @@ def test_struct_layout_matches_header(lib, tmp_path):
     got = dict(line.split() for line in out if line)
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
                       ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs),
-                      ("dsa_int8_gemm_args", B.Int8GemmArgs)):
+                      ("dsa_int8_gemm_args", B.Int8GemmArgs), ("dsa_mhc_args", B.MhcArgs)):
         assert int(got[cname]) == ctypes.sizeof(py)
         for f, _ in py._fields_:
             assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, f"{cname}.{f}"
@@ -125,6 +125,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 1                   # b not 16-byte aligned
     g.N = 0
     assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 0                   # empty: no-op
+    h = B.MhcArgs(16, 6, 5, 1e-6, 1 << 20, 1 << 21, 1 << 22, 1 << 23, 1 << 24, 1 << 25)
+    assert lib.dsa_mhc(ctypes.byref(h), null) == 2                         # hc 6
+    h.hc, h.eps = 4, -1.0
+    assert lib.dsa_mhc(ctypes.byref(h), null) == 1                         # negative eps
+    h.eps, h.comb = 1e-6, (1 << 25) + 4
+    assert lib.dsa_mhc(ctypes.byref(h), null) == 1                         # comb not 16-byte aligned
+    h.eps, h.n = 1e-6, 0
+    assert lib.dsa_mhc(ctypes.byref(h), null) == 0                         # empty: no-op
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -1,0 +1,33 @@
+"""Manifold-constrained hyper-connection mappings: CUDA path (fp32) vs the
+float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sparse_attention_prolog_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.mark.parametrize("hc", [4, 8])
+@pytest.mark.parametrize("iters", [0, 3, 20])
+def test_mhc_matches_oracle(hc, iters, cuda_lib):
+    n = 1000  # not a multiple of the 128-thread block
+    r = np.random.default_rng(hc * 10 + iters)
+    w = hc * (2 + hc)
+    mixes = (r.standard_normal((n, w)) * 2.0).astype(np.float32)
+    scale = np.array([0.8, 1.3, 1.7], np.float32)
+    base = (r.standard_normal(w) * 0.5).astype(np.float32)
+    eps = 1e-6
+    d = lambda a: torch.from_numpy(a).to(DEV)
+    pre = torch.empty((n, hc), device=DEV)
+    post = torch.empty((n, hc), device=DEV)
+    comb = torch.empty((n, hc, hc), device=DEV)
+    B.dsa_mhc(d(mixes), d(scale), d(base), hc, iters, eps, pre, post, comb)
+    torch.cuda.synchronize()
+    rp, rq, rc = O.mhc(mixes.astype(np.float64), scale.astype(np.float64), base.astype(np.float64), hc, iters, eps)
+    np.testing.assert_allclose(pre.cpu().numpy(), rp, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(post.cpu().numpy(), rq, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(comb.cpu().numpy(), rc, rtol=1e-4, atol=1e-6)

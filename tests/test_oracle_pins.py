@@ -474,3 +474,40 @@ def test_mhc_pins():
     _, _, c2 = O.mhc(shifted, np.ones(3), base, hc, 3, eps)
     np.testing.assert_allclose(c1, c2, rtol=1e-12)
 
+
+
+def test_mhc_scale_order_and_sinkhorn_limit():
+    """Independent of the step order written in the oracle: (1) the three
+    parts take hc_scale[0], [1], [2] in that order and the gates are the
+    logistic function, checked through its tanh form (1 + tanh(z/2)) / 2;
+    (2) with eps = 0 the last step is a column normalisation, so every column
+    sums to one and the rows in general do not; (3) a positive 2 x 2 matrix
+    has the Sinkhorn limit [[p, 1 - p], [1 - p, p]] with
+    p / (1 - p) = sqrt(c00 c11 / (c01 c10)), the cross ratio that row and
+    column scalings leave unchanged; after a row softmax it equals
+    exp(z00 + z11 - z01 - z10)."""
+    hc = 4
+    w = hc * (2 + hc)
+    x = np.zeros((1, w))
+    x[0, :hc] = [0.5, -1.0, 2.0, 0.0]
+    x[0, hc:2 * hc] = [1.0, -0.25, 0.0, 3.0]
+    scale = np.array([2.0, 3.0, 5.0])
+    base = np.zeros(w)
+    base[:2 * hc] = np.linspace(-0.3, 0.4, 2 * hc)
+    pre, post, _ = O.mhc(x, scale, base, hc, 0, 1e-3)
+    logistic = lambda v: 0.5 * (1.0 + np.tanh(0.5 * v))
+    np.testing.assert_allclose(pre[0], logistic(2.0 * x[0, :hc] + base[:hc]) + 1e-3, rtol=1e-13)
+    np.testing.assert_allclose(post[0], 2.0 * logistic(3.0 * x[0, hc:2 * hc] + base[hc:2 * hc]), rtol=1e-13)
+    r = np.random.default_rng(11)
+    mixes = r.standard_normal((8, w))
+    for iters in (0, 3):
+        _, _, c = O.mhc(mixes, np.ones(3), np.zeros(w), hc, iters, 0.0)
+        np.testing.assert_allclose(c.sum(axis=-2), 1.0, rtol=1e-13)
+        assert np.abs(c.sum(axis=-1) - 1.0).max() > 1e-6
+    z = np.array([[0.7, -0.4], [0.2, 1.1]])
+    m2 = np.zeros((1, 2 * 4))
+    m2[0, 4:] = z.reshape(-1)
+    _, _, c = O.mhc(m2, np.ones(3), np.zeros(8), 2, 200, 0.0)
+    ratio = np.sqrt(np.exp(z[0, 0] + z[1, 1] - z[0, 1] - z[1, 0]))
+    p = ratio / (1.0 + ratio)
+    np.testing.assert_allclose(c[0], [[p, 1.0 - p], [1.0 - p, p]], atol=1e-12)
