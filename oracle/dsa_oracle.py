@@ -29,6 +29,7 @@ __all__ = [
     "int8_gemm_dequant", "int8_gemm", "act_quant", "rope", "layer_norm", "indexer_prolog",
     "indexer_dots", "indexer_scores_token", "topk_indices",
     "sparse_attention_token", "sparse_attention", "logical_rows", "mhc",
+    "rms_norm", "mla_q", "mla_kv", "mla_prolog",
 ]
 
 
@@ -346,3 +347,74 @@ def mhc(mixes: np.ndarray, hc_scale: np.ndarray, hc_base: np.ndarray, hc: int, i
         c = c / (c.sum(axis=-2, keepdims=True) + eps)
     return pre, post, c
 
+
+
+# ----------------------------------------------------------------------------
+# MLA Prolog  [V3.2-PyPTO §Deepseek Indexer Attention: the first of the four
+# parts; it feeds q_lora to the Indexer Prolog (§Indexer Prolog, the Indexer
+# Q formula) and q plus the latent KV rows to Sparse Flash Attention]
+# ----------------------------------------------------------------------------
+MLA_D_C, MLA_D_N, MLA_D_R = 512, 128, 64  # latent, no-position and rotary dims
+
+
+def rms_norm(x: np.ndarray, gamma, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * gamma over the last axis (reading: the
+    RMS normalisation of the MLA latents, eps inside the root)."""
+    x = np.asarray(x, dtype=F64)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * np.asarray(gamma, F64)
+
+
+def mla_q(q_lora, q_lora_scale, w_uq, w_uq_scale, w_uk, H: int, pos, cos_tab, sin_tab,
+          interleaved: bool = False) -> np.ndarray:
+    """Query of the sparse MLA attention from the quantised query latent.
+
+    u = DeQuant(q_lora . w_uq) [T, H, d_n + d_r] (the Indexer Q formula's
+    int8 GEMM and dequant, the same q_lora feeding both); per head the
+    first d_n = 128 dims are multiplied into the latent space by w_uk[h]
+    [d_n, d_c] (q_abs = u_nope . w_uk[h], so that q_abs . c = u_nope .
+    (w_uk[h] c) for a latent row c), the last d_r = 64 dims are rotated.
+    Returns float64 [T, H, d_c + d_r] = [q_abs | RoPE(u_rope)]."""
+    T = np.asarray(q_lora).shape[0]
+    u = int8_gemm_dequant(q_lora, q_lora_scale, w_uq, w_uq_scale).reshape(T, H, MLA_D_N + MLA_D_R)
+    q_abs = np.einsum("thn,hnc->thc", u[..., :MLA_D_N], np.asarray(w_uk, dtype=F64))
+    q_pe = rope(u[..., MLA_D_N:], pos, cos_tab, sin_tab, MLA_D_R, interleaved)
+    return np.concatenate([q_abs, q_pe], axis=-1)
+
+
+def mla_kv(x, w_dkv, gamma_kv, eps: float, pos, cos_tab, sin_tab, interleaved: bool = False) -> np.ndarray:
+    """Latent KV row of each token: c = x . w_dkv^T [T, d_c + d_r]; the first
+    d_c = 512 dims RMS-normalised (gamma_kv), the last d_r = 64 rotated.
+    Returns float64 [T, d_c + d_r]."""
+    c = np.asarray(x, dtype=F64) @ np.asarray(w_dkv, dtype=F64).T
+    lat = rms_norm(c[:, :MLA_D_C], gamma_kv, eps)
+    pe = rope(c[:, None, MLA_D_C:], pos, cos_tab, sin_tab, MLA_D_R, interleaved)[:, 0, :]
+    return np.concatenate([lat, pe], axis=-1)
+
+
+def mla_prolog(p, kv_cache=None):
+    """The MLA Prolog of one step of query tokens.
+
+    The pages give it no formula.  Reading (the plainest one that its
+    neighbours support): the query latent is c_q = RMSNorm(x . w_dq^T) *
+    gamma_q [T, K_q]; its per-token DynamicQuant (the Indexer Prolog's
+    quantiser, one fp16 scale per token) is the int8 q_lora with fp16 scale
+    that the Indexer Q formula consumes; the same q_lora gives the
+    attention query through `mla_q` (w_uq int8 with per-channel fp16
+    scales, w_uk bf16 absorbed, 576 = 512 + 64 dims as the attention's
+    latent rows); the latent KV row comes from `mla_kv` and goes to
+    kv_cache[slot[t]] (slot -1: not written).  x, w_dq, w_dkv and w_uk are
+    raw bf16 bits.  Returns a dict: c_q float64 [T, K_q], q_lora int8
+    [T, K_q], q_lora_scale fp16 [T], q float64 [T, H, 576], kv float64
+    [T, 576]."""
+    x = bf16_bits_to_f64(p.x)
+    c_q = rms_norm(x @ bf16_bits_to_f64(p.w_dq).T, p.gamma_q, p.rms_eps)
+    q_lora, q_lora_scale = dynamic_quant(c_q)
+    inter = bool(p.rope_interleaved)
+    q = mla_q(q_lora, q_lora_scale, p.w_uq, p.w_uq_scale, bf16_bits_to_f64(p.w_uk), p.H, p.pos,
+              p.rope_cos, p.rope_sin, inter)
+    kv = mla_kv(x, bf16_bits_to_f64(p.w_dkv), p.gamma_kv, p.rms_eps, p.pos, p.rope_cos, p.rope_sin, inter)
+    if kv_cache is not None:
+        for t in range(p.T):
+            if p.slot[t] >= 0:
+                kv_cache[p.slot[t]] = kv[t]
+    return {"c_q": c_q, "q_lora": q_lora, "q_lora_scale": q_lora_scale, "q": q, "kv": kv}

@@ -122,6 +122,58 @@ def make_prolog_inputs(T, pos, slot, seed, H_I=64, d_I=128, K_q=1536, D_x=7168,
 
 
 # ----------------------------------------------------------------------------
+# MLA Prolog inputs
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class MlaInputs:
+    T: int
+    H: int
+    K_q: int
+    D_x: int
+    x: np.ndarray             # bf16 bits [T, D_x]
+    w_dq: np.ndarray          # bf16 bits [K_q, D_x] (row n = output channel n)
+    gamma_q: np.ndarray       # fp32 [K_q]
+    w_dkv: np.ndarray         # bf16 bits [576, D_x]: 512 latent rows, then 64 rotary rows
+    gamma_kv: np.ndarray      # fp32 [512]
+    rms_eps: float
+    w_uq: np.ndarray          # int8 [H*192, K_q]: per head 128 no-position rows, then 64 rotary rows
+    w_uq_scale: np.ndarray    # fp16 [H*192]
+    w_uk: np.ndarray          # bf16 bits [H, 128, 512]
+    pos: np.ndarray           # int32 [T]
+    rope_cos: np.ndarray      # fp32 [max_pos, 32]
+    rope_sin: np.ndarray
+    rope_interleaved: int
+    slot: np.ndarray          # int64 [T] latent-cache row, -1 = do not write
+
+
+def make_mla_inputs(T, pos, slot, seed, H=128, K_q=1536, D_x=7168, max_pos=None,
+                    rope_interleaved=0) -> MlaInputs:
+    """Projections scaled so that every intermediate is about N(0, 1):
+    w_dq, w_dkv ~ N(0, 1/D_x); w_uq codes like a quantised normal with
+    scales (4/127) K_q^-1/2 U(0.9, 1.1); w_uk ~ N(0, 1/128); gammas
+    1 + 0.1 N(0, 1)."""
+    rng = _rng(seed)
+    pos = np.asarray(pos, dtype=np.int32)
+    if max_pos is None:
+        max_pos = int(pos.max()) + 1
+    cos, sin = rope_tables(max_pos, 64)
+    return MlaInputs(
+        T=T, H=H, K_q=K_q, D_x=D_x,
+        x=bf16_normal(rng, (T, D_x)),
+        w_dq=bf16_normal(rng, (K_q, D_x), sigma=1.0 / math.sqrt(D_x)),
+        gamma_q=(1.0 + 0.1 * rng.standard_normal(K_q)).astype(np.float32),
+        w_dkv=bf16_normal(rng, (576, D_x), sigma=1.0 / math.sqrt(D_x)),
+        gamma_kv=(1.0 + 0.1 * rng.standard_normal(512)).astype(np.float32),
+        rms_eps=1e-6,
+        w_uq=int8_codes(rng, (H * 192, K_q)),
+        w_uq_scale=fp16_scales(rng, (H * 192,), 1.0 / math.sqrt(K_q)),
+        w_uk=bf16_normal(rng, (H, 128, 512), sigma=1.0 / math.sqrt(128)),
+        pos=pos, rope_cos=cos, rope_sin=sin, rope_interleaved=rope_interleaved,
+        slot=np.asarray(slot, dtype=np.int64),
+    )
+
+
+# ----------------------------------------------------------------------------
 # Indexer (+ top-k) and sparse attention inputs
 # ----------------------------------------------------------------------------
 @dataclasses.dataclass

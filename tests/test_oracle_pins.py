@@ -10,6 +10,7 @@ import scipy.special
 import torch
 
 import oracle as O
+from sparse_attention_prolog_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 rng = np.random.default_rng(12345)
@@ -511,3 +512,100 @@ def test_mhc_scale_order_and_sinkhorn_limit():
     ratio = np.sqrt(np.exp(z[0, 0] + z[1, 1] - z[0, 1] - z[1, 0]))
     p = ratio / (1.0 + ratio)
     np.testing.assert_allclose(c[0], [[p, 1.0 - p], [1.0 - p, p]], atol=1e-12)
+
+
+# ------------------------------------------------------------- MLA Prolog
+def test_rms_norm_pins():
+    """[3, 4] has mean square 12.5; a constant row c maps to
+    gamma c / sqrt(c^2 + eps); scale and sign equivariance at eps = 0; and
+    torch's own rms_norm on random rows."""
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), [1.0, 1.0], 0.0),
+                               np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    g = np.array([0.5, 2.0, -1.0])
+    np.testing.assert_allclose(O.rms_norm(np.full(3, 0.1), g, 1e-2), g * 0.1 / math.sqrt(0.01 + 1e-2), rtol=1e-14)
+    r = np.random.default_rng(21)
+    x = r.standard_normal((5, 64))
+    gam = 1.0 + 0.1 * r.standard_normal(64)
+    np.testing.assert_allclose(O.rms_norm(-3.5 * x, gam, 0.0), -O.rms_norm(x, gam, 0.0), rtol=1e-12)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,), torch.from_numpy(gam), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(x, gam, 1e-6), ref, rtol=1e-12)
+
+
+def _mla_small(T=3, H=2, K_q=128, D_x=128, pos=None, seed=31, interleaved=0):
+    pos = np.arange(T, dtype=np.int32) + 5 if pos is None else np.asarray(pos, dtype=np.int32)
+    return W.make_mla_inputs(T, pos, np.arange(T), seed, H=H, K_q=K_q, D_x=D_x, max_pos=64,
+                             rope_interleaved=interleaved)
+
+
+def test_mla_absorption_identity():
+    """The absorbed query scores a latent row c exactly as the head's
+    no-position query scores the up-projected key w_uk[h] c (both sides built
+    here from int8_gemm_dequant, which has its own pins)."""
+    p = _mla_small()
+    r = np.random.default_rng(3)
+    codes = W.int8_codes(r, (p.T, p.K_q))
+    sa = np.array([0.02, 0.03, 0.05])
+    wuk = O.bf16_bits_to_f64(p.w_uk)
+    q = O.mla_q(codes, sa, p.w_uq, p.w_uq_scale, wuk, p.H, p.pos, p.rope_cos, p.rope_sin)
+    u = O.int8_gemm_dequant(codes, sa, p.w_uq, p.w_uq_scale).reshape(p.T, p.H, 192)
+    c = r.standard_normal(512)
+    for h in range(p.H):
+        np.testing.assert_allclose(q[:, h, :512] @ c, u[:, h, :128] @ (wuk[h] @ c), rtol=1e-10)
+
+
+def test_mla_rope_relative_position():
+    """Rotary property: the q . k score of the rotary dims depends on the two
+    positions only through their difference (here both move by 11)."""
+    for inter in (0, 1):
+        a = _mla_small(pos=[3, 9, 20], interleaved=inter)
+        b = _mla_small(pos=[14, 20, 31], interleaved=inter)
+        ra, rb = O.mla_prolog(a), O.mla_prolog(b)
+        sa = np.einsum("thd,td->th", ra["q"][..., 512:], ra["kv"][:, 512:])
+        sb = np.einsum("thd,td->th", rb["q"][..., 512:], rb["kv"][:, 512:])
+        np.testing.assert_allclose(sa, sb, rtol=1e-5, atol=1e-6)
+        assert not np.allclose(ra["q"][..., 512:], rb["q"][..., 512:])
+
+
+def test_mla_one_hot_layout():
+    """One-hot inputs at position 0 (identity rotation) reduce every
+    projection to indexing: the kv row is [RMSNorm(a w_dkv[:512, j]) |
+    a w_dkv[512:, j]], token rows scaled by different a > 0 give the same
+    normalised query latent (per-token normalisation), a one-hot q_lora
+    selects column k of w_uq, whose rows per head are 128 no-position
+    dims then 64 rotary dims."""
+    T, j = 2, 7
+    p = _mla_small(T=T, pos=[0, 0])
+    x = np.zeros((T, p.D_x), np.float32)
+    x[0, j], x[1, j] = 2.0, 0.5
+    p.x = W.f32_to_bf16_bits(x)
+    p.gamma_q[:] = 1.0
+    p.gamma_kv[:] = 1.0
+    p.rms_eps = 0.0  # exact scale invariance
+    r = O.mla_prolog(p)
+    np.testing.assert_allclose(r["c_q"][0], r["c_q"][1], rtol=1e-9)
+    col = O.bf16_bits_to_f64(p.w_dkv)[:, j]
+    for t, a in ((0, 2.0), (1, 0.5)):
+        lat = a * col[:512]
+        np.testing.assert_allclose(r["kv"][t, :512], lat / np.sqrt((lat ** 2).mean() + p.rms_eps), rtol=1e-12)
+        np.testing.assert_allclose(r["kv"][t, 512:], a * col[512:], rtol=1e-12)
+    k = 5
+    codes = np.zeros((1, p.K_q), np.int8)
+    codes[0, k] = 1
+    q = O.mla_q(codes, np.ones(1), p.w_uq, np.ones(p.H * 192), O.bf16_bits_to_f64(p.w_uk), p.H,
+                np.zeros(1, np.int32), p.rope_cos, p.rope_sin)
+    wuk = O.bf16_bits_to_f64(p.w_uk)
+    for h in range(p.H):
+        rows = p.w_uq[h * 192:(h + 1) * 192, k].astype(np.float64)
+        np.testing.assert_allclose(q[0, h, 512:], rows[128:], rtol=1e-15)
+        np.testing.assert_allclose(q[0, h, :512], rows[:128] @ wuk[h], rtol=1e-12)
+
+
+def test_mla_cache_slots():
+    """Rows go to kv_cache[slot[t]]; slot -1 writes nothing."""
+    p = _mla_small()
+    p.slot = np.array([4, -1, 1], dtype=np.int64)
+    cache = np.full((6, 576), 7.0)
+    r = O.mla_prolog(p, cache)
+    np.testing.assert_array_equal(cache[4], r["kv"][0])
+    np.testing.assert_array_equal(cache[1], r["kv"][2])
+    assert np.all(cache[[0, 2, 3, 5]] == 7.0)
