@@ -648,6 +648,64 @@ def run_mhc(args):
     return res
 
 
+def run_mla(args):
+    """The MLA Prolog of one decode step (B=4 x MTP1 = 8 tokens, 128 heads,
+    K_q = 1536, D_x = 7168): 85 MB of weights per call, so three weight sets
+    (255 MB, larger than L2) are rotated call by call."""
+    from sparse_attention_prolog_gb300 import binding as B
+    from sparse_attention_prolog_gb300 import workloads as W
+    from sparse_attention_prolog_gb300.pipeline import MlaBuffers
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, H, K_q, D_x = 8, 128, 1536, 7168
+    pos = np.array([65534, 65535] * 4, dtype=np.int32)
+    slot = np.arange(T, dtype=np.int64) + 65528
+    p = W.make_mla_inputs(T, pos, slot, seed=9001, H=H, K_q=K_q, D_x=D_x, max_pos=65536)
+    bufs = [MlaBuffers(p, dev, 65536) for _ in range(3)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            bufs[i % 3].run(stream)
+    stream.synchronize()
+    assert B.device_error(stream) == 0
+    K_steps = min(args.steps, 300)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    with ClockSampler(device_uuid(dev)) as clk:
+        with torch.cuda.stream(stream):
+            for i, (e0, e1) in enumerate(evs):
+                e0.record(stream)
+                bufs[i % 3].run(stream)
+                e1.record(stream)
+        stream.synchronize()
+    assert B.device_error(stream) == 0
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    weights = K_q * D_x * 2 + 576 * D_x * 2 + H * 192 * K_q + H * 192 * 2 + H * 128 * 512 * 2 + (K_q + 512) * 4
+    io = T * D_x * 2 + T * K_q + T * 2 + T * H * 576 * 2 + T * 576 * 2
+    nbytes = weights + io
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    res = {"metric": "mla_prolog GB/s (T=8 tokens, H=128, K_q=1536, D_x=7168)", "value": round(gbs, 1),
+           "unit": "GB/s", "n_gpus": 1, "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+           "higher_is_better": True, "dtype": "bf16/int8", "data": "synthetic (seeded)",
+           "config": {"workload": "mla_prolog decode T=8 H=128 K_q=1536 D_x=7168",
+                      "l2": f"3 weight sets rotated ({3 * weights / 1e6:.0f} MB, larger than L2)",
+                      "bytes_per_call": nbytes},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+           "gpu_launches": 3 * K_steps, "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        reps = 3
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            O.mla_prolog(p)
+        dt = (time.perf_counter() - t0) / reps
+        res["cpu_baseline"] = {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": f"the same call, {reps} times, numpy float64 (BLAS threads "
+                                                           "up to the core count)"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,14 +718,15 @@ def main():
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
-    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm", "mhc"], default="step",
+    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm", "mhc", "mla_prolog"], default="step",
                     help="the decode step (default), or a standalone export: the activation quantiser, the int8 "
-                         "GEMM, the mHC mappings")
+                         "GEMM, the mHC mappings, the MLA Prolog")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op != "step":
-        run = {"act_quant": run_act_quant, "int8_gemm": run_int8_gemm, "mhc": run_mhc}[args.op]
+        run = {"act_quant": run_act_quant, "int8_gemm": run_int8_gemm, "mhc": run_mhc,
+               "mla_prolog": run_mla}[args.op]
         print(json.dumps(run(args)), flush=True)
         return
     rank, world, local = D.init()

@@ -8,6 +8,7 @@
  *   dsa_act_quant       : standalone activation quantisation (int8, per row)
  *   dsa_int8_gemm       : standalone int8 GEMM + dequant to fp16 (M <= 32)
  *   dsa_mhc             : manifold-constrained hyper-connection mappings
+ *   dsa_mla_prolog      : MLA Prolog (q_lora, absorbed query, latent KV rows)
  *
  * Page citations:
  *   [V3.2-PyPTO]  "NPU DeepSeek-V3.2-Exp PyPTO 融合算子开发优化实践",
@@ -350,6 +351,72 @@ typedef struct {
 } dsa_mhc_args;
 
 int dsa_mhc(const dsa_mhc_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
+ * MLA Prolog  [V3.2-PyPTO §Deepseek Indexer Attention: the first of its four
+ * parts, feeding q_lora to the Indexer Prolog and q plus the latent KV rows
+ * to the sparse attention; the pages give it no formula, so the operation
+ * below is a reading of it]
+ *
+ *   c_q          = RMSNorm(x . w_dq^T) * gamma_q                 [T, K_q]
+ *   q_lora, q_lora_scale = DynamicQuant(c_q)  (per token, as the Indexer
+ *                  Prolog's quantiser: scale = fp16(absmax / 127), codes
+ *                  round_half_even(clamp(c / scale, -127, 127)))
+ *   u            = DeQuant(q_lora . w_uq^T)                    [T, H, 192]
+ *                  (exact int32 sums times q_lora_scale[t] * w_uq_scale[n]
+ *                  in fp32; per head 128 no-position dims, then 64 rotary)
+ *   q[t, h]      = bf16([u[t,h,:128] . w_uk[h] | RoPE(u[t,h,128:])])
+ *                                                              [T, H, 576]
+ *   c            = x . w_dkv^T                                  [T, 576]
+ *   kv_cache[slot[t]] = bf16([RMSNorm(c[:512]) * gamma_kv | RoPE(c[512:])])
+ *
+ * RMSNorm: x / sqrt(mean(x^2) + rms_eps).  RoPE rotates the 64 rotary dims
+ * with the fp32 tables rope_cos / rope_sin [rope_max_pos, 32] at row pos[t];
+ * pairs (i, i + 32), or (2i, 2i+1) if rope_interleaved.
+ *
+ * Shapes: x bf16 [T, D_x]; w_dq bf16 [K_q, D_x] (row n = output channel n);
+ * gamma_q fp32 [K_q]; w_dkv bf16 [576, D_x] (512 latent rows, then 64
+ * rotary rows); gamma_kv fp32 [512]; w_uq int8 [H*192, K_q]; w_uq_scale fp16
+ * [H*192]; w_uk bf16 [H, 128, 512]; pos int32 [T]; q_lora int8 [T, K_q];
+ * q_lora_scale fp16 [T]; q bf16 [T, H, 576]; kv_cache bf16
+ * [cache_rows, 576]; slot int64 [T] (-1 = not written; slots must not
+ * repeat).  A slot >= cache_rows or a pos outside [0, rope_max_pos) is
+ * recorded in the device error word and that token's latent row is not
+ * written.
+ * Supported: 1 <= T <= 32, 1 <= H <= 128, K_q a multiple of 128 in
+ * [128, 2048], D_x a multiple of 64 in [64, 16384], rms_eps >= 0.
+ * x, w_dq, gamma_q, w_dkv, gamma_kv, w_uq, w_uk, q_lora, q and kv_cache
+ * 16-byte aligned.
+ * Workspace: dsa_mla_prolog_workspace() bytes, 256-byte aligned; it must
+ * be zero-filled once before its first use (each call leaves its sums
+ * zeroed; after a call that ended in DSA_ERR_DEVICE_TIMEOUT, zero it again).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, H, K_q, D_x;
+  float rms_eps;
+  int32_t rope_max_pos;
+  int32_t rope_interleaved;
+  const uint16_t* x;
+  const uint16_t* w_dq;
+  const float* gamma_q;
+  const uint16_t* w_dkv;
+  const float* gamma_kv;
+  const int8_t* w_uq;
+  const uint16_t* w_uq_scale;
+  const uint16_t* w_uk;
+  const int32_t* pos;
+  const float* rope_cos;
+  const float* rope_sin;
+  int8_t* q_lora;
+  uint16_t* q_lora_scale;
+  uint16_t* q;
+  uint16_t* kv_cache;
+  const int64_t* slot;
+  int64_t cache_rows;
+} dsa_mla_prolog_args;
+
+size_t dsa_mla_prolog_workspace(const dsa_mla_prolog_args* args);
+int dsa_mla_prolog(const dsa_mla_prolog_args* args, void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

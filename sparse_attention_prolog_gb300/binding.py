@@ -64,13 +64,22 @@ class MhcArgs(ctypes.Structure):
                 ("hc_scale", c_ptr), ("hc_base", c_ptr), ("pre", c_ptr), ("post", c_ptr), ("comb", c_ptr)]
 
 
+class MlaArgs(ctypes.Structure):
+    _fields_ = [("T", c_int), ("H", c_int), ("K_q", c_int), ("D_x", c_int), ("rms_eps", ctypes.c_float),
+                ("rope_max_pos", c_int), ("rope_interleaved", c_int), ("x", c_ptr), ("w_dq", c_ptr),
+                ("gamma_q", c_ptr), ("w_dkv", c_ptr), ("gamma_kv", c_ptr), ("w_uq", c_ptr), ("w_uq_scale", c_ptr),
+                ("w_uk", c_ptr), ("pos", c_ptr), ("rope_cos", c_ptr), ("rope_sin", c_ptr), ("q_lora", c_ptr),
+                ("q_lora_scale", c_ptr), ("q", c_ptr), ("kv_cache", c_ptr), ("slot", c_ptr),
+                ("cache_rows", ctypes.c_int64)]
+
+
 EXPORTS = [
     "dsa_status_string", "dsa_abi_version", "dsa_get_device_error",
     "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
     "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
     "dsa_indexer_scores", "dsa_topk_from_scores",
     "dsa_sparse_attn_workspace", "dsa_sparse_attn", "dsa_indexer_prolog_noalloc", "dsa_act_quant",
-    "dsa_int8_gemm", "dsa_mhc",
+    "dsa_int8_gemm", "dsa_mhc", "dsa_mla_prolog_workspace", "dsa_mla_prolog",
 ]
 
 _lib = None
@@ -115,6 +124,10 @@ def load(path: str = LIB_PATH):
     lib.dsa_int8_gemm.restype = c_int
     lib.dsa_mhc.argtypes = [ctypes.POINTER(MhcArgs), c_ptr]
     lib.dsa_mhc.restype = c_int
+    lib.dsa_mla_prolog_workspace.argtypes = [ctypes.POINTER(MlaArgs)]
+    lib.dsa_mla_prolog_workspace.restype = ctypes.c_size_t
+    lib.dsa_mla_prolog.argtypes = [ctypes.POINTER(MlaArgs), c_ptr, ctypes.c_size_t, c_ptr]
+    lib.dsa_mla_prolog.restype = c_int
     _lib = lib
     return lib
 
@@ -221,7 +234,7 @@ def dsa_sparse_attn(args: AttnArgs, workspace: Optional[torch.Tensor] = None, st
 def workspace_bytes(kind: str, args) -> int:
     lib = load()
     fn = {"prolog": lib.dsa_indexer_prolog_workspace, "topk": lib.dsa_indexer_topk_workspace,
-          "attn": lib.dsa_sparse_attn_workspace}[kind]
+          "attn": lib.dsa_sparse_attn_workspace, "mla": lib.dsa_mla_prolog_workspace}[kind]
     return int(fn(ctypes.byref(args)))
 
 
@@ -252,3 +265,25 @@ def dsa_mhc(mixes: torch.Tensor, hc_scale: torch.Tensor, hc_base: torch.Tensor, 
                    _p(comb))
     _check(load().dsa_mhc(ctypes.byref(args), _stream(stream)), "dsa_mhc")
 
+
+# ------------------------------------------------------------ MLA Prolog
+def mla_args(x, w_dq, gamma_q, w_dkv, gamma_kv, rms_eps, w_uq, w_uq_scale, w_uk, pos, rope_cos, rope_sin,
+             rope_interleaved, q_lora, q_lora_scale, q, kv_cache, slot) -> MlaArgs:
+    """x bf16 [T, D_x], w_dq bf16 [K_q, D_x], w_dkv bf16 [576, D_x], w_uq int8 [H*192, K_q], w_uk bf16
+    [H, 128, 512]; outputs q_lora int8 [T, K_q], q_lora_scale fp16 [T], q bf16 [T, H, 576] and the
+    kv_cache bf16 [rows, 576] rows at slot (see dsa.h)."""
+    T, D_x = x.shape
+    return MlaArgs(T, w_uk.shape[0], w_dq.shape[0], D_x, float(rms_eps), rope_cos.shape[0], int(rope_interleaved),
+                   _p(x), _p(w_dq), _p(gamma_q), _p(w_dkv), _p(gamma_kv), _p(w_uq), _p(w_uq_scale), _p(w_uk),
+                   _p(pos), _p(rope_cos), _p(rope_sin), _p(q_lora), _p(q_lora_scale), _p(q), _p(kv_cache),
+                   _p(slot), kv_cache.shape[0])
+
+
+def dsa_mla_prolog(args: MlaArgs, workspace: Optional[torch.Tensor] = None, stream=None, device=None):
+    """Runs the MLA Prolog; a new workspace is zero-filled, a given one must
+    have been zero-filled before its first use.  Returns the workspace."""
+    lib = load()
+    need = lib.dsa_mla_prolog_workspace(ctypes.byref(args))
+    ws, n = _ws(need, device or "cuda", workspace)
+    _check(lib.dsa_mla_prolog(ctypes.byref(args), _p(ws), n, _stream(stream)), "dsa_mla_prolog")
+    return ws

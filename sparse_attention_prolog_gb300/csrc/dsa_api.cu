@@ -187,7 +187,7 @@ const char* dsa_status_string(int status) {
   }
 }
 
-int dsa_abi_version(void) { return 101; }
+int dsa_abi_version(void) { return 102; }
 
 int dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
@@ -296,6 +296,34 @@ int dsa_mhc(const dsa_mhc_args* a, void* stream) {
       bad_ptr(a->post, 16) || bad_ptr(a->comb, 16))
     return DSA_ERR_INVALID_ARG;
   return launch_mhc(*a, static_cast<cudaStream_t>(stream));
+}
+
+static int check_mla(const dsa_mla_prolog_args* a) {
+  if (!a || a->T < 0 || a->H < 1 || !(a->rms_eps >= 0.f) || a->cache_rows < 0 || a->rope_max_pos < 1 ||
+      (a->rope_interleaved != 0 && a->rope_interleaved != 1))
+    return DSA_ERR_INVALID_ARG;
+  if (a->T > 32 || a->H > 128 || a->K_q < 128 || a->K_q > 2048 || a->K_q % 128 != 0 || a->D_x < 64 ||
+      a->D_x > 16384 || a->D_x % 64 != 0)
+    return DSA_ERR_UNSUPPORTED;
+  if (a->T == 0) return DSA_OK;
+  if (bad_ptr(a->x, 16) || bad_ptr(a->w_dq, 16) || bad_ptr(a->gamma_q, 16) || bad_ptr(a->w_dkv, 16) ||
+      bad_ptr(a->gamma_kv, 16) || bad_ptr(a->w_uq, 16) || bad_ptr(a->w_uq_scale, 2) || bad_ptr(a->w_uk, 16) ||
+      bad_ptr(a->pos, 4) || bad_ptr(a->rope_cos, 4) || bad_ptr(a->rope_sin, 4) || bad_ptr(a->q_lora, 16) ||
+      bad_ptr(a->q_lora_scale, 2) || bad_ptr(a->q, 16) || bad_ptr(a->kv_cache, 16) || bad_ptr(a->slot, 8))
+    return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+size_t dsa_mla_prolog_workspace(const dsa_mla_prolog_args* a) {
+  if (check_mla(a) != DSA_OK || a->T == 0) return 0;
+  return mla_workspace(*a);
+}
+
+int dsa_mla_prolog(const dsa_mla_prolog_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_mla(a);
+  if (st != DSA_OK || a->T == 0) return st;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < mla_workspace(*a)) return DSA_ERR_WORKSPACE;
+  return launch_mla(*a, ws, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -60,6 +60,38 @@ class PrologBuffers:
         B.dsa_indexer_prolog(self.args, self.ws, stream)
 
 
+class MlaBuffers:
+    """Device copies of a workloads.MlaInputs plus the MLA Prolog's outputs
+    (q_lora, q_lora_scale, q) and a latent cache of ``cache_rows`` rows."""
+
+    def __init__(self, p, device, cache_rows: int, kv_fill: float = 0.0):
+        self.p = p
+        d = device
+        self.x = to_dev(p.x, d, "bf16")
+        self.w_dq = to_dev(p.w_dq, d, "bf16")
+        self.gamma_q = to_dev(p.gamma_q, d)
+        self.w_dkv = to_dev(p.w_dkv, d, "bf16")
+        self.gamma_kv = to_dev(p.gamma_kv, d)
+        self.w_uq = to_dev(p.w_uq, d)
+        self.w_uq_scale = to_dev(p.w_uq_scale, d)
+        self.w_uk = to_dev(p.w_uk, d, "bf16")
+        self.pos = to_dev(p.pos, d)
+        self.rope_cos = to_dev(p.rope_cos, d)
+        self.rope_sin = to_dev(p.rope_sin, d)
+        self.slot = to_dev(p.slot, d)
+        self.q_lora = torch.zeros(p.T, p.K_q, dtype=torch.int8, device=d)
+        self.q_lora_scale = torch.zeros(p.T, dtype=torch.float16, device=d)
+        self.q = torch.zeros(p.T, p.H, 576, dtype=torch.bfloat16, device=d)
+        self.kv_cache = torch.full((cache_rows, 576), kv_fill, dtype=torch.bfloat16, device=d)
+        self.args = B.mla_args(self.x, self.w_dq, self.gamma_q, self.w_dkv, self.gamma_kv, p.rms_eps, self.w_uq,
+                               self.w_uq_scale, self.w_uk, self.pos, self.rope_cos, self.rope_sin,
+                               p.rope_interleaved, self.q_lora, self.q_lora_scale, self.q, self.kv_cache, self.slot)
+        self.ws = torch.zeros(max(B.workspace_bytes("mla", self.args), 256), dtype=torch.uint8, device=d)
+
+    def run(self, stream=None):
+        B.dsa_mla_prolog(self.args, self.ws, stream)
+
+
 class DecodeBuffers:
     """Device copies of a workloads.DecodeInputs and the indexer/attention
     outputs.  ``q_idx``/``q_idx_scale``/``w_idx`` may be replaced by the

@@ -45,7 +45,8 @@ def test_struct_layout_matches_header(lib, tmp_path):
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dsa.h"', "int main(void) {"]
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
                       ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs),
-                      ("dsa_int8_gemm_args", B.Int8GemmArgs), ("dsa_mhc_args", B.MhcArgs)):
+                      ("dsa_int8_gemm_args", B.Int8GemmArgs), ("dsa_mhc_args", B.MhcArgs),
+                      ("dsa_mla_prolog_args", B.MlaArgs)):
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
         for f, _ in py._fields_:
             lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
@@ -57,7 +58,8 @@ def test_struct_layout_matches_header(lib, tmp_path):
     got = dict(line.split() for line in out if line)
     for cname, py in (("dsa_prolog_args", B.PrologArgs), ("dsa_topk_args", B.TopkArgs),
                       ("dsa_attn_args", B.AttnArgs), ("dsa_act_quant_args", B.ActQuantArgs),
-                      ("dsa_int8_gemm_args", B.Int8GemmArgs), ("dsa_mhc_args", B.MhcArgs)):
+                      ("dsa_int8_gemm_args", B.Int8GemmArgs), ("dsa_mhc_args", B.MhcArgs),
+                      ("dsa_mla_prolog_args", B.MlaArgs)):
         assert int(got[cname]) == ctypes.sizeof(py)
         for f, _ in py._fields_:
             assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, f"{cname}.{f}"
@@ -67,7 +69,7 @@ def test_status_strings(lib):
     from sparse_attention_prolog_gb300 import binding as B
     assert B.status_string(0) == "ok"
     assert "workspace" in B.status_string(3)
-    assert lib.dsa_abi_version() == 101
+    assert lib.dsa_abi_version() == 102
 
 
 def test_host_validation_rejects_before_launch(lib):
@@ -133,6 +135,22 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_mhc(ctypes.byref(h), null) == 1                         # comb not 16-byte aligned
     h.eps, h.n = 1e-6, 0
     assert lib.dsa_mhc(ctypes.byref(h), null) == 0                         # empty: no-op
+    ptrs = [(1 << 20) * (i + 1) for i in range(16)]
+    m = B.MlaArgs(8, 128, 1536, 7168, 1e-6, 4096, 0, *ptrs, 64)
+    ws = ctypes.c_void_p(1 << 30)
+    need = lib.dsa_mla_prolog_workspace(ctypes.byref(m))
+    assert need >= 8 * (1536 + 576) * 4 + 8 * 128 * 128 * 4
+    assert lib.dsa_mla_prolog(ctypes.byref(m), null, 0, null) == 3          # no workspace
+    m.T = 33
+    assert lib.dsa_mla_prolog(ctypes.byref(m), ws, need, null) == 2         # T > 32
+    m.T, m.K_q = 8, 1000
+    assert lib.dsa_mla_prolog(ctypes.byref(m), ws, need, null) == 2         # K_q % 128
+    m.K_q, m.H = 1536, 0
+    assert lib.dsa_mla_prolog(ctypes.byref(m), ws, need, null) == 1         # no heads
+    m.H, m.q = 128, (1 << 20) * 18 + 4
+    assert lib.dsa_mla_prolog(ctypes.byref(m), ws, need, null) == 1         # q not 16-byte aligned
+    m.T = 0
+    assert lib.dsa_mla_prolog(ctypes.byref(m), null, 0, null) == 0          # empty: no-op
 
 
 def test_missing_library_fails_loudly(tmp_path):
