@@ -28,7 +28,7 @@ __all__ = [
     "bf16_bits_to_f64", "sylvester_hadamard", "hadamard_rows", "dynamic_quant",
     "int8_gemm_dequant", "int8_gemm", "act_quant", "rope", "layer_norm", "indexer_prolog",
     "indexer_dots", "indexer_scores_token", "topk_indices",
-    "sparse_attention_token", "sparse_attention", "logical_rows", "mhc",
+    "sparse_attention_token", "sparse_attention", "cache_rows", "logical_rows", "mhc",
     "rms_norm", "mla_q", "mla_kv", "mla_prolog",
 ]
 
@@ -220,14 +220,22 @@ def indexer_prolog(p, k_cache=None, k_scale_cache=None):
 # Lightning Indexer  [V3.2-PyPTO §Lightning Indexer: int8 q against the C8
 # key cache, then a per-query TopK; §Indexer Prolog for the scale types]
 # ----------------------------------------------------------------------------
-def logical_rows(inp, b: int, n: int) -> np.ndarray:
-    """Physical cache rows of keys 0..n-1 of sequence b (contiguous
-    [B, max_L, .] or paged through block_table[b, s // block_size])."""
-    s = np.arange(n, dtype=np.int64)
+def cache_rows(inp, b: int, s) -> np.ndarray:
+    """Physical cache rows of the keys at logical positions s of sequence b:
+    b * max_L + s for a contiguous [B, max_L, .] cache, else block
+    block_table[b, s // block_size], row s % block_size of that block
+    (reading: the paged-cache addressing of the PagedAttention-style block
+    table that the ragged workload uses; the pages give block sizes only)."""
+    s = np.asarray(s, dtype=np.int64)
     if inp.block_table is None:
         return b * inp.max_L + s
-    blk = inp.block_table[b, s // inp.block_size].astype(np.int64)
+    blk = np.asarray(inp.block_table)[b, s // inp.block_size].astype(np.int64)
     return blk * inp.block_size + s % inp.block_size
+
+
+def logical_rows(inp, b: int, n: int) -> np.ndarray:
+    """Physical cache rows of keys 0..n-1 of sequence b."""
+    return cache_rows(inp, b, np.arange(n, dtype=np.int64))
 
 
 def indexer_dots(q_tok: np.ndarray, keys: np.ndarray) -> np.ndarray:
@@ -307,7 +315,7 @@ def sparse_attention(inp, topk_idx: np.ndarray, tokens=None, sink=None):
         idx = np.asarray(topk_idx[t], dtype=np.int64)
         idx = idx[idx >= 0]
         b = int(inp.seq_of_token[t])
-        phys = np.asarray(inp.physical_row(b, idx)) if idx.size else np.zeros(0, np.int64)
+        phys = cache_rows(inp, b, idx) if idx.size else np.zeros(0, np.int64)
         rows = bf16_bits_to_f64(inp.kv_cache[phys])
         o, l = sparse_attention_token(bf16_bits_to_f64(inp.q_attn[t]), rows, inp.scale, inp.d_v, sink)
         outs.append(o)

@@ -209,13 +209,6 @@ class DecodeInputs:
     q_attn: np.ndarray         # bf16 bits [T, H, d_qk]
     kv_cache: np.ndarray       # bf16 bits [rows, d_qk]
 
-    def physical_row(self, b: int, s: np.ndarray) -> np.ndarray:
-        s = np.asarray(s, dtype=np.int64)
-        if self.block_table is None:
-            return b * self.max_L + s
-        blk = self.block_table[b, s // self.block_size].astype(np.int64)
-        return blk * self.block_size + s % self.block_size
-
 
 def make_decode_inputs(B, n_q, seq_lens, H_I, d_I, topk, H, seed, max_L=None,
                        w_sigma=None, block_size=0, d_qk=576, d_v=512,

@@ -609,3 +609,35 @@ def test_mla_cache_slots():
     np.testing.assert_array_equal(cache[4], r["kv"][0])
     np.testing.assert_array_equal(cache[1], r["kv"][2])
     assert np.all(cache[[0, 2, 3, 5]] == 7.0)
+
+
+def test_paged_and_contiguous_caches_agree():
+    """The same sequences stored contiguously and in shuffled 16-row blocks
+    (the blocks scattered here, block by block, without the oracle's address
+    function) give the same key rows and the same sparse attention; an
+    identity block table reproduces the contiguous addresses."""
+    from types import SimpleNamespace
+    r = np.random.default_rng(77)
+    B, max_L, bs, d_qk, d_v, H, T = 3, 64, 16, 40, 32, 2, 4
+    nblk = max_L // bs
+    contig = W.f32_to_bf16_bits(r.standard_normal((B * max_L, d_qk)).astype(np.float32))
+    table = r.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    paged = np.zeros_like(contig)
+    for b in range(B):
+        for j in range(nblk):
+            paged[table[b, j] * bs:(table[b, j] + 1) * bs] = contig[b * max_L + j * bs:b * max_L + (j + 1) * bs]
+    q = W.f32_to_bf16_bits(r.standard_normal((T, H, d_qk)).astype(np.float32))
+    seq = np.array([0, 2, 1, 2], np.int32)
+    common = dict(T=T, max_L=max_L, block_size=bs, seq_of_token=seq, q_attn=q, scale=d_qk ** -0.5, d_v=d_v)
+    a = SimpleNamespace(block_table=None, kv_cache=contig, **common)
+    p = SimpleNamespace(block_table=table, kv_cache=paged, **common)
+    for b in range(B):
+        np.testing.assert_array_equal(paged[O.logical_rows(p, b, 50)], contig[b * max_L + np.arange(50)])
+    ident = SimpleNamespace(block_table=np.arange(B * nblk, dtype=np.int32).reshape(B, nblk), block_size=bs, max_L=max_L)
+    np.testing.assert_array_equal(O.cache_rows(ident, 2, [0, 17, 63]), 2 * max_L + np.array([0, 17, 63]))
+    idx = np.stack([r.choice(max_L, 20, replace=False) for _ in range(T)])
+    idx[1, 5:] = -1
+    oa, la = O.sparse_attention(a, idx)
+    op, lp = O.sparse_attention(p, idx)
+    np.testing.assert_array_equal(oa, op)
+    np.testing.assert_array_equal(la, lp)
