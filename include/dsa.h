@@ -30,8 +30,9 @@
  *     launch, and a rejected call enqueues nothing.
  *   - Return value: DSA_OK or an error status.  No C++ exception crosses
  *     this boundary.  A launch failure returns DSA_ERR_CUDA.  A kernel whose
- *     bounded wait expired records it in a device error word that
- *     dsa_get_device_error() reads (DSA_ERR_DEVICE_TIMEOUT).
+ *     bounded wait expired, or that met invalid device-side data, records it
+ *     in a device error word that dsa_get_device_error() reads
+ *     (DSA_ERR_DEVICE_TIMEOUT, DSA_ERR_DEVICE_DATA).
  *   - T = 0 (no query tokens) is a no-op returning DSA_OK.
  *   - Kernels are launched with programmatic dependent launch: a call's
  *     kernel may start while the kernel enqueued just before it on the
@@ -59,7 +60,11 @@ typedef enum {
   DSA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d_I = 96)  */
   DSA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than needed   */
   DSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed       */
-  DSA_ERR_DEVICE_TIMEOUT = 5 /* a device-side bounded wait expired         */
+  DSA_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait expired        */
+  DSA_ERR_DEVICE_DATA = 6     /* a kernel met invalid device-side data: an
+                                 out-of-range slot or position, an unmapped
+                                 page, or a workspace not zero-filled; what
+                                 depended on it was not written            */
 } dsa_status_t;
 
 /* Static description of a status code.  Never NULL. */
@@ -70,7 +75,8 @@ int dsa_abi_version(void);
 
 /* Synchronises `stream`, then returns DSA_OK if no kernel of this library
  * has recorded a device-side error since the last call, else
- * DSA_ERR_DEVICE_TIMEOUT; the error word is cleared.  DSA_ERR_CUDA if the
+ * DSA_ERR_DEVICE_TIMEOUT if a bounded wait expired, else
+ * DSA_ERR_DEVICE_DATA; the error word is cleared.  DSA_ERR_CUDA if the
  * synchronisation itself fails. */
 int dsa_get_device_error(void* stream);
 

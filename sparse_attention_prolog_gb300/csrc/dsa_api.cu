@@ -183,11 +183,12 @@ const char* dsa_status_string(int status) {
     case DSA_ERR_WORKSPACE: return "workspace missing or too small";
     case DSA_ERR_CUDA: return "CUDA error";
     case DSA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case DSA_ERR_DEVICE_DATA: return "invalid device-side data (index, page or unzeroed workspace)";
     default: return "unknown status";
   }
 }
 
-int dsa_abi_version(void) { return 102; }
+int dsa_abi_version(void) { return 103; }
 
 int dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
@@ -198,7 +199,7 @@ int dsa_get_device_error(void* stream) {
   if (v == 0) return DSA_OK;
   const uint32_t zero = 0;
   if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DSA_ERR_CUDA;
-  return DSA_ERR_DEVICE_TIMEOUT;
+  return (v & kErrTimeout) ? DSA_ERR_DEVICE_TIMEOUT : DSA_ERR_DEVICE_DATA;
 }
 
 size_t dsa_indexer_prolog_workspace(const dsa_prolog_args* a) {

@@ -7,6 +7,13 @@
 
 namespace dsa {
 
+// Bits of the per-library device error word: a bounded wait that timed out;
+// invalid device-side data (an out-of-range slot or position, an unmapped
+// page, a histogram that disagrees with its row because the workspace was
+// not zero-filled).
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrBadIndex = 2u;
+
 // Address of the library's device error word on the current device
 // (resolved once per device).  nullptr if CUDA fails.
 uint32_t* error_word();

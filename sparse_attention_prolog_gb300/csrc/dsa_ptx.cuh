@@ -19,9 +19,8 @@ namespace dsa {
 // phase completes or this many nanoseconds pass, then re-checks the clock.
 constexpr uint32_t kSuspendHintNs = 20000;
 
-// Bit set in the per-library error word by a wait that timed out.
-constexpr uint32_t kErrTimeout = 1u;
-constexpr uint32_t kErrBadIndex = 2u;
+// The error-word bits (kErrTimeout, kErrBadIndex) are defined in
+// dsa_internal.h, which every translation unit includes first.
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -69,7 +69,10 @@ def test_status_strings(lib):
     from sparse_attention_prolog_gb300 import binding as B
     assert B.status_string(0) == "ok"
     assert "workspace" in B.status_string(3)
-    assert lib.dsa_abi_version() == 102
+    assert lib.dsa_abi_version() == 103
+    assert "timed out" in B.status_string(5)
+    assert "device-side data" in B.status_string(6)
+    assert B.status_string(7) == "unknown status"
 
 
 def test_host_validation_rejects_before_launch(lib):
