@@ -89,14 +89,63 @@ def topk_bytes(inp) -> int:
 
 
 # ----------------------------------------------------------------- clocks
+CLOCK_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def _sample_time(stamp: str):
+    """nvidia-smi's timestamp field ('YYYY/MM/DD HH:MM:SS.mmm', local time)
+    as seconds since the epoch, or None."""
+    import datetime
+    try:
+        return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    except ValueError:
+        return None
+
+
+def summarize_clocks(lines, uuid: str, t0: float = None, t1: float = None) -> dict:
+    """Median SM clock, the maximum clock and the throttle reasons seen in the
+    samples of one GPU (matched by uuid; index 0 if no uuid matches) taken
+    within [t0, t1] (host wall-clock seconds).  If no sample fell inside the
+    window (a region shorter than the polling period) every sample is used
+    and "samples_in_window" says 0."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) >= 11:
+            rows.append(parts)
+    want = uuid.lower().replace("gpu-", "")
+    mine = [r for r in rows if r[2].lower().replace("gpu-", "") == want]
+    if mine:
+        rows = mine
+    elif len({r[2] for r in rows}) > 1:
+        rows = [r for r in rows if r[1] == "0"]
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    inside = rows
+    if t0 is not None and t1 is not None:
+        inside = [r for r in rows if (_sample_time(r[0]) is not None and t0 <= _sample_time(r[0]) <= t1)]
+    used = inside if inside else rows
+    num = lambda v: v.replace(".", "", 1).isdigit()
+    sm = [float(r[3]) for r in used if num(r[3])]
+    mx = [float(r[4]) for r in used if num(r[4])]
+    reasons = sorted({CLOCK_REASONS[i] for r in used for i in range(4) if r[7 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(used), "samples_in_window": len(inside)}
+
+
 class ClockSampler:
-    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi polling every PERIOD_MS around a timed region: entering
+    waits for the first sample, so the poller is live when the region
+    starts; the summary keeps the samples stamped inside the region."""
+    QUERY = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, uuid: str):
         self.uuid = uuid
         self.proc = None
+        self.t0 = self.t1 = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
 
     def __enter__(self):
@@ -104,13 +153,20 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", str(self.PERIOD_MS)], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        if self.proc is not None:
+            deadline = time.time() + 5.0
+            while time.time() < deadline and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
         if self.proc is not None:
+            time.sleep(2 * self.PERIOD_MS / 1000.0)  # the samples of the region's last moments
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -121,27 +177,8 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 10:
-                continue
-            rows.append(parts)
-        ids = {r[1] for r in rows}
-        want = self.uuid.lower().replace("gpu-", "")
-        mine = [r for r in rows if r[1].lower().replace("gpu-", "") == want]
-        if mine:
-            rows = mine
-        elif len(ids) > 1:
-            rows = [r for r in rows if r[0] == "0"]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        with open(self.path) as f:
+            return summarize_clocks(f.readlines(), self.uuid, self.t0, self.t1)
 
 
 def device_uuid(dev) -> str:
@@ -515,7 +552,7 @@ def run_act_quant(args):
         for _ in range(args.warmup):
             B.dsa_act_quant(x, y, sc, False, stream)
     stream.synchronize()
-    K = min(args.steps, 200)
+    K = min(args.steps, 3000)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with ClockSampler(device_uuid(dev)) as clk:
         with torch.cuda.stream(stream):
@@ -566,7 +603,7 @@ def run_int8_gemm(args):
         for _ in range(args.warmup):
             B.dsa_int8_gemm(a, sa, b, sb, c, stream)
     stream.synchronize()
-    K_steps = min(args.steps, 200)
+    K_steps = min(args.steps, 3000)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
     with ClockSampler(device_uuid(dev)) as clk:
         with torch.cuda.stream(stream):
@@ -617,7 +654,7 @@ def run_mhc(args):
         for _ in range(args.warmup):
             B.dsa_mhc(mixes, scale, base, hc, iters, 1e-6, pre, post, comb, stream)
     stream.synchronize()
-    K_steps = min(args.steps, 200)
+    K_steps = min(args.steps, 3000)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
     with ClockSampler(device_uuid(dev)) as clk:
         with torch.cuda.stream(stream):
@@ -668,7 +705,7 @@ def run_mla(args):
             bufs[i % 3].run(stream)
     stream.synchronize()
     assert B.device_error(stream) == 0
-    K_steps = min(args.steps, 300)
+    K_steps = min(args.steps, 3000)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
     with ClockSampler(device_uuid(dev)) as clk:
         with torch.cuda.stream(stream):
