@@ -59,6 +59,19 @@ def test_quant_argmax_maps_to_127_and_error_bound():
     assert np.abs(c).max() <= 127
 
 
+def test_quant_codes_are_nearest_on_the_stored_scale_grid():
+    """Away from the clamp, code * scale is the point of the stored fp16
+    scale's grid nearest to x, to within the fp32 rounding of x and of
+    x / scale (1.5e-5 of a step at |code| <= 127): the division uses the
+    stored scale, not absmax / 127 before its rounding to fp16."""
+    x = rng.standard_normal((200, 128)) * rng.uniform(0.01, 10, size=(200, 1))
+    c, s = O.dynamic_quant(x)
+    sf = np.broadcast_to(s.astype(np.float64)[:, None], x.shape)
+    inside = np.abs(x) <= 126.5 * sf
+    err = np.abs(c * sf - x)
+    assert (err[inside] <= sf[inside] * (0.5 + 3e-5)).all()
+
+
 def test_quant_zero_row_and_exact_grid():
     c, s = O.dynamic_quant(np.zeros((2, 64)))
     assert (c == 0).all() and (s == 0).all()
@@ -326,7 +339,9 @@ def test_attention_special_cases():
     q2 = q.copy(); q2[:, :dv] = 0
     mix = rows[1:5].copy(); mix[:, dv:] = rows[0, dv:]
     out2, lse2 = O.sparse_attention_token(q2, mix, 0.1, dv)
-    np.testing.assert_allclose(out2, np.repeat(mix[:, :dv].mean(0, keepdims=True), H, 0), rtol=1e-12)
+    # (sums of O(1) terms in another order: equal to float64 rounding, so
+    # entries that nearly cancel get an absolute bound at that scale)
+    np.testing.assert_allclose(out2, np.repeat(mix[:, :dv].mean(0, keepdims=True), H, 0), rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(lse2, 0.1 * q2 @ rows[0] + math.log(4), rtol=1e-12)
     out3, lse3 = O.sparse_attention_token(q, rows[:0], 0.1, dv)
     assert (out3 == 0).all() and np.isneginf(lse3).all()
@@ -335,7 +350,7 @@ def test_attention_special_cases():
     w = np.exp(0.1 * q @ rows[[0, 1]].T)
     w[:, 0] *= 2
     ref = (w @ rows[[0, 1], :dv]) / w.sum(1, keepdims=True)
-    np.testing.assert_allclose(o_dup, ref, rtol=1e-12)
+    np.testing.assert_allclose(o_dup, ref, rtol=1e-12, atol=1e-14)
 
 
 def test_attention_sink_is_a_zero_value_key_with_logit_sink():
@@ -475,6 +490,19 @@ def test_mhc_pins():
     _, _, c2 = O.mhc(shifted, np.ones(3), base, hc, 3, eps)
     np.testing.assert_allclose(c1, c2, rtol=1e-12)
 
+
+
+def test_mhc_hand_worked_eps_placement():
+    """hc = 2, zero inputs, eps = 0.1, worked by hand: the row softmax gives
+    1/2 everywhere, + eps 0.6; divided by the column sums 1.2 + eps: 6/13.
+    One more round: rows sum to 12/13 + 1/10 = 133/130, giving 60/133;
+    columns sum to 120/133 + 1/10 = 1333/1330, giving 600/1333.  The gates:
+    pre = 1/2 + eps, post = 2 * 1/2."""
+    for iters, want in ((0, 6 / 13), (1, 600 / 1333)):
+        pre, post, c = O.mhc(np.zeros((1, 8)), np.ones(3), np.zeros(8), 2, iters, 0.1)
+        np.testing.assert_allclose(c, np.full((1, 2, 2), want), rtol=1e-14)
+        np.testing.assert_allclose(pre, 0.6, rtol=1e-15)
+        np.testing.assert_allclose(post, 1.0, rtol=1e-15)
 
 
 def test_mhc_scale_order_and_sinkhorn_limit():
