@@ -78,6 +78,47 @@ MUTANTS = [
      "return np.concatenate([lat, pe], axis=-1)", "return np.concatenate([pe, lat], axis=-1)"),
     ("paged rows offset by the block number instead of the row in the block",
      "return blk * inp.block_size + s % inp.block_size", "return blk * inp.block_size + s // inp.block_size"),
+    ("k stream without its Hadamard transform",
+     "k, k_scale = dynamic_quant(hadamard_rows(kr))", "k, k_scale = dynamic_quant(kr)"),
+    ("LayerNorm without beta",
+     "/ np.sqrt(var + eps) * np.asarray(gamma, F64) + np.asarray(beta, F64)",
+     "/ np.sqrt(var + eps) * np.asarray(gamma, F64)"),
+    ("weight stream without w_scale", "* float(p.w_scale)).astype(np.float32)", ").astype(np.float32)"),
+    ("q stream without RoPE",
+     "qr = rope(qf, p.pos, p.rope_cos, p.rope_sin, p.d_rope, bool(p.rope_interleaved))", "qr = qf"),
+    ("key-cache scale taken from the first token",
+     "k_scale_cache[p.slot[t]] = k_scale[t]", "k_scale_cache[p.slot[t]] = k_scale[0]"),
+    ("act_quant dividing in float64 instead of the page's fp32",
+     "        y = x32 / sd\n", "        y = x32.astype(np.float64) / sd\n"),
+    ("int8 GEMM output left in fp32",
+     "return int8_gemm_dequant(a, a_scale, b, b_scale).astype(np.float16)",
+     "return int8_gemm_dequant(a, a_scale, b, b_scale).astype(np.float32)"),
+    ("attention lse without the running maximum",
+     "return out, (m + np.log(l))[:, 0]", "return out, (np.log(l))[:, 0]"),
+    ("top-k padded with 0 instead of -1",
+     "out = np.full(k, -1, dtype=np.int64)", "out = np.zeros(k, dtype=np.int64)"),
+    ("indexer weights without the q scale",
+     "coef = np.asarray(w_tok, F64) * np.asarray(q_scale_tok, F64)", "coef = np.asarray(w_tok, F64)"),
+    ("attention sink ignored when nothing is selected",
+     "return np.zeros((H, d_v)), (np.full(H, -np.inf) if sk is None else sk.copy())",
+     "return np.zeros((H, d_v)), np.full(H, -np.inf)"),
+    ("mHC pre gate without eps", "pre = sig(z[:, :hc]) + eps", "pre = sig(z[:, :hc])"),
+    ("mHC first column step without eps",
+     "c = c / c.sum(axis=-1, keepdims=True) + eps\n    c = c / (c.sum(axis=-2, keepdims=True) + eps)",
+     "c = c / c.sum(axis=-1, keepdims=True) + eps\n    c = c / c.sum(axis=-2, keepdims=True)"),
+    ("RMSNorm without eps",
+     "x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)", "x / np.sqrt((x * x).mean(axis=-1, keepdims=True))"),
+    ("MLA query latent without gamma_q",
+     "c_q = rms_norm(x @ bf16_bits_to_f64(p.w_dq).T, p.gamma_q, p.rms_eps)",
+     "c_q = rms_norm(x @ bf16_bits_to_f64(p.w_dq).T, np.ones_like(p.gamma_q), p.rms_eps)"),
+    ("MLA latent row without gamma_kv",
+     "lat = rms_norm(c[:, :MLA_D_C], gamma_kv, eps)", "lat = rms_norm(c[:, :MLA_D_C], np.ones_like(gamma_kv), eps)"),
+    ("MLA query rotated one position late",
+     "q_pe = rope(u[..., MLA_D_N:], pos, cos_tab, sin_tab, MLA_D_R, interleaved)",
+     "q_pe = rope(u[..., MLA_D_N:], np.asarray(pos) + 1, cos_tab, sin_tab, MLA_D_R, interleaved)"),
+    ("MLA up-projection without the q_lora scale",
+     "u = int8_gemm_dequant(q_lora, q_lora_scale, w_uq, w_uq_scale)",
+     "u = int8_gemm_dequant(q_lora, np.ones_like(q_lora_scale), w_uq, w_uq_scale)"),
 ]
 
 

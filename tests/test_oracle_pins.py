@@ -235,6 +235,43 @@ def test_prolog_weight_stream_and_cache_write_brute_force():
     assert (cache[[0, 1, 2, 4]] == 9).all() and (cs[[0, 1, 2, 4]] == 7).all()
 
 
+def test_prolog_cache_rows_take_each_tokens_key():
+    """Slots [3, -1, 1]: rows 3 and 1 receive the codes and the scale of
+    tokens 0 and 2 (keys in different directions, so different scales);
+    token 1 writes nothing."""
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    p = _prolog_fixture(T=3, Dx=8, pos=(0, 1, 2))
+    r2 = np.random.default_rng(31)
+    p.x = f32_to_bf16_bits(r2.standard_normal((3, 8)).astype(np.float32))
+    p.w_k = f32_to_bf16_bits(r2.standard_normal((128, 8)).astype(np.float32))
+    p.slot = np.array([3, -1, 1], np.int64)
+    cache = np.full((5, 128), 9, np.int8)
+    cs = np.full(5, 7, np.float16)
+    r = O.indexer_prolog(p, cache, cs)
+    assert r["k_scale"][0] != r["k_scale"][2]
+    for row, t in ((3, 0), (1, 2)):
+        np.testing.assert_array_equal(cache[row], r["k"][t])
+        assert cs[row] == r["k_scale"][t]
+    assert (cache[[0, 2, 4]] == 9).all() and (cs[[0, 2, 4]] == 7).all()
+
+
+def test_prolog_q_and_k_rotary_relative_position():
+    """The Hadamard transform is orthonormal, so the pre-quantisation q . k
+    of two tokens is the dot of their rotated vectors: moving both positions
+    by the same amount keeps it, moving only one changes it."""
+    from sparse_attention_prolog_gb300.workloads import make_prolog_inputs
+
+    def score(pos):
+        p = make_prolog_inputs(T=2, pos=pos, slot=[-1, -1], seed=41, H_I=2, d_I=64, K_q=128, D_x=128,
+                               with_weights=False, max_pos=64)
+        r = O.indexer_prolog(p)
+        return np.einsum("hd,d->h", r["q_prequant"][0], r["k_prequant"][1])
+
+    a, b, c = score([5, 20]), score([17, 32]), score([17, 20])
+    np.testing.assert_allclose(a, b, rtol=1e-5)
+    assert not np.allclose(a, c, rtol=1e-3)
+
+
 # ------------------------------------------------------- Lightning Indexer
 def _read_golden():
     g = {}
@@ -412,6 +449,11 @@ def test_act_quant_hand_worked_rows():
     y2, s2 = O.act_quant(x, round_scale=True)
     assert s2[0] == np.float32(2.0 ** -5)
     assert y2.tolist() == [[32, -80, 16, 0]]
+    # The division is in fp32, as the page states: for max 0.5859375 the
+    # fp32 scale is a little above max/127, so x = max/2 divided by it is
+    # 63.4999982 exactly but 63.5 in fp32, a tie that goes to the even 64.
+    y3, _ = O.act_quant(_bits([[0.5859375, 0.29296875, -0.29296875, 0.0]]))
+    assert y3.tolist() == [[127, 64, -64, 0]]
 
 
 def test_act_quant_properties():
@@ -626,6 +668,23 @@ def test_mla_one_hot_layout():
         rows = p.w_uq[h * 192:(h + 1) * 192, k].astype(np.float64)
         np.testing.assert_allclose(q[0, h, 512:], rows[128:], rtol=1e-15)
         np.testing.assert_allclose(q[0, h, :512], rows[:128] @ wuk[h], rtol=1e-12)
+
+
+def test_mla_gammas_select_channels():
+    """A one-hot gamma keeps one channel: gamma_q = e_j makes the query
+    latent of every token a single code of magnitude 127 at j; gamma_kv =
+    e_i leaves one nonzero latent dim i in every KV row (the rotary dims
+    have no gamma)."""
+    p = _mla_small()
+    p.gamma_q[:] = 0.0
+    p.gamma_q[9] = 1.5
+    p.gamma_kv[:] = 0.0
+    p.gamma_kv[100] = 0.7
+    r = O.mla_prolog(p)
+    assert (np.abs(r["q_lora"][:, 9]) == 127).all()
+    assert (np.delete(r["q_lora"], 9, axis=1) == 0).all()
+    assert (np.delete(r["kv"][:, :512], 100, axis=1) == 0).all()
+    assert (r["kv"][:, 100] != 0).all() and (r["kv"][:, 512:] != 0).any()
 
 
 def test_mla_cache_slots():
