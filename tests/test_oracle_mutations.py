@@ -119,6 +119,30 @@ MUTANTS = [
     ("MLA up-projection without the q_lora scale",
      "u = int8_gemm_dequant(q_lora, q_lora_scale, w_uq, w_uq_scale)",
      "u = int8_gemm_dequant(q_lora, np.ones_like(q_lora_scale), w_uq, w_uq_scale)"),
+    ("attention taking index -1 as row 0", "idx = idx[idx >= 0]", "idx = np.where(idx >= 0, idx, 0)"),
+    ("mHC one Sinkhorn round too many", "for _ in range(iters):", "for _ in range(iters + 1):"),
+    ("RMSNorm with eps outside the root",
+     "x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)",
+     "x / (np.sqrt((x * x).mean(axis=-1, keepdims=True)) + eps)"),
+    ("LayerNorm without centring the numerator",
+     "return (x - mu) / np.sqrt(var + eps)", "return x / np.sqrt(var + eps)"),
+    ("act_quant scale stored through fp16",
+     "return codes.astype(np.int8), s.astype(np.float32)",
+     "return codes.astype(np.int8), s.astype(np.float16).astype(np.float32)"),
+    ("power-of-two scale one step up when it already is one",
+     "up = np.where(m == 0.5, e - 1, e).astype(np.int32)", "up = e.astype(np.int32)"),
+    ("int8 GEMM with one activation scale for every row",
+     "return acc * np.asarray(a_scale, dtype=F64)[:, None] * np.asarray(b_scale, dtype=F64)[None, :]",
+     "return acc * np.asarray(a_scale, dtype=F64).mean() * np.asarray(b_scale, dtype=F64)[None, :]"),
+    ("attention sink in log2 units", "l = l + np.exp(sk[:, None] - m)", "l = l + np.exp2(sk[:, None] - m)"),
+    ("mHC comb logits scaled by the post scale", "np.full(hc * hc, hc_scale[2])", "np.full(hc * hc, hc_scale[1])"),
+    ("MLA query rotary dims not rotated",
+     "q_pe = rope(u[..., MLA_D_N:], pos, cos_tab, sin_tab, MLA_D_R, interleaved)", "q_pe = u[..., MLA_D_N:]"),
+    ("MLA latent row rotary dims not rotated",
+     "pe = rope(c[:, None, MLA_D_C:], pos, cos_tab, sin_tab, MLA_D_R, interleaved)[:, 0, :]", "pe = c[:, MLA_D_C:]"),
+    ("Hadamard applied twice",
+     "return np.asarray(x, dtype=F64) @ (sylvester_hadamard(n) / np.sqrt(n))",
+     "return np.asarray(x, dtype=F64) @ (sylvester_hadamard(n) / np.sqrt(n)) @ (sylvester_hadamard(n) / np.sqrt(n))"),
 ]
 
 

@@ -365,6 +365,25 @@ def test_attention_equals_dense_masked_sdpa():
     np.testing.assert_allclose(lse, scipy.special.logsumexp(full[:, sel], axis=1), rtol=1e-12)
 
 
+def test_attention_padding_selects_nothing():
+    """Through the batched call, -1 entries of a token's index row select
+    nothing: the result is torch's SDPA over the other rows only."""
+    from types import SimpleNamespace
+    r = np.random.default_rng(19)
+    H, L, d, dv = 2, 16, 48, 32
+    q = _bf16(r.standard_normal((1, H, d)))
+    kv = _bf16(r.standard_normal((L, d)))
+    from sparse_attention_prolog_gb300.workloads import f32_to_bf16_bits
+    inp = SimpleNamespace(T=1, max_L=L, block_table=None, block_size=0, seq_of_token=np.zeros(1, np.int32),
+                          q_attn=f32_to_bf16_bits(q.astype(np.float32)), kv_cache=f32_to_bf16_bits(kv.astype(np.float32)),
+                          scale=0.3, d_v=dv)
+    out, _ = O.sparse_attention(inp, np.array([[5, -1, 11, -1, -1]]))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(kv[[5, 11]])[None], torch.from_numpy(kv[[5, 11], :dv])[None],
+        scale=0.3)[0].numpy()
+    np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-12)
+
+
 def test_attention_special_cases():
     H, d, dv = 3, 576, 512
     q = _bf16(rng.standard_normal((H, d)))
@@ -454,6 +473,10 @@ def test_act_quant_hand_worked_rows():
     # 63.4999982 exactly but 63.5 in fp32, a tie that goes to the even 64.
     y3, _ = O.act_quant(_bits([[0.5859375, 0.29296875, -0.29296875, 0.0]]))
     assert y3.tolist() == [[127, 64, -64, 0]]
+    # max 1.984375 = 127/64: the scale is exactly 2^-6, already a power of
+    # two, so round_scale keeps it (codes 127 and 64 for 1.0)
+    y4, s4 = O.act_quant(_bits([[1.984375, 1.0, 0.0, 0.0]]), round_scale=True)
+    assert s4[0] == np.float32(2.0 ** -6) and y4.tolist() == [[127, 64, 0, 0]]
 
 
 def test_act_quant_properties():
@@ -578,10 +601,14 @@ def test_mhc_scale_order_and_sinkhorn_limit():
     z = np.array([[0.7, -0.4], [0.2, 1.1]])
     m2 = np.zeros((1, 2 * 4))
     m2[0, 4:] = z.reshape(-1)
-    _, _, c = O.mhc(m2, np.ones(3), np.zeros(8), 2, 200, 0.0)
-    ratio = np.sqrt(np.exp(z[0, 0] + z[1, 1] - z[0, 1] - z[1, 0]))
-    p = ratio / (1.0 + ratio)
-    np.testing.assert_allclose(c[0], [[p, 1.0 - p], [1.0 - p, p]], atol=1e-12)
+    # the comb logits take hc_scale[2] (0.3 z under scale 5: a cross ratio of
+    # about e^3.9, within reach of 400 rounds)
+    for sc, zz in ((np.ones(3), z), (np.array([2.0, 3.0, 5.0]), 0.3 * z)):
+        m2[0, 4:] = zz.reshape(-1)
+        _, _, c = O.mhc(m2, sc, np.zeros(8), 2, 400, 0.0)
+        ratio = np.sqrt(np.exp(sc[2] * (zz[0, 0] + zz[1, 1] - zz[0, 1] - zz[1, 0])))
+        p = ratio / (1.0 + ratio)
+        np.testing.assert_allclose(c[0], [[p, 1.0 - p], [1.0 - p, p]], atol=1e-12)
 
 
 # ------------------------------------------------------------- MLA Prolog
