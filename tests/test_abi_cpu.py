@@ -169,3 +169,44 @@ def _fresh_load(B, path):
         B.load(path)
     finally:
         B._lib = saved
+
+
+def test_plain_c_program_links_and_calls_the_abi(lib, tmp_path):
+    """The boundary is a C ABI: a C program compiled against dsa.h and
+    linked to libdsa.so reads the version and status strings and gets the
+    host-side rejections (nothing is launched on these paths)."""
+    from sparse_attention_prolog_gb300 import binding
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "dsa.h"
+int main(void) {
+  if (dsa_abi_version() < 100) return 10;
+  if (strcmp(dsa_status_string(DSA_OK), "ok") != 0) return 11;
+  if (strcmp(dsa_status_string(42), "unknown status") != 0) return 12;
+  dsa_mhc_args m;
+  memset(&m, 0, sizeof m);
+  m.n = 4; m.hc = 6; m.iters = 1; m.eps = 1e-6f;
+  if (dsa_mhc(&m, NULL) != DSA_ERR_UNSUPPORTED) return 13;           /* hc 6 */
+  dsa_mla_prolog_args a;
+  memset(&a, 0, sizeof a);
+  a.T = 8; a.H = 128; a.K_q = 1536; a.D_x = 7168; a.rope_max_pos = 1;
+  if (dsa_mla_prolog(&a, NULL, 0, NULL) != DSA_ERR_INVALID_ARG) return 14;  /* null pointers */
+  if (dsa_mla_prolog_workspace(&a) != 0) return 15;                  /* invalid: no size */
+  a.T = 0;
+  if (dsa_mla_prolog(&a, NULL, 0, NULL) != DSA_OK) return 16;        /* empty: no-op */
+  dsa_act_quant_args q;
+  memset(&q, 0, sizeof q);
+  q.M = 2; q.N = 7;
+  if (dsa_act_quant(&q, NULL) != DSA_ERR_UNSUPPORTED) return 17;     /* N % 8 */
+  printf("ok\n");
+  return 0;
+}
+""")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(binding.LIB_PATH)
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe), "-L", libdir, "-ldsa",
+                    f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
