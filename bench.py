@@ -216,7 +216,7 @@ def profiled_traffic(parts):
         if vals.get("source_sha256_16") != src_hash(kernel_file):
             return None
         try:
-            total += float(vals["traffic_bytes_per_launch"])
+            total += float(vals["traffic_bytes_per_launch"].split()[0])
         except (KeyError, ValueError):
             return None
     return total
@@ -572,7 +572,8 @@ def run_act_quant(args):
            "config": {"workload": "act_quant M=16384 N=7168 round_scale=0",
                       "l2": "inputs larger than L2 (235 MB read per launch)"},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                        "traffic": profiled_traffic([("quant.cu", "act_quant_16384x7168.txt")])},
            "gpu_launches": K, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -623,7 +624,8 @@ def run_int8_gemm(args):
            "data": "synthetic (seeded)", "config": {"workload": "int8_gemm M=8 N=24576 K=7168",
                                                    "l2": "weight larger than L2 (176 MB per launch)"},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                        "traffic": profiled_traffic([("quant.cu", "int8_gemm_8x24576x7168.txt")])},
            "gpu_launches": K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -673,7 +675,8 @@ def run_mhc(args):
            "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded)",
            "config": {"workload": "mhc n=1048576 hc=4 iters=20", "l2": "inputs larger than L2 (201 MB per launch)"},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                        "traffic": profiled_traffic([("quant.cu", "mhc_1048576x4.txt")])},
            "gpu_launches": K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -729,7 +732,8 @@ def run_mla(args):
                       "l2": f"3 weight sets rotated ({3 * weights / 1e6:.0f} MB, larger than L2)",
                       "bytes_per_call": nbytes},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind},
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                        "traffic": profiled_traffic([("mla.cu", "mla_prolog_decode_T8.txt")])},
            "gpu_launches": 3 * K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O

@@ -31,3 +31,21 @@ def test_clock_summary_without_samples_in_the_window():
     assert s["samples_in_window"] == 0 and s["samples"] == 2
     assert s["sm_mhz"] == (1980 + 2070) / 2
     assert bench.summarize_clocks([], "GPU-aaa")["reasons"] == ["no samples"]
+
+
+def test_profiled_traffic_needs_the_current_source(tmp_path, monkeypatch):
+    """The traffic of a committed ncu summary counts only when its source
+    hash is the kernel file's current one; a note after the number is
+    allowed; any missing or stale summary makes the total null."""
+    (tmp_path / "profiles").mkdir()
+    csrc = tmp_path / "sparse_attention_prolog_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.src_hash("k.cu")
+    (tmp_path / "profiles" / "a.txt").write_text(f"source_sha256_16: {h}\ntraffic_bytes_per_launch: 1000 (a note)\n")
+    (tmp_path / "profiles" / "b.txt").write_text(f"source_sha256_16: {h}\ntraffic_bytes_per_launch: 24\n")
+    assert bench.profiled_traffic([("k.cu", "a.txt"), ("k.cu", "b.txt")]) == 1024.0
+    assert bench.profiled_traffic([("k.cu", "a.txt"), ("k.cu", "missing.txt")]) is None
+    (csrc / "k.cu").write_text("kernel v2")
+    assert bench.profiled_traffic([("k.cu", "a.txt")]) is None
