@@ -39,8 +39,9 @@
  *     stream is still running, and waits for that kernel to complete before
  *     it reads anything the kernel may have written.  The exceptions are
  *     inputs that a decode step never produces in the kernel right before
- *     the call, which are read as soon as the kernel starts: pos of
- *     dsa_indexer_topk / dsa_indexer_scores and q of dsa_sparse_attn.  The
+ *     the call, which are read as soon as the kernel starts: pos and
+ *     seq_of_token of dsa_indexer_topk / dsa_indexer_scores, and q and
+ *     seq_of_token of dsa_sparse_attn.  The
  *     kernel enqueued just before such a call must not write them (an event
  *     or a memcpy in between lifts the rule).
  */
@@ -80,6 +81,18 @@ int dsa_abi_version(void);
  * synchronisation itself fails. */
 int dsa_get_device_error(void* stream);
 
+/* Sets the time limit of every bounded device-side wait of this library's
+ * kernels on the current device (nanoseconds; 0 restores the default of 4 s;
+ * at most 60 s, else DSA_ERR_INVALID_ARG).  A wait that runs out records
+ * DSA_ERR_DEVICE_TIMEOUT (see dsa_get_device_error) and its CTA leaves its
+ * loops.  The Indexer Prolog first lets its own bulk copies and tensor-core
+ * operations finish (up to 4 s), so after a timeout its next call is safe
+ * once its workspace is zeroed again; the other kernels leave at once, so
+ * shorten the limit only for the Indexer Prolog.  Synchronous: it takes
+ * effect for kernels launched after it returns; call it while none of this
+ * library's kernels runs.  No counterpart on the pages: a test hook. */
+int dsa_set_wait_limit_ns(uint64_t ns);
+
 /* ------------------------------------------------------------------------
  * Indexer Prolog  [V3.2-PyPTO §Indexer Prolog, the three formulas; the
  * quantisation paragraph: W8A8 q.w_qb, A8 indexer q, C8 key cache, FP16
@@ -103,7 +116,9 @@ int dsa_get_device_error(void* stream);
  * Shapes: q_lora int8 [T, K_q]; q_lora_scale fp16 [T]; w_qb int8
  * [H_I*d_I, K_q] (K-major: row n is output channel n); w_qb_scale fp16
  * [H_I*d_I]; x bf16 [T, D_x]; w_k bf16 [d_I, D_x]; w_proj bf16 [H_I, D_x]
- * or NULL; pos int32 [T] (each in [0, rope_max_pos)); q_out int8
+ * or NULL; pos int32 [T] (each in [0, rope_max_pos): a position outside
+ * it is recorded as DSA_ERR_DEVICE_DATA and that token's q, q_scale and key
+ * rows are not written; its w row is); q_out int8
  * [T, H_I, d_I]; q_scale_out fp16 [T, H_I]; k_cache int8 [cache_rows, d_I];
  * k_scale_cache fp16 [cache_rows]; slot int64 [T]: row of k_cache that
  * receives token t's key, -1 = none (slots must not repeat); w_out fp32
@@ -161,8 +176,10 @@ int dsa_indexer_prolog(const dsa_prolog_args* args, void* workspace, size_t work
  *     DSA_ERR_WORKSPACE before anything is enqueued (every supported prolog
  *     shape, T <= 32 and d_I + H_I <= 256 channels, fits).
  *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.
+ *     array's device address (cudaGetSymbolAddress) and caches it with the
+ *     current context; make that first call before any stream capture.  A
+ *     call made under another context (after cudaDeviceReset, or with a
+ *     context the caller created) looks the address up again.
  *   - Every call shares the one array and clears the part that must start at
  *     zero itself; calls that may overlap on the GPU (other streams, other
  *     threads) race on it and must be serialised by the caller. */
@@ -180,7 +197,14 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * followed by -1 when fewer than `topk` keys are visible.  Equal scores at
  * the boundary are broken arbitrarily.
  *
- * Token layout: T = B * n_q; token t belongs to sequence t / n_q.
+ * Token layout: seq_of_token int32 [T] names each token's sequence (in
+ * [0, B)); the tokens of one sequence must be adjacent in the token order
+ * (the indexer scores up to G = min(128 / H_I, 32) adjacent tokens of a
+ * sequence against each key tile together).  seq_of_token == NULL is the
+ * uniform batch: T = B * n_q, token t in sequence t / n_q.  An id outside
+ * [0, B), or a sequence whose tokens are split, is recorded as
+ * DSA_ERR_DEVICE_DATA (that token's outputs are then unspecified).  With a
+ * map, n_q is ignored and T <= 65535.
  * Shapes: q int8 [T, H_I, d_I]; q_scale fp16 [T, H_I]; w fp32 [T, H_I];
  * pos int32 [T] with 0 <= pos[t] < max_L; topk_idx int32 [T, topk];
  * scores_out fp32 [T, max_L] or NULL (when given it receives I, with -inf
@@ -192,7 +216,9 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * max_L = max_blocks * block_size.  k_cache and k_scale are 16-byte
  * aligned (each tile's scales are copied with its keys in bulk).
  * Supported: d_I in {64, 128}; H_I in {4, 8, 16, 32, 64, 128}; topk >= 1;
- * B * ceil(n_q / G) <= 4096 token groups, G = min(n_q, 128 / H_I, 32);
+ * a token-group table that fits shared memory (B * ceil(n_q / G) <= 4096
+ * groups for a uniform batch, G = min(n_q, 128 / H_I, 32); about
+ * ceil(T / G) + B <= 4096 with a map; else DSA_ERR_UNSUPPORTED);
  * max_L a multiple of 128; block_size a multiple of 8 that divides 128 or
  * is a multiple of 128.  Workspace: dsa_indexer_topk_workspace() bytes (the
  * fp32 score rows live there when scores_out is NULL, and, for H_I >= 64
@@ -212,6 +238,7 @@ typedef struct {
   const int32_t* pos;
   int32_t* topk_idx;
   float* scores_out;
+  const int32_t* seq_of_token;
 } dsa_topk_args;
 
 size_t dsa_indexer_topk_workspace(const dsa_topk_args* args);
@@ -254,7 +281,10 @@ int dsa_indexer_dots_debug(const dsa_topk_args* args, int32_t* dots, void* strea
  * so a token with no selected row gets out = 0 and lse = sink[h].  Entries
  * are finite or -inf (-inf = no sink for that head).
  *
- * Token layout: T = B * n_q, token t in sequence t / n_q.
+ * Token layout: seq_of_token int32 [T] (each in [0, B); any order) or NULL
+ * for the uniform batch T = B * n_q, token t in sequence t / n_q.  A token
+ * whose id lies outside [0, B) is recorded as DSA_ERR_DEVICE_DATA and gets
+ * out = 0 (no row read).
  * Shapes: q bf16 [T, H, d_qk]; kv bf16 contiguous [B, max_L, d_qk] or paged
  * [n_rows, d_qk] through block_table int32 [B, max_blocks] as above;
  * topk_idx int32 [T, topk] with entries in [-1, max_L); out bf16
@@ -273,6 +303,7 @@ typedef struct {
   uint16_t* out;
   float* lse;
   const float* sink;
+  const int32_t* seq_of_token;
 } dsa_attn_args;
 
 size_t dsa_sparse_attn_workspace(const dsa_attn_args* args);

@@ -37,7 +37,7 @@ class TopkArgs(ctypes.Structure):
         ("T", c_int), ("B", c_int), ("n_q", c_int), ("H_I", c_int), ("d_I", c_int), ("topk", c_int), ("max_L", c_int),
         ("q", c_ptr), ("q_scale", c_ptr), ("w", c_ptr), ("k_cache", c_ptr), ("k_scale", c_ptr),
         ("block_table", c_ptr), ("block_size", c_int), ("max_blocks", c_int), ("pos", c_ptr),
-        ("topk_idx", c_ptr), ("scores_out", c_ptr),
+        ("topk_idx", c_ptr), ("scores_out", c_ptr), ("seq_of_token", c_ptr),
     ]
 
 
@@ -46,7 +46,7 @@ class AttnArgs(ctypes.Structure):
         ("T", c_int), ("B", c_int), ("n_q", c_int), ("H", c_int), ("d_qk", c_int), ("d_v", c_int), ("topk", c_int),
         ("max_L", c_int), ("scale", ctypes.c_float), ("q", c_ptr), ("kv", c_ptr), ("block_table", c_ptr),
         ("block_size", c_int), ("max_blocks", c_int), ("topk_idx", c_ptr), ("out", c_ptr), ("lse", c_ptr),
-        ("sink", c_ptr),
+        ("sink", c_ptr), ("seq_of_token", c_ptr),
     ]
 
 
@@ -74,7 +74,7 @@ class MlaArgs(ctypes.Structure):
 
 
 EXPORTS = [
-    "dsa_status_string", "dsa_abi_version", "dsa_get_device_error",
+    "dsa_status_string", "dsa_abi_version", "dsa_get_device_error", "dsa_set_wait_limit_ns",
     "dsa_indexer_prolog_workspace", "dsa_indexer_prolog",
     "dsa_indexer_topk_workspace", "dsa_indexer_topk", "dsa_indexer_dots_debug",
     "dsa_indexer_scores", "dsa_topk_from_scores",
@@ -102,6 +102,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_abi_version.restype = c_int
     lib.dsa_get_device_error.argtypes = [c_ptr]
     lib.dsa_get_device_error.restype = c_int
+    lib.dsa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.dsa_set_wait_limit_ns.restype = c_int
     for name, st in (("prolog", PrologArgs), ("topk", TopkArgs), ("attn", AttnArgs)):
         ws = {"prolog": "dsa_indexer_prolog_workspace", "topk": "dsa_indexer_topk_workspace",
               "attn": "dsa_sparse_attn_workspace"}[name]
@@ -188,10 +190,13 @@ def dsa_indexer_prolog_noalloc(args: PrologArgs, stream=None):
 
 # ----------------------------------------------------------------- top-k
 def topk_args(T, B, n_q, H_I, d_I, topk, max_L, q, q_scale, w, k_cache, k_scale, pos, topk_idx,
-              block_table=None, block_size=0, scores_out=None) -> TopkArgs:
+              block_table=None, block_size=0, scores_out=None, seq_of_token=None) -> TopkArgs:
+    """seq_of_token: int32 [T] sequence of each token (then n_q is ignored), or
+    None for the uniform batch T = B * n_q."""
     max_blocks = 0 if block_table is None else block_table.shape[1]
     return TopkArgs(T, B, n_q, H_I, d_I, topk, max_L, _p(q), _p(q_scale), _p(w), _p(k_cache), _p(k_scale),
-                    _p(block_table), block_size, max_blocks, _p(pos), _p(topk_idx), _p(scores_out))
+                    _p(block_table), block_size, max_blocks, _p(pos), _p(topk_idx), _p(scores_out),
+                    _p(seq_of_token))
 
 
 def dsa_indexer_topk(args: TopkArgs, workspace: Optional[torch.Tensor] = None, stream=None, device=None):
@@ -217,10 +222,10 @@ def dsa_topk_from_scores(args: TopkArgs, scores: torch.Tensor, stream=None):
 
 # -------------------------------------------------------------- attention
 def attn_args(T, B, n_q, H, topk, max_L, scale, q, kv, topk_idx, out, lse=None, block_table=None,
-              block_size=0, d_qk=576, d_v=512, sink=None) -> AttnArgs:
+              block_size=0, d_qk=576, d_v=512, sink=None, seq_of_token=None) -> AttnArgs:
     max_blocks = 0 if block_table is None else block_table.shape[1]
     return AttnArgs(T, B, n_q, H, d_qk, d_v, topk, max_L, float(scale), _p(q), _p(kv), _p(block_table),
-                    block_size, max_blocks, _p(topk_idx), _p(out), _p(lse), _p(sink))
+                    block_size, max_blocks, _p(topk_idx), _p(out), _p(lse), _p(sink), _p(seq_of_token))
 
 
 def dsa_sparse_attn(args: AttnArgs, workspace: Optional[torch.Tensor] = None, stream=None, device=None):
@@ -240,6 +245,12 @@ def workspace_bytes(kind: str, args) -> int:
 
 def device_error(stream=None) -> int:
     return int(load().dsa_get_device_error(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    """Time limit of the library's bounded device waits on the current device
+    (0 restores the default)."""
+    _check(load().dsa_set_wait_limit_ns(int(ns)), "dsa_set_wait_limit_ns")
 
 
 def dsa_act_quant(x: torch.Tensor, y: torch.Tensor, scale: torch.Tensor, round_scale: bool = False, stream=None):

@@ -62,7 +62,8 @@ constexpr uint32_t kTmemQ = 0, kTmemS = 288;    // CTA 0 column map
 constexpr int kSmemA = kStagesK * kStageK;  // 221,184 B
 
 struct AttnParams {
-  int T, n_q, H, topk, max_L, n_chunks, chunk_rows, head_blocks;
+  int T, B, n_q, H, topk, max_L, n_chunks, chunk_rows, head_blocks;
+  const int32_t* seq;  // [T] sequence of each token, or null (token t in sequence t / n_q)
   float scale_log2;
   const __nv_bfloat16* q;
   const __nv_bfloat16* kv;
@@ -137,9 +138,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const int chunk = blockIdx.x >> 1, hb = blockIdx.y, t = blockIdx.z;
-  const int b = t / P.n_q;
+  int b = t / P.n_q;
+  bool bad_seq = false;
+  if (P.seq != nullptr) {  // a token outside [0, B) reads no row and gets out = 0
+    b = __ldg(P.seq + t);
+    bad_seq = b < 0 || b >= P.B;
+    if (bad_seq) {
+      if (tid == 0 && rank == 0 && chunk == 0 && hb == 0) atomicOr(P.err, kErrBadIndex);
+      b = 0;
+    }
+  }
   const int slot_begin = chunk * P.chunk_rows;
-  const int rows_here = max(0, min(P.chunk_rows, P.topk - slot_begin));
+  const int rows_here = bad_seq ? 0 : max(0, min(P.chunk_rows, P.topk - slot_begin));
   const int n_tiles = (rows_here + kRows - 1) / kRows;
   const int32_t* idx_row = P.idx + static_cast<size_t>(t) * P.topk;
 
@@ -618,7 +628,8 @@ size_t attn_workspace(const dsa_attn_args& a) {
 int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s) {
   AttnParams P{};
   plan(a, P.head_blocks, P.n_chunks, P.chunk_rows);
-  P.T = a.T; P.n_q = a.n_q; P.H = a.H; P.topk = a.topk; P.max_L = a.max_L;
+  P.T = a.T; P.B = a.B; P.n_q = a.n_q; P.H = a.H; P.topk = a.topk; P.max_L = a.max_L;
+  P.seq = a.seq_of_token;
   P.scale_log2 = a.scale * 1.4426950408889634f;
   P.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   P.kv = reinterpret_cast<const __nv_bfloat16*>(a.kv);

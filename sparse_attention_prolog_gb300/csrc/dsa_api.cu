@@ -2,17 +2,31 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <cstddef>
 #include <mutex>
 #include "dsa_internal.h"
+#include "dsa_ptx.cuh"
 
 namespace dsa {
 
-// One word per device; kernels OR error bits into it.
-static __device__ uint32_t g_error_word;
+// Per device: the error word kernels OR their error bits into, and the time
+// limit of their bounded waits (read through the same pointer, see
+// wait_limit_ns() in dsa_ptx.cuh).
+struct DeviceControl {
+  uint32_t error_word;
+  uint32_t reserved;
+  uint64_t wait_limit_ns;
+};
+static_assert(offsetof(DeviceControl, wait_limit_ns) == kWaitLimitOffset, "wait limit offset");
+static __device__ __align__(16) DeviceControl g_ctl = {0u, 0u, DSA_WAIT_NS};
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Device address of g_ctl per device, with the context it was
+// resolved in: a different current context (a reset device, a context the
+// caller created) resolves it again.
+void* g_err_ctx[kMaxDevices] = {};
 uint32_t* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 
@@ -23,14 +37,36 @@ int current_device() {
 }
 }  // namespace
 
+void* current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!fn) {
+      cudaDriverEntryPointQueryResult q;
+      void* p = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !p)
+        return nullptr;
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }
+  }
+  CUcontext c = nullptr;
+  if (fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 uint32_t* error_word() {
   const int d = current_device();
   if (d < 0) return nullptr;
+  // cudaGetDevice made the device's primary context current if none was.
+  void* ctx = current_context();
+  if (!ctx) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[d]) {
+  if (!g_err_ptr[d] || g_err_ctx[d] != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_ctl) != cudaSuccess) return nullptr;
     g_err_ptr[d] = static_cast<uint32_t*>(p);
+    g_err_ctx[d] = ctx;
   }
   return g_err_ptr[d];
 }
@@ -120,10 +156,23 @@ int check_prolog(const dsa_prolog_args* a) {
   return DSA_OK;
 }
 
+// The token layout: a map (any T, B >= 1) or the uniform batch T = B * n_q.
+int check_tokens(int T, int B, int n_q, const int32_t* seq) {
+  if (T < 0) return DSA_ERR_INVALID_ARG;
+  if (seq != nullptr) {
+    if (B < 1 || !aligned(seq, 4)) return T == 0 ? DSA_OK : DSA_ERR_INVALID_ARG;
+    return T > 65535 ? DSA_ERR_UNSUPPORTED : DSA_OK;
+  }
+  if (B < 1 || n_q < 1 || static_cast<long long>(B) * n_q != T) return T == 0 ? DSA_OK : DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
 int check_topk(const dsa_topk_args* a) {
   if (!a) return DSA_ERR_INVALID_ARG;
-  if (a->T < 0 || a->B < 1 || a->n_q < 1 || static_cast<long long>(a->B) * a->n_q != a->T)
-    return a->T == 0 ? DSA_OK : DSA_ERR_INVALID_ARG;
+  {
+    const int st = check_tokens(a->T, a->B, a->n_q, a->seq_of_token);
+    if (st != DSA_OK || a->T == 0) return st;
+  }
   if (a->d_I != 64 && a->d_I != 128) return DSA_ERR_UNSUPPORTED;
   switch (a->H_I) {
     case 4: case 8: case 16: case 32: case 64: case 128: break;
@@ -145,8 +194,10 @@ int check_topk(const dsa_topk_args* a) {
 
 int check_attn(const dsa_attn_args* a) {
   if (!a) return DSA_ERR_INVALID_ARG;
-  if (a->T < 0 || a->B < 1 || a->n_q < 1 || static_cast<long long>(a->B) * a->n_q != a->T)
-    return a->T == 0 ? DSA_OK : DSA_ERR_INVALID_ARG;
+  {
+    const int st = check_tokens(a->T, a->B, a->n_q, a->seq_of_token);
+    if (st != DSA_OK || a->T == 0) return st;
+  }
   if (a->d_qk != 576 || a->d_v != 512) return DSA_ERR_UNSUPPORTED;
   if (a->H < 1 || a->topk < 1 || a->topk > 65536 || a->max_L < 1) return DSA_ERR_INVALID_ARG;
   if (!(a->scale > 0.f)) return DSA_ERR_INVALID_ARG;
@@ -188,7 +239,16 @@ const char* dsa_status_string(int status) {
   }
 }
 
-int dsa_abi_version(void) { return 103; }
+int dsa_abi_version(void) { return 104; }
+
+int dsa_set_wait_limit_ns(uint64_t ns) {
+  if (ns > 60000000000ull) return DSA_ERR_INVALID_ARG;
+  const uint64_t v = ns == 0 ? DSA_WAIT_NS : ns;
+  if (!error_word()) return DSA_ERR_CUDA;
+  return cudaMemcpyToSymbol(g_ctl, &v, sizeof(v), offsetof(DeviceControl, wait_limit_ns)) == cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
+}
 
 int dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;

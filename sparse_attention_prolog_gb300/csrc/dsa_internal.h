@@ -13,10 +13,17 @@ namespace dsa {
 // not zero-filled).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadIndex = 2u;
+// Byte offset, from the error word, of the uint64 time limit (ns) of every
+// bounded device wait (set by dsa_set_wait_limit_ns).
+constexpr size_t kWaitLimitOffset = 8;
 
 // Address of the library's device error word on the current device
-// (resolved once per device).  nullptr if CUDA fails.
+// (resolved once per device and context).  nullptr if CUDA fails.
 uint32_t* error_word();
+
+// The calling thread's current CUDA context (a CUcontext), nullptr if none
+// or if the driver entry point is unavailable.
+void* current_context();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -46,6 +53,8 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t s);
 size_t prolog_workspace(const dsa_prolog_args& a);
 
 int launch_indexer(const dsa_topk_args& a, float* scores, uint32_t* hist, cudaStream_t s);
+// Query tokens the indexer scores together against one key tile (a group).
+int indexer_group_tokens(const dsa_topk_args& a);
 
 // Fused top-k path: the indexer also counts each token's scores by their
 // leading 12 key bits; the top-k pass then needs one read of the row.

@@ -9,8 +9,10 @@
 
 namespace dsa {
 
-// Time limit of one bounded mbarrier wait before it gives up and reports a
-// device timeout (nanoseconds of %globaltimer).
+// Default time limit of one bounded mbarrier wait before it gives up and
+// reports a device timeout (nanoseconds of %globaltimer).  The limit in
+// force is a per-device value next to the error word (see wait_limit_ns);
+// DSA_WAIT_NS stays the bound of the drain waits below.
 #ifndef DSA_WAIT_NS
 #define DSA_WAIT_NS 4000000000ull
 #endif
@@ -44,13 +46,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = kSuspendHintNs) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs) : "memory");
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
   return ok != 0;
 }
 // Probe without a suspend hint: ~15 cycles on a completed phase, against
@@ -64,13 +66,25 @@ __device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                      uint32_t hint_ns = kSuspendHintNs) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
       "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs) : "memory");
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
+// The cluster-scope probe without a suspend hint.
+__device__ __forceinline__ bool mbar_probe_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
 
@@ -80,25 +94,52 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait on one phase of an mbarrier.  After DSA_WAIT_NS it records
-// kErrTimeout in *err, raises the CTA abort flag and returns false; once the
-// abort flag is up every later wait returns false at once.
+// The wait limit in force on this device: a uint64 kWaitLimitOffset bytes
+// past the error word (dsa_set_wait_limit_ns writes it between calls).
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* err) {
+  return *reinterpret_cast<const volatile uint64_t*>(reinterpret_cast<const uint8_t*>(err) + kWaitLimitOffset);
+}
+
+// Bounded wait on one phase of an mbarrier.  After the device's wait limit
+// it records kErrTimeout in *err, raises the CTA abort flag and returns
+// false; once the abort flag is up every later wait returns false at once.
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err,
                                                   volatile int* abort_flag) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_probe(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = wait_limit_ns(err);
+  // A limit below the suspend hint spins on the probe and reads the clock
+  // on every pass: a suspended try_wait may sleep until the phase completes.
+  const bool spin = limit < kSuspendHintNs;
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i)
-      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < (spin ? 1 : 4); ++i) {
+      if (spin) {
+        if (kCluster ? mbar_probe_cluster(bar, parity) : mbar_probe(bar, parity)) return true;
+      } else if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) {
+        return true;
+      }
+    }
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > DSA_WAIT_NS) {
+    if (globaltimer_ns() - t0 > limit) {
       atomicOr(err, kErrTimeout);
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+// After a wait gave up: waits for the same phase again, ignoring the abort
+// flag and the device's limit (bounded by DSA_WAIT_NS), so that the bulk
+// copies or tensor-core operations that complete on it have finished before
+// the CTA reuses or releases the memory they write.  Returns true if the
+// phase completed.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > DSA_WAIT_NS) return false;
+  return true;
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           volatile int* abort_flag) {
@@ -227,12 +268,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, in
 __device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar) : "memory");
-}
-// tcgen05.commit that arrives on the mbarrier at the same offset in every
-// CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
 }
 // Copies a 128-row x 256-bit slice of a shared-memory matrix (descriptor)
 // into TMEM lanes 0..127, 8 columns from taddr.

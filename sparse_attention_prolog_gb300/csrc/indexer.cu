@@ -58,7 +58,10 @@ constexpr int kCoef = 256;    // max query rows (N) of a group
 constexpr int kHistBins = 4096;  // leading 12 bits of the score's order key
 
 struct IdxParams {
-  int T, n_q, H_I, d_I, G, N, groups_per_seq, n_groups, n_tiles, max_L;
+  // n_groups: the group count of a uniform batch (seq == null), else the
+  // most groups the token map may form (the size of the group table).
+  int T, B, n_q, H_I, d_I, G, N, groups_per_seq, n_groups, n_tiles, max_L;
+  const int32_t* seq;  // [T] sequence of each token, or null (token t in sequence t / n_q)
   const int8_t* q;
   const __half* q_scale;
   const float* w;
@@ -77,17 +80,29 @@ struct Group {
   int b, t0, ntok, maxpos;
 };
 
+// Group g of a batch given by its token map: tokens [grp[g], grp[g + 1])
+// (a run of adjacent tokens of one sequence, at most G long; built on the
+// device by build_groups).  Of a uniform batch: the G-token slices of each
+// sequence's n_q tokens.
+
 // max(x, 0) of two floats packed into one 64-bit register (fma_f32x2 operand).
 __device__ __forceinline__ uint64_t relu_pair(uint32_t x, uint32_t y) {
   return pack_f32x2(fmaxf(__uint_as_float(x), 0.f), fmaxf(__uint_as_float(y), 0.f));
 }
 
-__device__ __forceinline__ Group group_of(const IdxParams& P, int g) {
+__device__ __forceinline__ Group group_of(const IdxParams& P, const uint16_t* grp, int g) {
   Group G;
-  G.b = g / P.groups_per_seq;
-  const int gj = g % P.groups_per_seq;
-  G.t0 = G.b * P.n_q + gj * P.G;
-  G.ntok = min(P.G, P.n_q - gj * P.G);
+  if (grp != nullptr) {
+    G.t0 = grp[g];
+    G.ntok = grp[g + 1] - G.t0;
+    const int b = __ldg(P.seq + G.t0);
+    G.b = (b >= 0 && b < P.B) ? b : 0;  // out of range: recorded by build_groups
+  } else {
+    G.b = g / P.groups_per_seq;
+    const int gj = g % P.groups_per_seq;
+    G.t0 = G.b * P.n_q + gj * P.G;
+    G.ntok = min(P.G, P.n_q - gj * P.G);
+  }
   int m = -1;
   for (int i = 0; i < G.ntok; ++i) m = max(m, __ldg(P.pos + G.t0 + i));
   G.maxpos = min(m, P.max_L - 1);
@@ -99,14 +114,13 @@ __device__ __forceinline__ Group group_of(const IdxParams& P, int g) {
 // counts and their prefix sum, then walks its own contiguous, equal share of
 // the list, so a decode CTA stays in one group and a prefill CTA gets an
 // equal number of tiles however causal masking thins the groups.
-constexpr int kMaxGroupsScheduled = 4096;
 
 struct Walker {
   int g, j, left;  // current group, tile within the group, items left
 };
 
-__device__ __forceinline__ int group_tiles(const IdxParams& P, int g) {
-  const Group G = group_of(P, g);
+__device__ __forceinline__ int group_tiles(const IdxParams& P, const uint16_t* grp, int g) {
+  const Group G = group_of(P, grp, g);
   return G.maxpos < 0 ? 0 : min(P.n_tiles, G.maxpos / kTileKeys + 1);
 }
 
@@ -121,6 +135,81 @@ __device__ __forceinline__ bool walk_next(const int* tiles_prefix, int n_groups,
     w.j = 0;
   }
   return true;
+}
+
+// Exclusive block-wide scan (sum, or max when kMax) of one value per thread
+// of a kThreads-thread block; `tmp` holds one int per warp.  Every thread
+// must call it; returns the exclusive prefix and sets `total`.
+template <bool kMax, int kNT>
+__device__ __forceinline__ int block_scan_excl(int v, int* tmp, int& total, int identity) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = kMax ? max(incl, n) : incl + n;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  int woff = identity, all = identity;
+  for (int w2 = 0; w2 < kNT / 32; ++w2) {
+    if (w2 < warp) woff = kMax ? max(woff, tmp[w2]) : woff + tmp[w2];
+    all = kMax ? max(all, tmp[w2]) : all + tmp[w2];
+  }
+  __syncthreads();  // tmp may be reused by the next scan
+  const int excl_in_warp = __shfl_up_sync(0xffffffffu, incl, 1);
+  const int excl = lane == 0 ? woff : (kMax ? max(woff, excl_in_warp) : woff + excl_in_warp);
+  total = all;
+  return excl;
+}
+
+// Group table of a batch given by its token map: a group starts at every
+// token whose sequence differs from the previous token's and then every G
+// tokens within such a run.  grp[0..n) receives the first token of each
+// group and grp[n] = T; returns n (the same in every thread).  Out-of-range
+// sequence ids, and more groups than the table holds (the tokens of a
+// sequence not adjacent), are recorded in the error word; groups past the
+// table are dropped.
+template <int kNT>
+__device__ int build_groups(const IdxParams& P, uint16_t* grp, int* tmp) {
+  const int T = P.T;
+  const int per = (T + kNT - 1) / kNT;
+  const int c0 = min(T, static_cast<int>(threadIdx.x) * per), c1 = min(T, c0 + per);
+  int last = -1;
+  bool bad = false;
+  for (int t = c0; t < c1; ++t) {
+    const int b = __ldg(P.seq + t);
+    bad |= (b < 0 || b >= P.B);
+    if (t == 0 || b != __ldg(P.seq + t - 1)) last = t;
+  }
+  if (bad) atomicOr(P.err, kErrBadIndex);
+  int unused;
+  const int rs0 = block_scan_excl<true, kNT>(last, tmp, unused, -1);  // start of the run entering the chunk
+  int rs = rs0, cnt = 0;
+  for (int t = c0; t < c1; ++t) {
+    if (t == 0 || __ldg(P.seq + t) != __ldg(P.seq + t - 1)) rs = t;
+    cnt += ((t - rs) % P.G) == 0;
+  }
+  int n = 0;
+  int off = block_scan_excl<false, kNT>(cnt, tmp, n, 0);
+  rs = rs0;
+  for (int t = c0; t < c1; ++t) {
+    if (t == 0 || __ldg(P.seq + t) != __ldg(P.seq + t - 1)) rs = t;
+    if (((t - rs) % P.G) == 0) {
+      // entry n_groups of a full table is the start of the first dropped
+      // group, so the last kept group still ends where it should
+      if (off <= P.n_groups) grp[off] = static_cast<uint16_t>(t);
+      ++off;
+    }
+  }
+  if (n > P.n_groups) {
+    if (threadIdx.x == 0) atomicOr(P.err, kErrBadIndex);
+    n = P.n_groups;
+  } else if (threadIdx.x == 0) {
+    grp[n] = static_cast<uint16_t>(T);
+  }
+  __syncthreads();
+  return n;
 }
 
 __device__ __forceinline__ int64_t key_row(const IdxParams& P, int b, int s) {
@@ -147,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t tile8_bytes = kTileKeys * DI;     // int8 tile (TMA-swizzled)
   uint8_t* s8 = smem;                                  // [kStages8][tile8]
   uint8_t* sQ = s8 + kStages8 * tile8_bytes;           // [d_I/64 atoms][N rows][128 B]
+  // [n_groups + 1] tile prefix, then (token map only) the group table
+  int* tiles_prefix = reinterpret_cast<int*>(sQ + static_cast<size_t>(N) * DI * 2);
+  uint16_t* grp = P.seq != nullptr ? reinterpret_cast<uint16_t*>(tiles_prefix + P.n_groups + 1) : nullptr;
   __shared__ Bars bars;
   // fp16 key scales of each ring stage, copied with its key tile.
   __shared__ __align__(16) unsigned short ks_s[kStages8][kTileKeys];
@@ -154,7 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   __shared__ __align__(16) float coef[kCoef];
   __shared__ int tok_pos[kMaxG];
-  __shared__ int tiles_prefix[kMaxGroupsScheduled + 1];
   __shared__ int scan_tmp[kThreads / 32];
   // Per-token histogram of each visible score's leading 12 key bits (groups
   // of at most two tokens, H_I >= 64); flushed to global memory at every
@@ -199,13 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base;
   volatile int* abort_v = &abort_flag;
 
-  // Per-group tile counts and their exclusive prefix (block-wide scan).
+  // The group table of a token map (uniform batches need none), then the
+  // per-group tile counts and their exclusive prefix (block-wide scan).
+  const int ngroups = grp != nullptr ? build_groups<kThreads>(P, grp, scan_tmp) : P.n_groups;
   {
-    const int ng = P.n_groups;
+    const int ng = ngroups;
     const int per = (ng + kThreads - 1) / kThreads;
     const int g0 = min(ng, tid * per), g1 = min(ng, g0 + per);
     int local = 0;
-    for (int g = g0; g < g1; ++g) local += group_tiles(P, g);
+    for (int g = g0; g < g1; ++g) local += group_tiles(P, grp, g);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -219,23 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = woff + incl - local;
     for (int g = g0; g < g1; ++g) {
       tiles_prefix[g] = run;
-      run += group_tiles(P, g);
+      run += group_tiles(P, grp, g);
     }
     if (tid == kThreads - 1) tiles_prefix[ng] = run;
     __syncthreads();
   }
-  const int total_items = tiles_prefix[P.n_groups];
+  const int total_items = tiles_prefix[ngroups];
   const int item_lo = static_cast<int>((static_cast<long long>(total_items) * blockIdx.x) / gridDim.x);
   const int item_hi = static_cast<int>((static_cast<long long>(total_items) * (blockIdx.x + 1)) / gridDim.x);
   // First (group, tile) of this CTA's share: binary search in the prefix.
   Walker w0{0, 0, item_hi - item_lo};
   {
-    int lo = 0, hi = P.n_groups;  // largest g with tiles_prefix[g] <= item_lo
+    int lo = 0, hi = ngroups;  // largest g with tiles_prefix[g] <= item_lo
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (tiles_prefix[mid] <= item_lo) lo = mid; else hi = mid;
     }
-    while (lo < P.n_groups && tiles_prefix[lo + 1] <= item_lo) ++lo;
+    while (lo < ngroups && tiles_prefix[lo + 1] <= item_lo) ++lo;
     w0.g = lo;
     w0.j = item_lo - tiles_prefix[lo];
   }
@@ -254,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cur_g = -1, maxpos_cache = -1, b = 0;
       int64_t row0 = 0;
       auto set_group = [&](int g) {
-        const Group G = group_of(P, g);
+        const Group G = group_of(P, grp, g);
         cur_g = g;
         maxpos_cache = G.maxpos;
         b = G.b;
@@ -263,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w0.left > 0) set_group(w0.g);
       griddep_wait();  // the key cache holds rows the previous kernel wrote
       Walker w = w0;
-      for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w)) {
+      for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, ngroups, w)) {
         const int g = w.g, j = w.j;
         if (g != cur_g) set_group(g);
         if (!mbar_wait(&bars.empty8[st], ph ^ 1, P.err, abort_v)) break;
@@ -306,31 +399,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool first_group = true;
     const int chunks = d_I / 16;  // 16-byte int8 chunks per row
     Walker w = w0;
-    for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w)) {
+    for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, ngroups, w)) {
       const int g = w.g;
       if (g != cur_g) {
         cur_g = g;
         if (!first_group && !mbar_wait(&bars.qempty, qph, P.err, abort_v)) break;
         if (!first_group) qph ^= 1;
         first_group = false;
-        const Group G = group_of(P, g);
+        const Group G = group_of(P, grp, g);
         const int rows_real = G.ntok * P.H_I;
-        for (int task = ct; task < N * chunks; task += 128) {
-          const int n = task / chunks, c = task % chunks;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (n < rows_real) {
-            const int8_t* src = P.q + (static_cast<size_t>(G.t0) * P.H_I + n) * d_I + c * 16;
-            v = __ldg(reinterpret_cast<const uint4*>(src));
+        // Eight 16-byte loads in flight per thread before any is used (the
+        // group's q rows were written by the previous kernel: L2 round trips).
+        constexpr int kQBatch = 8;
+        for (int task0 = ct; task0 < N * chunks; task0 += 128 * kQBatch) {
+          uint4 v[kQBatch];
+#pragma unroll
+          for (int u = 0; u < kQBatch; ++u) {
+            const int task = task0 + u * 128;
+            const int n = task / chunks, c = task % chunks;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (task < N * chunks && n < rows_real) {
+              const int8_t* src = P.q + (static_cast<size_t>(G.t0) * P.H_I + n) * d_I + c * 16;
+              v[u] = __ldg(reinterpret_cast<const uint4*>(src));
+            }
           }
-          uint32_t f[8];
-          i8x4_to_f16x4(v.x, f[0], f[1]);
-          i8x4_to_f16x4(v.y, f[2], f[3]);
-          i8x4_to_f16x4(v.z, f[4], f[5]);
-          i8x4_to_f16x4(v.w, f[6], f[7]);
-          uint8_t* atom = sQ + (c / 4) * (N * 128);
-          const int cc = (c % 4) * 2;
-          *reinterpret_cast<uint4*>(atom + sw128_off(n, cc)) = make_uint4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<uint4*>(atom + sw128_off(n, cc + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+          for (int u = 0; u < kQBatch; ++u) {
+            const int task = task0 + u * 128;
+            if (task >= N * chunks) break;
+            const int n = task / chunks, c = task % chunks;
+            uint32_t f[8];
+            i8x4_to_f16x4(v[u].x, f[0], f[1]);
+            i8x4_to_f16x4(v[u].y, f[2], f[3]);
+            i8x4_to_f16x4(v[u].z, f[4], f[5]);
+            i8x4_to_f16x4(v[u].w, f[6], f[7]);
+            uint8_t* atom = sQ + (c / 4) * (N * 128);
+            const int cc = (c % 4) * 2;
+            *reinterpret_cast<uint4*>(atom + sw128_off(n, cc)) = make_uint4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<uint4*>(atom + sw128_off(n, cc + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -386,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Walker w = w0;
       for (bool more = w.left > 0; more;) {
         const int g = w.g;
-        more = walk_next(tiles_prefix, P.n_groups, w);
+        more = walk_next(tiles_prefix, ngroups, w);
         if (g != cur_g) {
           cur_g = g;
           if (!mbar_wait(&bars.qfull, qph, P.err, abort_v)) break;
@@ -457,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g != cur_g) {
         if (do_hist && cur_g >= 0 && !flush_hist()) return false;
         cur_g = g;
-        G = group_of(P, g);
+        G = group_of(P, grp, g);
         if (!ep_sync()) return false;
         for (int n = et; n < kCoef; n += 256) {
           const int gi = n / HI, h = n % HI;
@@ -547,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_wait();  // w and qs come from the previous kernel
     bool aborted = false;
     Walker w = w0;
-    for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, P.n_groups, w))
+    for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, ngroups, w))
       if (!score_item(w)) { aborted = true; break; }
     if (do_hist && cur_g >= 0 && !aborted) flush_hist();
   }
@@ -561,7 +668,11 @@ __global__ void dots_kernel(const IdxParams P, int32_t* dots) {
   const int t = blockIdx.y;
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= P.max_L) return;
-  const int b = t / P.n_q;
+  int b = t / P.n_q;
+  if (P.seq != nullptr) {
+    b = __ldg(P.seq + t);
+    if (b < 0 || b >= P.B) return;
+  }
   const int64_t row = key_row(P, b, s);
   if (row < 0) return;
   const int8_t* k = P.k_cache + row * P.d_I;
@@ -576,12 +687,20 @@ __global__ void dots_kernel(const IdxParams P, int32_t* dots) {
 
 IdxParams make_params(const dsa_topk_args& a, float* scores, int64_t ld, uint32_t* hist) {
   IdxParams P{};
-  P.T = a.T; P.n_q = a.n_q; P.H_I = a.H_I; P.d_I = a.d_I; P.max_L = a.max_L;
-  P.G = a.H_I >= 128 ? 1 : (128 / a.H_I < a.n_q ? 128 / a.H_I : a.n_q);
-  if (P.G > kMaxG) P.G = kMaxG;
+  P.T = a.T; P.B = a.B; P.n_q = a.n_q; P.H_I = a.H_I; P.d_I = a.d_I; P.max_L = a.max_L;
+  P.seq = a.seq_of_token;
+  P.G = indexer_group_tokens(a);
   P.N = static_cast<int>(round_up(static_cast<size_t>(P.G) * a.H_I, 16));
-  P.groups_per_seq = (a.n_q + P.G - 1) / P.G;
-  P.n_groups = a.B * P.groups_per_seq;
+  if (P.seq != nullptr) {
+    // runs of adjacent tokens of one sequence, each cut into G-token groups:
+    // at most ceil(T / G) + B groups when every sequence's tokens are adjacent
+    P.groups_per_seq = 0;
+    const long long ub = (a.T + P.G - 1) / P.G + static_cast<long long>(a.B);
+    P.n_groups = static_cast<int>(ub < a.T ? ub : a.T);
+  } else {
+    P.groups_per_seq = (a.n_q + P.G - 1) / P.G;
+    P.n_groups = a.B * P.groups_per_seq;
+  }
   P.n_tiles = a.max_L / kTileKeys;
   P.q = a.q; P.q_scale = reinterpret_cast<const __half*>(a.q_scale); P.w = a.w;
   P.k_cache = a.k_cache; P.k_scale = reinterpret_cast<const __half*>(a.k_scale);
@@ -591,10 +710,26 @@ IdxParams make_params(const dsa_topk_args& a, float* scores, int64_t ld, uint32_
   return P;
 }
 
+// Dynamic shared memory: alignment slack, the int8 ring, Q, the tile prefix
+// and (token map) the group table.
+size_t indexer_smem(const IdxParams& P, int DI) {
+  size_t n = 1024 + static_cast<size_t>(kStages8) * kTileKeys * DI + static_cast<size_t>(P.N) * DI * 2;
+  n += 4 * static_cast<size_t>(P.n_groups + 1);
+  if (P.seq != nullptr) n += 2 * static_cast<size_t>(P.n_groups + 1);
+  return n;
+}
+
+constexpr size_t kSmemPerBlock = 232448;  // 227 KB opt-in limit of sm_103a
+
 template <int HI, int DI>
-cudaError_t launch_hi(const IdxParams& P, const CUtensorMap& tmap, cudaStream_t s) {
-  const size_t smem = 1024 + static_cast<size_t>(kStages8) * kTileKeys * DI + static_cast<size_t>(P.N) * DI * 2;
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t launch_hi(const IdxParams& P, const CUtensorMap& tmap, cudaStream_t s, bool& too_big) {
+  const size_t smem = indexer_smem(P, DI);
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, indexer_kernel<HI, DI>);
+  if (e != cudaSuccess) return e;
+  too_big = smem + fa.sharedSizeBytes > kSmemPerBlock;
+  if (too_big) return cudaSuccess;
+  e = cudaFuncSetAttribute(indexer_kernel<HI, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(P.n_groups) * P.n_tiles;
   const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
@@ -612,23 +747,30 @@ cudaError_t launch_hi(const IdxParams& P, const CUtensorMap& tmap, cudaStream_t 
 }
 
 template <int DI>
-cudaError_t launch_di(int H_I, const IdxParams& P, const CUtensorMap& tmap, cudaStream_t s) {
+cudaError_t launch_di(int H_I, const IdxParams& P, const CUtensorMap& tmap, cudaStream_t s, bool& too_big) {
   switch (H_I) {
-    case 4: return launch_hi<4, DI>(P, tmap, s);
-    case 8: return launch_hi<8, DI>(P, tmap, s);
-    case 16: return launch_hi<16, DI>(P, tmap, s);
-    case 32: return launch_hi<32, DI>(P, tmap, s);
-    case 64: return launch_hi<64, DI>(P, tmap, s);
-    default: return launch_hi<128, DI>(P, tmap, s);
+    case 4: return launch_hi<4, DI>(P, tmap, s, too_big);
+    case 8: return launch_hi<8, DI>(P, tmap, s, too_big);
+    case 16: return launch_hi<16, DI>(P, tmap, s, too_big);
+    case 32: return launch_hi<32, DI>(P, tmap, s, too_big);
+    case 64: return launch_hi<64, DI>(P, tmap, s, too_big);
+    default: return launch_hi<128, DI>(P, tmap, s, too_big);
   }
 }
 
 }  // namespace
 
+int indexer_group_tokens(const dsa_topk_args& a) {
+  // 128 query rows (tokens x heads) per MMA; a uniform batch never groups
+  // more tokens than one sequence has
+  int G = a.H_I >= 128 ? 1 : 128 / a.H_I;
+  if (a.seq_of_token == nullptr && a.n_q < G) G = a.n_q;
+  return G < kMaxG ? G : kMaxG;
+}
+
 int launch_indexer(const dsa_topk_args& a, float* scores, uint32_t* hist, cudaStream_t s) {
   IdxParams P = make_params(a, scores, a.max_L, hist);
   if (!P.err) return DSA_ERR_CUDA;
-  if (P.n_groups > kMaxGroupsScheduled) return DSA_ERR_UNSUPPORTED;
   if (a.H_I != 4 && a.H_I != 8 && a.H_I != 16 && a.H_I != 32 && a.H_I != 64 && a.H_I != 128)
     return DSA_ERR_UNSUPPORTED;
   // One TMA box is a whole 128-key tile of a contiguous cache, or one page.
@@ -637,7 +779,10 @@ int launch_indexer(const dsa_topk_args& a, float* scores, uint32_t* hist, cudaSt
   alignas(64) CUtensorMap tmap;
   if (!encode_tmap_u8_2d(&tmap, a.k_cache, a.d_I, rows, a.d_I, P.box_rows, a.d_I == 128 ? 128 : 64))
     return DSA_ERR_CUDA;
-  const cudaError_t e = a.d_I == 128 ? launch_di<128>(a.H_I, P, tmap, s) : launch_di<64>(a.H_I, P, tmap, s);
+  bool too_big = false;
+  const cudaError_t e =
+      a.d_I == 128 ? launch_di<128>(a.H_I, P, tmap, s, too_big) : launch_di<64>(a.H_I, P, tmap, s, too_big);
+  if (e == cudaSuccess && too_big) return DSA_ERR_UNSUPPORTED;  // too many token groups
   return cuda_status(e);
 }
 

@@ -27,17 +27,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ctx[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  Resolved on
-// the first call made while that device is current, then cached.
+// the first call made while that device is current, then cached together
+// with the context it was resolved in: when another context is current (the
+// device was reset, or the caller made its own context current) the
+// address is resolved again.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+  void* ctx = current_context();
+  if (ctx == nullptr) return DSA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DSA_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return DSA_OK;
@@ -51,6 +58,9 @@ extern "C" int dsa_indexer_prolog_noalloc(const dsa_prolog_args* a, void* stream
   const size_t need = dsa_indexer_prolog_workspace(a);
   if (a == nullptr || need == 0) return dsa_indexer_prolog(a, nullptr, 0, stream);  // reports the arg error
   if (a->T == 0) return DSA_OK;
+  // Every shape the prolog supports needs at most 33 KB (T <= 32 tokens of
+  // d_I + H_I <= 256 fp32 sums, plus the 256-byte ticket): this check only
+  // guards shapes a later version may add.
   if (need > dsa::kNoAllocScratchBytes) return DSA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int st = dsa::scratch_address(&scratch);

@@ -43,7 +43,7 @@ constexpr int kMaxT = 32;
 constexpr int kMaxRope = 64;     // max d_rope / 2 entries per RoPE row
 
 struct PrologParams {
-  int T, H_I, d_I, d_rope, K_q, D_x, interleaved, n_q_ctas, n_kw_ctas, n_kw_channels, kw_atoms;
+  int T, H_I, d_I, d_rope, K_q, D_x, interleaved, n_q_ctas, n_kw_ctas, n_kw_channels, kw_atoms, rope_max_pos;
   const int8_t* q_lora;
   const __half* q_lora_scale;
   const int8_t* w_qb;
@@ -79,6 +79,7 @@ struct Pre {
   float gamma[128];
   float beta[128];
   int64_t slot[kMaxT];
+  int pos_ok[kMaxT];  // pos[t] lies in [0, rope_max_pos)
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -93,13 +94,23 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // RoPE rows of the tokens (d_rope/2 cos and sin each) into shared memory.
+// A position outside [0, rope_max_pos) reads no table row: the token is
+// marked (its q and key rows are then not written) and the error recorded.
 __device__ __forceinline__ void prefetch_rope(const PrologParams& P, Pre& pre, int tid) {
   const int half = P.d_rope / 2;
+  if (tid < P.T) {
+    const int p = __ldg(P.pos + tid);
+    const bool ok = p >= 0 && p < P.rope_max_pos;
+    pre.pos_ok[tid] = ok;
+    if (!ok && blockIdx.x == 0) atomicOr(P.err, kErrBadIndex);
+  }
   for (int i = tid; i < P.T * half; i += kThreads) {
     const int t = i / half, c = i % half;
-    const size_t off = static_cast<size_t>(__ldg(P.pos + t)) * half + c;
-    pre.cos_t[t][c] = __ldg(P.rope_cos + off);
-    pre.sin_t[t][c] = __ldg(P.rope_sin + off);
+    const int p = __ldg(P.pos + t);
+    const bool ok = p >= 0 && p < P.rope_max_pos;
+    const size_t off = static_cast<size_t>(ok ? p : 0) * half + c;
+    pre.cos_t[t][c] = ok ? __ldg(P.rope_cos + off) : 0.f;
+    pre.sin_t[t][c] = ok ? __ldg(P.rope_sin + off) : 0.f;
   }
 }
 
@@ -237,7 +248,9 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
   if (tid < D) pre.sb[tid] = __half2float(__ldg(P.w_qb_scale + head * D + tid));
   if (tid >= D && tid - D < T) pre.sa[tid - D] = __half2float(__ldg(P.q_lora_scale + (tid - D)));
   prefetch_rope(P, pre, tid);
-  mbar_wait(&bar, 0, P.err, &abort_flag);
+  // a wait that gave up still lets every copy land before the slabs are read
+  // (or the CTA leaves): the copies write this CTA's shared memory
+  if (!mbar_wait(&bar, 0, P.err, &abort_flag)) mbar_drain(&bar, 0);
   __syncthreads();  // zero rows and prefetched tables written by other threads
 
   // int32 partial dots over this CTA's K_q slice.
@@ -271,6 +284,7 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
   // Tokens t = rank (mod kQSplit): sum the pair's partials, then the
   // dequant -> RoPE -> Hadamard -> quant epilogue, one warp per token.
   for (int t = rank + kQSplit * warp; t < T; t += kQSplit * (kThreads / 32)) {
+    if (!pre.pos_ok[t]) continue;  // warp-uniform: the whole warp skips the token
     float v[DPL];
     const float sa = pre.sa[t];
     uint32_t pv[kQSplit][DPL];
@@ -353,7 +367,8 @@ __device__ void kw_stream(const PrologParams& P, const CUtensorMap* tm_wk, const
   prefetch_rope(P, pre, tid);
 
   if (tid == 0) {
-    if (mbar_wait(&bar, 0, P.err, &abort_flag)) {
+    const bool loaded = mbar_wait(&bar, 0, P.err, &abort_flag);
+    if (loaded) {
       tc_fence_after();
       const uint32_t idesc = idesc_f16(128, NX, kFmtBF16, 0, 0);
       for (int a = 0; a < nb; ++a) {
@@ -369,11 +384,16 @@ __device__ void kw_stream(const PrologParams& P, const CUtensorMap* tm_wk, const
       }
     }
     mma_commit(&mdone);
+    if (!loaded) mbar_drain(&bar, 0);  // the tiles land before the CTA leaves
   }
   if (warp < 4) {
     // Row r of D0 / D1 (TMEM lane r) is channel r / d_I + r; column t is token t.
-    // a CTA whose weight tiles never arrived adds nothing (its error is recorded)
-    const bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag) && !*static_cast<volatile int*>(&abort_flag);
+    // a CTA whose weight tiles never arrived adds nothing (its error is
+    // recorded); a wait on the MMAs that gave up still lets them finish
+    // before the tensor memory is read or released
+    bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag);
+    if (!ok) mbar_drain(&mdone, 0);
+    ok = ok && !*static_cast<volatile int*>(&abort_flag);
     tc_fence_after();
     const int r = warp * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -406,6 +426,7 @@ __device__ void kw_stream(const PrologParams& P, const CUtensorMap* tm_wk, const
 
   // Last CTA: LayerNorm -> RoPE -> Hadamard -> quant for every token's key.
   for (int t = warp; t < T; t += kThreads / 32) {
+    if (!pre.pos_ok[t]) continue;  // warp-uniform
     float v[DPL];
     float s = 0.f;
 #pragma unroll
@@ -476,12 +497,27 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   P.n_q_ctas = a.H_I * kQSplit;
   P.n_kw_channels = a.d_I + (a.w_proj ? a.H_I : 0);
   // The k / weight CTAs split D_x into 64-column atoms, as few per CTA as
-  // the SMs left over by the q stream allow (at most kKwMaxAtoms).
+  // the SMs left over by the q stream allow (at most kKwMaxAtoms, and at
+  // most what fits in shared memory beside the kernel's static tables).
+  const int tm = a.T <= 8 ? 8 : (a.T <= 16 ? 16 : 32);
+  const int nx = tm < 16 ? 16 : tm;  // MMA N: tokens padded with zero rows
+  const void* kern = a.d_I == 128 ? (tm == 8 ? (const void*)prolog_kernel<4, 8>
+                                             : tm == 16 ? (const void*)prolog_kernel<4, 16>
+                                                        : (const void*)prolog_kernel<4, 32>)
+                                  : (tm == 8 ? (const void*)prolog_kernel<2, 8>
+                                             : tm == 16 ? (const void*)prolog_kernel<2, 16>
+                                                        : (const void*)prolog_kernel<2, 32>);
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return DSA_ERR_CUDA;
+  constexpr size_t kSmemPerBlock = 232448;  // 227 KB opt-in limit of sm_103a
+  const size_t per_atom = 2 * kKwAtom + static_cast<size_t>(nx) * 128;
+  const int fit_atoms = static_cast<int>((kSmemPerBlock - fa.sharedSizeBytes - 1024) / per_atom);
   const int atoms = a.D_x / 64;
   const int spare = sm_count() - P.n_q_ctas;
   const int want = spare >= 8 ? spare : 8;
   P.kw_atoms = (atoms + want - 1) / want;
   if (P.kw_atoms > kKwMaxAtoms) P.kw_atoms = kKwMaxAtoms;
+  if (P.kw_atoms > fit_atoms) P.kw_atoms = fit_atoms;
   P.n_kw_ctas = (atoms + P.kw_atoms - 1) / P.kw_atoms;
   P.q_lora = a.q_lora; P.q_lora_scale = reinterpret_cast<const __half*>(a.q_lora_scale);
   P.w_qb = a.w_qb; P.w_qb_scale = reinterpret_cast<const __half*>(a.w_qb_scale);
@@ -489,7 +525,7 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   P.w_k = reinterpret_cast<const __nv_bfloat16*>(a.w_k);
   P.ln_gamma = a.ln_gamma; P.ln_beta = a.ln_beta; P.ln_eps = a.ln_eps;
   P.w_proj = reinterpret_cast<const __nv_bfloat16*>(a.w_proj); P.w_scale = a.w_scale;
-  P.pos = a.pos; P.rope_cos = a.rope_cos; P.rope_sin = a.rope_sin;
+  P.pos = a.pos; P.rope_cos = a.rope_cos; P.rope_sin = a.rope_sin; P.rope_max_pos = a.rope_max_pos;
   P.q_out = a.q_out; P.q_scale_out = reinterpret_cast<__half*>(a.q_scale_out);
   P.k_cache = a.k_cache; P.k_scale_cache = reinterpret_cast<__half*>(a.k_scale_cache);
   P.slot = a.slot; P.cache_rows = a.cache_rows; P.w_out = a.w_out;
@@ -501,8 +537,6 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   const int kchunk = a.K_q / kQSplit;
   const size_t smem_q = static_cast<size_t>(a.d_I) * (kchunk + 16) + static_cast<size_t>(kMaxT) * kchunk +
                         static_cast<size_t>(kMaxT) * a.d_I * 4;
-  const int tm = a.T <= 8 ? 8 : (a.T <= 16 ? 16 : 32);
-  const int nx = tm < 16 ? 16 : tm;  // MMA N: tokens padded with zero rows
   const size_t smem_kw = 1024 + static_cast<size_t>(P.kw_atoms) * (2 * kKwAtom + nx * 128);
   const size_t smem = smem_q > smem_kw ? smem_q : smem_kw;
   // bf16 tiles of 64 columns x rows; rows past the tensor (channels past

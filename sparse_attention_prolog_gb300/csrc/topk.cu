@@ -627,8 +627,7 @@ cudaError_t launch_cs(const TopkParams& P, int T, cudaStream_t s) {
 bool topk_hist_eligible(const dsa_topk_args& a) {
   // groups of at most two tokens (the indexer's histogram); a row fits one
   // cluster of at most 8 CTAs with 16 keys per thread
-  const int G = a.H_I >= 128 ? 1 : (128 / a.H_I < a.n_q ? 128 / a.H_I : a.n_q);
-  return G <= 2 && a.H_I >= 64 && a.T <= 512 && a.max_L <= kThreads * 16 * 8;
+  return indexer_group_tokens(a) <= 2 && a.H_I >= 64 && a.T <= 512 && a.max_L <= kThreads * 16 * 8;
 }
 
 size_t topk_hist_workspace(const dsa_topk_args& a) {

@@ -92,13 +92,21 @@ class MlaBuffers:
         B.dsa_mla_prolog(self.args, self.ws, stream)
 
 
+def is_uniform(inp) -> bool:
+    """True if token t of the batch belongs to sequence t // n_q, n_q = T / B."""
+    if inp.T % inp.B:
+        return False
+    return bool(np.array_equal(inp.seq_of_token, np.repeat(np.arange(inp.B, dtype=np.int32), inp.T // inp.B)))
+
+
 class DecodeBuffers:
     """Device copies of a workloads.DecodeInputs and the indexer/attention
     outputs.  ``q_idx``/``q_idx_scale``/``w_idx`` may be replaced by the
-    prolog's outputs (then pass them in)."""
+    prolog's outputs (then pass them in).  The calls get the token map
+    (seq_of_token) when the batch is not uniform, or when ``seq_map``."""
 
     def __init__(self, inp, device, q_idx=None, q_idx_scale=None, w_idx=None, k_cache=None, k_scale=None,
-                 with_attention=True, keep_scores=False):
+                 with_attention=True, keep_scores=False, seq_map=False):
         self.inp = inp
         d = device
         self.q_idx = q_idx if q_idx is not None else to_dev(inp.q_idx, d)
@@ -109,11 +117,13 @@ class DecodeBuffers:
         self.block_table = None if inp.block_table is None else to_dev(inp.block_table, d)
         self.pos = to_dev(inp.pos, d)
         T = inp.T
+        self.seq = to_dev(inp.seq_of_token.astype(np.int32), d) if (seq_map or not is_uniform(inp)) else None
+        n_q = max(T // inp.B, 1)
         self.topk_idx = torch.full((T, inp.topk), -7, dtype=torch.int32, device=d)
         self.scores = torch.empty(T, inp.max_L, dtype=torch.float32, device=d) if keep_scores else None
-        self.targs = B.topk_args(T, inp.B, T // inp.B, inp.H_I, inp.d_I, inp.topk, inp.max_L, self.q_idx,
+        self.targs = B.topk_args(T, inp.B, n_q, inp.H_I, inp.d_I, inp.topk, inp.max_L, self.q_idx,
                                  self.q_idx_scale, self.w_idx, self.k_cache, self.k_scale, self.pos, self.topk_idx,
-                                 self.block_table, inp.block_size, self.scores)
+                                 self.block_table, inp.block_size, self.scores, seq_of_token=self.seq)
         self.tws = torch.zeros(max(B.workspace_bytes("topk", self.targs), 256), dtype=torch.uint8, device=d)
         self.with_attention = with_attention
         if with_attention:
@@ -121,8 +131,9 @@ class DecodeBuffers:
             self.kv = to_dev(inp.kv_cache, d, "bf16")
             self.out = torch.zeros(T, inp.H, inp.d_v, dtype=torch.bfloat16, device=d)
             self.lse = torch.zeros(T, inp.H, dtype=torch.float32, device=d)
-            self.aargs = B.attn_args(T, inp.B, T // inp.B, inp.H, inp.topk, inp.max_L, inp.scale, self.q_attn,
-                                     self.kv, self.topk_idx, self.out, self.lse, self.block_table, inp.block_size)
+            self.aargs = B.attn_args(T, inp.B, n_q, inp.H, inp.topk, inp.max_L, inp.scale, self.q_attn,
+                                     self.kv, self.topk_idx, self.out, self.lse, self.block_table, inp.block_size,
+                                     seq_of_token=self.seq)
             self.aws = torch.zeros(max(B.workspace_bytes("attn", self.aargs), 256), dtype=torch.uint8, device=d)
 
     def run_topk(self, stream=None):

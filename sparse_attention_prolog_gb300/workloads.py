@@ -213,16 +213,19 @@ class DecodeInputs:
 def make_decode_inputs(B, n_q, seq_lens, H_I, d_I, topk, H, seed, max_L=None,
                        w_sigma=None, block_size=0, d_qk=576, d_v=512,
                        with_attention=True) -> DecodeInputs:
-    """Uniform-n_q decode/prefill batch.  Token t = b*n_q + j sits at
-    position seq_len[b] - n_q + j (so a prefill of S tokens uses n_q = S)."""
+    """Decode/prefill batch.  n_q is the query-token count of every sequence
+    (an int) or of each sequence (a list, e.g. mixed MTP depths); token j of
+    sequence b sits at position seq_len[b] - n_q[b] + j (so a prefill of S
+    tokens uses n_q = S), and the tokens of a sequence are adjacent."""
     rng = _rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
-    assert seq_lens.shape == (B,) and (seq_lens >= n_q).all()
-    T = B * n_q
+    counts = np.full(B, n_q, dtype=np.int64) if np.isscalar(n_q) else np.asarray(n_q, dtype=np.int64)
+    assert seq_lens.shape == (B,) and counts.shape == (B,) and (counts >= 1).all() and (seq_lens >= counts).all()
+    T = int(counts.sum())
     if max_L is None:
         max_L = int(seq_lens.max())
-    seq_of_token = np.repeat(np.arange(B, dtype=np.int32), n_q)
-    pos = (np.repeat(seq_lens, n_q) - n_q + np.tile(np.arange(n_q), B)).astype(np.int32)
+    seq_of_token = np.repeat(np.arange(B, dtype=np.int32), counts)
+    pos = np.concatenate([np.arange(int(L) - int(c), int(L)) for L, c in zip(seq_lens, counts)]).astype(np.int32)
     if w_sigma is None:
         w_sigma = 1.0 / math.sqrt(H_I)
     block_table = None

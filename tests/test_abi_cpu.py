@@ -69,7 +69,7 @@ def test_status_strings(lib):
     from sparse_attention_prolog_gb300 import binding as B
     assert B.status_string(0) == "ok"
     assert "workspace" in B.status_string(3)
-    assert lib.dsa_abi_version() == 103
+    assert lib.dsa_abi_version() == 104
     assert "timed out" in B.status_string(5)
     assert "device-side data" in B.status_string(6)
     assert B.status_string(7) == "unknown status"
@@ -107,6 +107,16 @@ def test_host_validation_rejects_before_launch(lib):
     t.k_scale = base + 4 * 4096 + 2
     assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) == 0            # k_scale must be 16-byte aligned
     assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 1
+    # a per-token sequence map lifts T == B * n_q (n_q is then ignored)
+    t.k_scale = base + 4 * 4096
+    t.T, t.n_q = 7, 3
+    assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) == 0            # no map: 7 != 4 * 3
+    t.seq_of_token = base + 9 * 4096
+    assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) > 0             # with a map: valid
+    t.seq_of_token = base + 9 * 4096 + 2
+    assert lib.dsa_indexer_topk_workspace(ctypes.byref(t)) == 0            # map not 4-byte aligned
+    t.seq_of_token, t.T = base + 9 * 4096, 65536
+    assert lib.dsa_indexer_topk(ctypes.byref(t), null, 0, null) == 2        # a map covers < 65536 tokens
     at = B.AttnArgs()
     at.T, at.B, at.n_q, at.H, at.d_qk, at.d_v, at.topk, at.max_L, at.scale = 8, 4, 2, 128, 512, 512, 2048, 65536, 0.07
     assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 2        # d_qk 512
@@ -114,6 +124,15 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 1        # null tensors
     at.T = 0
     assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) == 0
+    for i, f in enumerate(("q", "kv", "topk_idx", "out")):
+        setattr(at, f, base + i * 4096)
+    at.T, at.n_q = 7, 5
+    assert lib.dsa_sparse_attn_workspace(ctypes.byref(at)) == 0             # no map: 7 != 4 * 5
+    at.seq_of_token = base + 9 * 4096
+    # past the argument checks: what follows needs a GPU (workspace or CUDA status here)
+    assert lib.dsa_sparse_attn(ctypes.byref(at), null, 0, null) in (0, 3, 4)
+    at.seq_of_token = 0
+    assert lib.dsa_indexer_prolog_noalloc(None, null) == 1                 # the no-allocation entry: null args
     assert lib.dsa_act_quant(None, null) == 1
     aq = B.ActQuantArgs(4, 100, 1 << 20, 1 << 21, 1 << 22, 0)
     assert lib.dsa_act_quant(ctypes.byref(aq), null) == 2                  # N % 8
@@ -154,6 +173,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_mla_prolog(ctypes.byref(m), ws, need, null) == 1         # q not 16-byte aligned
     m.T = 0
     assert lib.dsa_mla_prolog(ctypes.byref(m), null, 0, null) == 0          # empty: no-op
+    assert lib.dsa_set_wait_limit_ns(61 * 10 ** 9) == 1                     # wait limit beyond 60 s
 
 
 def test_missing_library_fails_loudly(tmp_path):

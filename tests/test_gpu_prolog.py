@@ -75,6 +75,17 @@ def test_prolog_128_heads_two_waves(d_I, cuda_lib):
     _run_and_check(p, cuda_lib)
 
 
+@pytest.mark.parametrize("H_I,d_I", [(64, 128), (128, 64)])
+def test_prolog_largest_supported_shape(H_I, d_I, cuda_lib):
+    """T = 32 tokens, K_q = 2048, D_x = 12288 (every bound of the header at
+    once): the k / weight CTAs take as many D_x atoms as fit beside the
+    kernel's static tables, so more of them run than there are spare SMs."""
+    T = 32
+    p = W.make_prolog_inputs(T=T, pos=np.arange(T) * 61, slot=np.arange(T) * 2, seed=93, H_I=H_I, d_I=d_I,
+                             K_q=2048, D_x=12288, max_pos=2048)
+    _run_and_check(p, cuda_lib, cache_rows=2 * T)
+
+
 def test_prolog_repeated_calls_share_the_workspace(cuda_lib):
     """The k / weight sums accumulate in the workspace and the call leaves
     it zeroed: three calls on one workspace give the same checked result."""
