@@ -283,6 +283,114 @@ def stage_times_separate(stage_fns_per_set, stream, prep, reps):
     return out, "one graph per stage, replayed alone (same L2 policy as the timed steps)"
 
 
+def time_replays(graphs, K, stream, prep, dev):
+    """Mean ms of K replays of graphs[k % len(graphs)] (CUDA events on the
+    launching stream around each replay, a barrier and a synchronize on both
+    sides of the timed region), and the clocks of a loaded window around it:
+    untimed replays of the same graphs run just before and after the timed
+    ones, so that the 20 ms clock poll sees the region however short it is."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for w in range(2 * len(graphs)):
+            graphs[w % len(graphs)].replay()
+        b.record(stream)
+    stream.synchronize()
+    est_ms = max(a.elapsed_time(b) / (2 * len(graphs)), 1e-3)
+    soak_pre, soak_post = int(150.0 / est_ms) + 1, int(60.0 / est_ms) + 1
+
+    def soak(n):
+        with torch.cuda.stream(stream):
+            for w in range(n):
+                prep()
+                graphs[w % len(graphs)].replay()
+
+    with ClockSampler(device_uuid(dev)) as clk:
+        soak(soak_pre)
+        D.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                prep()
+                starts[k].record(stream)
+                graphs[k % len(graphs)].replay()
+                ends[k].record(stream)
+        torch.cuda.synchronize()
+        D.barrier()
+        soak(soak_post)
+        torch.cuda.synchronize()
+    ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+    clocks = clk.summary()
+    clocks["window"] = (f"the {K} timed steps with {soak_pre} untimed replays of the same step graphs before "
+                        f"and {soak_post} after them (one loaded window, sampled every {ClockSampler.PERIOD_MS} ms)")
+    return ms, clocks
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        fn(stream)
+    return g
+
+
+def pipelined_e2e(dev, stream, io, n, prep=lambda: None):
+    """End to end through the C ABI, as a serving loop overlaps it.  io[k] =
+    (copy_in, step, read_out) of input set k: copy_in(s) copies a step's
+    inputs from pinned host memory into set k, step(s) issues the C calls on
+    set k, read_out(s) copies the result into pinned host memory.  Step j
+    uses set j % S; its inputs are copied on a copy stream while step j-1
+    runs, its result is read back on a third stream while step j+1 runs, and
+    the copy into a set waits for the read-back of the step that used it
+    last.  Returns seconds per step over n steps (host wall clock from the
+    first copy to the last read-back), or None if the copies or calls cannot
+    be captured as graphs."""
+    S = len(io)
+    cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    try:
+        copy_graphs = [capture(c, cs_in) for c, _, _ in io]
+        step_graphs = [capture(st, stream) for _, st, _ in io]
+    except RuntimeError:
+        return None
+
+    def run(m):
+        copied = [torch.cuda.Event() for _ in range(m)]
+        computed = [torch.cuda.Event() for _ in range(m)]
+        done = [torch.cuda.Event() for _ in range(m)]
+        with torch.cuda.stream(stream):
+            prep()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(cs_in):
+            copy_graphs[0].replay()
+            copied[0].record(cs_in)
+        for k in range(m):
+            if k + 1 < m:
+                with torch.cuda.stream(cs_in):
+                    if k + 1 - S >= 0:
+                        cs_in.wait_event(done[k + 1 - S])
+                    copy_graphs[(k + 1) % S].replay()
+                    copied[k + 1].record(cs_in)
+            with torch.cuda.stream(stream):
+                stream.wait_event(copied[k])
+                step_graphs[k % S].replay()
+                computed[k].record(stream)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(computed[k])
+                io[k % S][2](cs_out)
+                done[k].record(cs_out)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / m
+
+    run(2 * S)  # warm-up
+    return run(n)
+
+
+def nbytes(*tensors) -> int:
+    return int(sum(t.numel() * t.element_size() for t in tensors))
+
+
 def run_ours(args, rank, world, local):
     from sparse_attention_prolog_gb300 import binding as B
     from sparse_attention_prolog_gb300.pipeline import DecodeBuffers, PrologBuffers
@@ -337,48 +445,10 @@ def run_ours(args, rank, world, local):
     stream.synchronize()
 
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    # The clock poll (every 20 ms) needs a loaded window longer than a short
-    # timed region: untimed replays of the same step graphs run just before
-    # and after the timed steps, inside the sampler's window.
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        for w in range(2 * len(graphs)):
-            graphs[w % len(graphs)].replay()
-        b.record(stream)
-    stream.synchronize()
-    est_ms = max(a.elapsed_time(b) / (2 * len(graphs)), 1e-3)
-    soak_pre, soak_post = int(150.0 / est_ms) + 1, int(60.0 / est_ms) + 1
-
-    def soak(n):
-        with torch.cuda.stream(stream):
-            for w in range(n):
-                prep()
-                graphs[w % len(graphs)].replay()
-
-    with ClockSampler(device_uuid(dev)) as clk:
-        soak(soak_pre)
-        D.barrier()
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            for k in range(K):
-                prep()
-                starts[k].record(stream)
-                graphs[k % len(graphs)].replay()
-                ends[k].record(stream)
-        torch.cuda.synchronize()
-        D.barrier()
-        soak(soak_post)
-        torch.cuda.synchronize()
-    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms, clocks = time_replays(graphs, K, stream, prep, dev)
     ms_max = D.max_over_ranks(ms, dev)
     tokens_total = D.sum_over_ranks(inp.T, dev)
     value = tokens_total / (ms_max / 1e3)
-    clocks = clk.summary()
-    clocks["window"] = (f"the {K} timed steps with {soak_pre} untimed replays of the same step graphs before "
-                        f"and {soak_post} after them (one loaded window, sampled every {ClockSampler.PERIOD_MS} ms)")
 
     # Per-stage times inside the step: a second copy of the step graph with
     # event nodes at the boundaries of the three C calls (event nodes split
@@ -455,65 +525,28 @@ def run_ours(args, rank, world, local):
     e2e_eager_s = time_e2e(False)
     e2e_serial_s = time_e2e(True) if e2e_graphs else e2e_eager_s
 
-    # As a serving loop overlaps them: step k+1's inputs are copied from
-    # pinned memory into its input set on a copy stream while step k runs,
-    # and step k's output is read back on a third stream while step k+1
-    # runs.  The set of step k+1 was last used by step k+1-S (S sets), so
-    # its copy waits for that step's read-back.  Every copy of every step is
-    # inside the timed region.
+    # As a serving loop overlaps them (see pipelined_e2e): step k+1's inputs
+    # are copied while step k runs, step k's output is read back while step
+    # k+1 runs; every copy of every step is inside the timed region.
     S = len(sets)
-    cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     outs_host = [torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory() for _ in range(S)]
-    copy_graphs, step_graphs = [], []
-    try:
-        for k in range(S):
-            pr, bu = sets[k]
-            dst = dev_inputs(pr, bu)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cs_in, capture_error_mode="relaxed"):
-                for name in names:
-                    dst[name].copy_(pinned[name], non_blocking=True)
-            copy_graphs.append(g)
-            g2 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g2, stream=stream, capture_error_mode="relaxed"):
-                steps[k](stream)
-            step_graphs.append(g2)
-    except RuntimeError:
-        copy_graphs, step_graphs = [], []
 
-    def time_e2e_pipelined(n):
-        copied = [torch.cuda.Event() for _ in range(n)]
-        computed = [torch.cuda.Event() for _ in range(n)]
-        done = [torch.cuda.Event() for _ in range(n)]
-        with torch.cuda.stream(stream):
-            prep()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        with torch.cuda.stream(cs_in):
-            copy_graphs[0].replay()
-            copied[0].record(cs_in)
-        for k in range(n):
-            if k + 1 < n:
-                with torch.cuda.stream(cs_in):
-                    if k + 1 - S >= 0:
-                        cs_in.wait_event(done[k + 1 - S])
-                    copy_graphs[(k + 1) % S].replay()
-                    copied[k + 1].record(cs_in)
-            with torch.cuda.stream(stream):
-                stream.wait_event(copied[k])
-                step_graphs[k % S].replay()
-                computed[k].record(stream)
-            with torch.cuda.stream(cs_out):
-                cs_out.wait_event(computed[k])
-                outs_host[k % S].copy_(sets[k % S][1].out, non_blocking=True)
-                done[k].record(cs_out)
-        torch.cuda.synchronize()
-        return (time.perf_counter() - t0) / n
+    def io_of(k):
+        pr, bu = sets[k]
+        dst = dev_inputs(pr, bu)
 
-    if step_graphs:
-        n_pipe = max(min(K, 2000), 8 * S)
-        time_e2e_pipelined(4 * S)  # warm-up
-        e2e_s = D.max_over_ranks(time_e2e_pipelined(n_pipe), dev)
+        def copy_in(s_):
+            for name in names:
+                dst[name].copy_(pinned[name], non_blocking=True)
+
+        def read_out(s_):
+            outs_host[k].copy_(bu.out, non_blocking=True)
+        return copy_in, steps[k], read_out
+
+    n_pipe = max(min(K, 2000), 8 * S)
+    e2e_s = pipelined_e2e(dev, stream, [io_of(k) for k in range(S)], n_pipe, prep)
+    if e2e_s is not None:
+        e2e_s = D.max_over_ranks(e2e_s, dev)
         e2e_launch = (f"pipelined over {n_pipe} consecutive steps: per step one CUDA graph of the 7 host-to-device "
                       "copies from pinned memory (copy stream, into the step's rotated input set), one graph of "
                       "the three C calls (compute stream) and the device-to-host read of the attention output "
@@ -559,6 +592,304 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, p, budget_s=args.cpu_budget)
     return result
+
+
+# ------------------------------------------------- the other three workloads
+def measured_tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s) and its kind: the sustained cuBLAS
+    figure (the prefill kernels run for milliseconds inside a long step); f16
+    operands run at the bf16 rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured sustained bf16 dense (cuBLAS)"
+        return float(d["bf16_tflops"]), "measured burst bf16 dense (cuBLAS)"
+    return 1700.0, "fallback sustained bf16 dense"
+
+
+def prolog_config(args, dev, K):
+    """The Indexer Prolog alone: T=8 tokens at positions 0..7, no weight
+    stream (14.6 MB per call).  Twelve input sets (175 MB) rotate, so no call
+    finds its weights in L2."""
+    from sparse_attention_prolog_gb300 import binding as B
+    from sparse_attention_prolog_gb300.pipeline import PrologBuffers
+    p = W.prolog_alone()
+    S = 12
+    sets = [PrologBuffers(p, dev) for _ in range(S)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for pr in sets:
+                pr.run(stream)
+    stream.synchronize()
+    if B.device_error() != 0:
+        raise RuntimeError("device-side error in the prolog warm-up")
+    graphs = [capture(pr.run, stream) for pr in sets]
+    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    peak, peak_kind = measured_peaks()
+    alg = prolog_bytes(p)
+    achieved = alg / (ms / 1e3) / 1e9
+    names = ["q_lora", "q_lora_scale", "x", "pos", "slot"]
+    pinned = {n: getattr(sets[0], n).detach().cpu().pin_memory() for n in names}
+    rows = int(p.slot.max()) + 1
+    outs = [(torch.empty(sets[0].q_out.shape, dtype=torch.int8).pin_memory(),
+             torch.empty(sets[0].q_scale_out.shape, dtype=torch.float16).pin_memory(),
+             torch.empty((rows, p.d_I), dtype=torch.int8).pin_memory(),
+             torch.empty((rows,), dtype=torch.float16).pin_memory()) for _ in range(S)]
+
+    def io_of(k):
+        pr = sets[k]
+
+        def copy_in(s_):
+            for n in names:
+                getattr(pr, n).copy_(pinned[n], non_blocking=True)
+
+        def read_out(s_):
+            o = outs[k]
+            o[0].copy_(pr.q_out, non_blocking=True)
+            o[1].copy_(pr.q_scale_out, non_blocking=True)
+            o[2].copy_(pr.k_cache[:rows], non_blocking=True)
+            o[3].copy_(pr.k_scale_cache[:rows], non_blocking=True)
+        return copy_in, pr.run, read_out
+
+    n_pipe = max(min(K, 2000), 8 * S)
+    e2e_s = pipelined_e2e(dev, stream, [io_of(k) for k in range(S)], n_pipe)
+    res = {
+        "metric": "prolog query-tok/s (Indexer Prolog alone, T=8); % roofline", "value": round(p.T / (ms / 1e3), 1),
+        "unit": "query-tok/s", "n_gpus": 1, "steps": K, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "dtype": "int8 q GEMM (dp4a), bf16 k GEMM (tcgen05), fp32 epilogue", "data": "synthetic (seeded)",
+        "config": {"workload": "Indexer Prolog alone: T=8, positions 0..7, H_I=64 d_I=128, K_q=1536, D_x=7168, "
+                               "no weight stream", "l2": f"{S} rotating input sets ({S * alg / 1e6:.0f} MB), no flush"},
+        "roofline": {"bound": "hbm", "kernel": "prolog_kernel", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes": alg,
+                     "traffic": profiled_traffic([("prolog.cu", "prolog_alone_T8.txt")])},
+        "gpu_launches": K, "clocks": clocks,
+    }
+    if e2e_s is not None:
+        res["e2e"] = {"value": round(p.T / e2e_s, 1), "unit": "query-tok/s",
+                      "h2d_bytes_per_step": nbytes(*pinned.values()), "d2h_bytes_per_step": nbytes(*outs[0]),
+                      "ms_per_step": round(e2e_s * 1e3, 4),
+                      "launch": f"pipelined over {n_pipe} calls (copy stream, compute stream, read-back stream)"}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 3.0:
+            O.indexer_prolog(p)
+            reps += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(reps * p.T / el, 3), "unit": "query-tok/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": f"{reps} full calls of the same workload, numpy float64"}
+    return res
+
+
+def prefill_config(args, dev, K):
+    """Causal prefill: B=1, S=8192 query tokens over 8192 keys, top-2048
+    among s <= t, 128 attention heads; the indexer and the attention are
+    tensor-core bound, so the roofline is the dense tensor peak.  Its
+    queries (1.2 GB) and outputs (1.1 GB) exceed L2: one input set."""
+    from sparse_attention_prolog_gb300 import binding as B
+    from sparse_attention_prolog_gb300.pipeline import DecodeBuffers
+    inp = W.causal_prefill()
+    buf = DecodeBuffers(inp, dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            buf.run(stream)
+    stream.synchronize()
+    if B.device_error() != 0:
+        raise RuntimeError("device-side error in the prefill warm-up")
+    graphs = [capture(buf.run, stream)]
+    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    st_ms, stage_timing = stage_times_in_graph([[("indexer+topk", buf.run_topk), ("attention", buf.run_attn)]],
+                                               stream, lambda: None, max(K, 3))
+    if st_ms is None:
+        st_ms, stage_timing = stage_times_separate([[("indexer+topk", buf.run_topk), ("attention", buf.run_attn)]],
+                                                   stream, lambda: None, max(K, 3))
+    n_vis = np.minimum(inp.pos.astype(np.int64) + 1, inp.max_L)
+    idx_ops = float(n_vis.sum()) * inp.H_I * inp.d_I * 2
+    att_flop = float(np.minimum(n_vis, inp.topk).sum()) * inp.H * (inp.d_qk + inp.d_v) * 2
+    peak, peak_kind = measured_tensor_peak()
+    stage = {"indexer+topk": idx_ops / (st_ms["indexer+topk"] / 1e3) / 1e12,
+             "attention": att_flop / (st_ms["attention"] / 1e3) / 1e12}
+    dom = max(st_ms, key=lambda k: st_ms[k])
+    step_tf = (idx_ops + att_flop) / (ms / 1e3) / 1e12
+    names = ["q_idx", "q_idx_scale", "w_idx", "pos", "q_attn"]
+    pinned = {n: getattr(buf, n).detach().cpu().pin_memory() for n in names}
+    out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+
+    def copy_in(s_):
+        for n in names:
+            getattr(buf, n).copy_(pinned[n], non_blocking=True)
+
+    def read_out(s_):
+        out_host.copy_(buf.out, non_blocking=True)
+
+    n_pipe = max(min(K, 10), 3)
+    e2e_s = pipelined_e2e(dev, stream, [(copy_in, buf.run, read_out)], n_pipe)
+    res = {
+        "metric": "prefill query-tok/s (indexer+topk+sparse attn), B=1 S=8192 causal top-2048; % tensor roofline",
+        "value": round(inp.T / (ms / 1e3), 1), "unit": "query-tok/s", "n_gpus": 1, "steps": K,
+        "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "dtype": "int8 indexer (exact f16 MMA), bf16 attention, fp32 accumulate", "data": "synthetic (seeded)",
+        "config": {"workload": "causal prefill B=1, S=8192 query tokens over KV 8192, H_I=64 d_I=128 int8, top-2048 "
+                               "(rows t<2048 keep t+1), sparse MLA attention 128 heads d_qk=576 d_v=512 bf16",
+                   "l2": "inputs larger than L2 (1.3 GB of queries per step), one set, no flush"},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(stage[dom], 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(stage[dom] / peak, 4), "peak_kind": peak_kind,
+                     "algorithmic_flops": idx_ops if dom == "indexer+topk" else att_flop,
+                     "traffic": None},
+        "stage_roofline": {k: {"achieved_tflops": round(v, 1), "frac": round(v / peak, 4)} for k, v in stage.items()},
+        "step_roofline": {"algorithmic_flops": idx_ops + att_flop, "achieved_tflops": round(step_tf, 1),
+                          "frac": round(step_tf / peak, 4)},
+        "stages_ms": {k: round(v, 4) for k, v in st_ms.items()}, "stages_timing": stage_timing,
+        "gpu_launches": 3 * K, "clocks": clocks,
+    }
+    if e2e_s is not None:
+        res["e2e"] = {"value": round(inp.T / e2e_s, 1), "unit": "query-tok/s",
+                      "h2d_bytes_per_step": nbytes(*pinned.values()), "d2h_bytes_per_step": nbytes(out_host),
+                      "ms_per_step": round(e2e_s * 1e3, 4),
+                      "launch": f"pipelined over {n_pipe} steps on one input set (the next step's copy waits for "
+                                "the previous read-back)"}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        rng = np.random.default_rng(4)
+        sample = np.sort(rng.choice(inp.T, size=256, replace=False))
+        t0 = time.perf_counter()
+        idx = np.full((inp.T, inp.topk), -1, np.int64)
+        for t in sample:
+            n = int(inp.pos[t]) + 1
+            rows = O.logical_rows(inp, 0, n)
+            sc = O.indexer_scores_token(inp.q_idx[t], inp.q_idx_scale[t], inp.w_idx[t], inp.k_cache[rows],
+                                        inp.k_scale[rows], n - 1)
+            idx[t] = O.topk_indices(sc, n, inp.topk)
+        t_idx = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        O.sparse_attention(inp, idx, list(sample))
+        t_att = time.perf_counter() - t0
+        # per-row work: the indexer grows with the visible keys, the attention
+        # with the selected rows
+        est = t_idx * n_vis.sum() / n_vis[sample].sum() + \
+            t_att * np.minimum(n_vis, inp.topk).sum() / np.minimum(n_vis[sample], inp.topk).sum()
+        res["cpu_baseline"] = {"value": round(inp.T / est, 4), "unit": "query-tok/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": f"{len(sample)} random rows of the 8192 (indexer, top-k and "
+                               "attention), extrapolated to all rows by their visible keys and selected rows",
+                               "extrapolated": True, "seconds": round(t_idx + t_att, 2)}
+    return res
+
+
+def ragged_config(args, dev, K):
+    """Long-context ragged decode: B=32 sequences of L ~ U[4096, 131072]
+    keys, one query token each, both caches paged in 64-token blocks through
+    a shuffled block table; the step is the prolog of the 32 tokens (new keys
+    at each sequence's last position) + indexer/top-k + attention.  Its
+    caches (2.8 GB) exceed L2: one input set."""
+    from sparse_attention_prolog_gb300 import binding as B
+    from sparse_attention_prolog_gb300.pipeline import DecodeBuffers, PrologBuffers
+    inp = W.ragged_paged_decode()
+    last = inp.seq_len.astype(np.int64) - 1
+    slot = inp.block_table[np.arange(inp.B), last // inp.block_size].astype(np.int64) * inp.block_size + \
+        last % inp.block_size
+    p = W.make_prolog_inputs(T=inp.T, pos=inp.pos, slot=slot, seed=2005, max_pos=inp.max_L)
+    kc = torch.from_numpy(inp.k_cache).to(dev)
+    ks = torch.from_numpy(inp.k_scale).to(dev)
+    pro = PrologBuffers(p, dev, kc, ks)
+    buf = DecodeBuffers(inp, dev, q_idx=pro.q_out, q_idx_scale=pro.q_scale_out, w_idx=pro.w_out, k_cache=kc,
+                        k_scale=ks, keep_scores=True)
+
+    def step(s_):
+        pro.run(s_)
+        buf.run(s_)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step(stream)
+    stream.synchronize()
+    if B.device_error() != 0:
+        raise RuntimeError("device-side error in the ragged warm-up")
+    graphs = [capture(step, stream)]
+    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    fns = [[("prolog", pro.run), ("indexer+topk", buf.run_topk), ("attention+combine", buf.run_attn)]]
+    st_ms, stage_timing = stage_times_in_graph(fns, stream, lambda: None, min(max(K, 5), 50))
+    if st_ms is None:
+        st_ms, stage_timing = stage_times_separate(fns, stream, lambda: None, min(max(K, 5), 50))
+    idx = buf.topk_idx.cpu().numpy()
+    alg = {"prolog": prolog_bytes(p), "indexer+topk": indexer_bytes(inp) + topk_bytes(inp),
+           "attention+combine": attention_bytes(inp, idx)}
+    dom = max(alg, key=lambda k: st_ms[k])
+    peak, peak_kind = measured_peaks()
+    achieved = alg[dom] / (st_ms[dom] / 1e3) / 1e9
+    step_bytes = sum(alg.values())
+    names = ["q_lora", "q_lora_scale", "x", "pos", "slot"]
+    pinned = {n: getattr(pro, n).detach().cpu().pin_memory() for n in names}
+    pinned["pos_idx"] = buf.pos.detach().cpu().pin_memory()
+    pinned["q_attn"] = buf.q_attn.detach().cpu().pin_memory()
+    out_host = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+
+    def copy_in(s_):
+        for n in names:
+            getattr(pro, n).copy_(pinned[n], non_blocking=True)
+        buf.pos.copy_(pinned["pos_idx"], non_blocking=True)
+        buf.q_attn.copy_(pinned["q_attn"], non_blocking=True)
+
+    def read_out(s_):
+        out_host.copy_(buf.out, non_blocking=True)
+
+    n_pipe = max(min(K, 200), 8)
+    e2e_s = pipelined_e2e(dev, stream, [(copy_in, step, read_out)], n_pipe)
+    res = {
+        "metric": "ragged decode query-tok/s (prolog+indexer+topk+sparse attn), B=32 paged L~U[4K,128K]; % roofline",
+        "value": round(inp.T / (ms / 1e3), 1), "unit": "query-tok/s", "n_gpus": 1, "steps": K,
+        "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "dtype": "int8 indexer (exact f16 MMA), bf16 attention, fp32 accumulate", "data": "synthetic (seeded)",
+        "config": {"workload": "ragged paged decode B=32 x 1 token, KV lengths ~ U[4096, 131072] (seeded, "
+                               f"sum {int(inp.seq_len.sum())}), 64-token blocks, shuffled block table; H_I=64 d_I=128 "
+                               "int8, top-2048; sparse MLA attention 128 heads; prolog T=32",
+                   "l2": f"inputs larger than L2 ({(inp.k_cache.nbytes + inp.kv_cache.nbytes) / 1e9:.1f} GB of caches), "
+                         "one set, no flush"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes": alg[dom], "traffic": None},
+        "step_roofline": {"algorithmic_bytes": step_bytes, "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
+                          "frac": round(step_bytes / (peak * 1e9) / (ms / 1e3), 4)},
+        "stages_ms": {k: round(v, 5) for k, v in st_ms.items()}, "stages_timing": stage_timing,
+        "gpu_launches": 5 * K, "clocks": clocks,
+    }
+    if e2e_s is not None:
+        res["e2e"] = {"value": round(inp.T / e2e_s, 1), "unit": "query-tok/s",
+                      "h2d_bytes_per_step": nbytes(*pinned.values()), "d2h_bytes_per_step": nbytes(out_host),
+                      "ms_per_step": round(e2e_s * 1e3, 4),
+                      "launch": f"pipelined over {n_pipe} steps on one input set (the next step's copy waits for "
+                                "the previous read-back)"}
+    if not args.no_cpu_baseline:
+        import oracle as O
+        picks = list(range(0, inp.B, 2))
+        t0 = time.perf_counter()
+        pr = O.indexer_prolog(p)
+        t_pro = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        idx_h = np.full((inp.T, inp.topk), -1, np.int64)
+        for t in picks:
+            n = int(inp.pos[t]) + 1
+            rows = O.logical_rows(inp, t, n)
+            sc = O.indexer_scores_token(pr["q"][t], pr["q_scale"][t], pr["w"][t], inp.k_cache[rows],
+                                        inp.k_scale[rows], n - 1)
+            idx_h[t] = O.topk_indices(sc, n, inp.topk)
+        O.sparse_attention(inp, idx_h, picks)
+        t_rest = time.perf_counter() - t0
+        lens = inp.seq_len.astype(np.float64)
+        est = t_pro + t_rest * lens.sum() / lens[picks].sum()
+        res["cpu_baseline"] = {"value": round(inp.T / est, 4), "unit": "query-tok/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": f"the prolog of all 32 tokens, then indexer, top-k and "
+                               f"attention of {len(picks)} of the 32 sequences, extrapolated by their key counts",
+                               "extrapolated": True, "seconds": round(t_pro + t_rest, 2)}
+    return res
+
+
+EXTRA_CONFIGS = {"prolog": prolog_config, "prefill": prefill_config, "ragged": ragged_config}
 
 
 # ---------------------------------------------------------------- oracle
@@ -858,6 +1189,12 @@ def main():
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
+    ap.add_argument("--config", choices=["decode", "prolog", "prefill", "ragged"], default="decode",
+                    help="the workload of the step: the headline decode (default; its line also carries the other "
+                         "three under 'configs'), the Indexer Prolog alone, the causal prefill, the ragged paged "
+                         "decode")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="do not add the prolog, prefill and ragged lines to the decode line")
     ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm", "mhc", "mla_prolog"], default="step",
                     help="the decode step (default), or a standalone export: the activation quantiser, the int8 "
                          "GEMM, the mHC mappings, the MLA Prolog")
@@ -869,6 +1206,16 @@ def main():
                "mla_prolog": run_mla}[args.op]
         print(json.dumps(run(args)), flush=True)
         return
+    extra_steps = {"prolog": 500, "prefill": 10, "ragged": 100}
+    if args.config != "decode":
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        D.init()
+        res = EXTRA_CONFIGS[args.config](args, dev, max(min(args.steps, extra_steps[args.config]), 3))
+        res["warmup"] = args.warmup
+        print(json.dumps(res), flush=True)
+        D.shutdown()
+        return
     rank, world, local = D.init()
     if args.impl == "reference":
         if rank == 0:
@@ -876,6 +1223,18 @@ def main():
         D.shutdown()
         return
     res = run_ours(args, rank, world, local)
+    if world == 1 and not args.no_extra_configs:
+        # the other three workloads, one line each inside the headline line
+        dev = torch.device("cuda", local)
+        res["configs"] = {}
+        for name, fn in EXTRA_CONFIGS.items():
+            torch.cuda.empty_cache()
+            try:
+                r = fn(args, dev, max(min(args.steps, extra_steps[name]), 3))
+                r["warmup"] = args.warmup
+                res["configs"][name] = r
+            except Exception as e:  # a failed extra line must not hide the headline
+                res["configs"][name] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(res), flush=True)
     D.barrier()
