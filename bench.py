@@ -674,15 +674,20 @@ def prolog_config(args, dev, K):
                       "ms_per_step": round(e2e_s * 1e3, 4),
                       "launch": f"pipelined over {n_pipe} calls (copy stream, compute stream, read-back stream)"}
     if not args.no_cpu_baseline:
-        import oracle as O
-        reps, t0 = 0, time.perf_counter()
-        while time.perf_counter() - t0 < 3.0:
-            O.indexer_prolog(p)
-            reps += 1
-        el = time.perf_counter() - t0
-        res["cpu_baseline"] = {"value": round(reps * p.T / el, 3), "unit": "query-tok/s", "cores": os.cpu_count(),
-                               "kind": "oracle", "sample": f"{reps} full calls of the same workload, numpy float64"}
+        res["cpu_baseline"] = prolog_cpu_baseline(p)
     return res
+
+
+def prolog_cpu_baseline(p):
+    """The oracle's Indexer Prolog on the same inputs, repeated for ~3 s."""
+    import oracle as O
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < 3.0:
+        O.indexer_prolog(p)
+        reps += 1
+    el = time.perf_counter() - t0
+    return {"value": round(reps * p.T / el, 3), "unit": "query-tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} full calls of the same workload, numpy float64"}
 
 
 def prefill_config(args, dev, K):
@@ -754,30 +759,35 @@ def prefill_config(args, dev, K):
                       "launch": f"pipelined over {n_pipe} steps on one input set (the next step's copy waits for "
                                 "the previous read-back)"}
     if not args.no_cpu_baseline:
-        import oracle as O
-        rng = np.random.default_rng(4)
-        sample = np.sort(rng.choice(inp.T, size=256, replace=False))
-        t0 = time.perf_counter()
-        idx = np.full((inp.T, inp.topk), -1, np.int64)
-        for t in sample:
-            n = int(inp.pos[t]) + 1
-            rows = O.logical_rows(inp, 0, n)
-            sc = O.indexer_scores_token(inp.q_idx[t], inp.q_idx_scale[t], inp.w_idx[t], inp.k_cache[rows],
-                                        inp.k_scale[rows], n - 1)
-            idx[t] = O.topk_indices(sc, n, inp.topk)
-        t_idx = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        O.sparse_attention(inp, idx, list(sample))
-        t_att = time.perf_counter() - t0
-        # per-row work: the indexer grows with the visible keys, the attention
-        # with the selected rows
-        est = t_idx * n_vis.sum() / n_vis[sample].sum() + \
-            t_att * np.minimum(n_vis, inp.topk).sum() / np.minimum(n_vis[sample], inp.topk).sum()
-        res["cpu_baseline"] = {"value": round(inp.T / est, 4), "unit": "query-tok/s", "cores": os.cpu_count(),
-                               "kind": "oracle", "sample": f"{len(sample)} random rows of the 8192 (indexer, top-k and "
-                               "attention), extrapolated to all rows by their visible keys and selected rows",
-                               "extrapolated": True, "seconds": round(t_idx + t_att, 2)}
+        res["cpu_baseline"] = prefill_cpu_baseline(inp, n_vis)
     return res
+
+
+def prefill_cpu_baseline(inp, n_vis):
+    """The oracle on 256 random rows of the prefill (indexer, top-k and
+    attention), extrapolated to all 8192 rows: the indexer part by the
+    rows' visible keys, the attention part by their selected rows."""
+    import oracle as O
+    rng = np.random.default_rng(4)
+    sample = np.sort(rng.choice(inp.T, size=256, replace=False))
+    t0 = time.perf_counter()
+    idx = np.full((inp.T, inp.topk), -1, np.int64)
+    for t in sample:
+        n = int(inp.pos[t]) + 1
+        rows = O.logical_rows(inp, 0, n)
+        sc = O.indexer_scores_token(inp.q_idx[t], inp.q_idx_scale[t], inp.w_idx[t], inp.k_cache[rows],
+                                    inp.k_scale[rows], n - 1)
+        idx[t] = O.topk_indices(sc, n, inp.topk)
+    t_idx = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    O.sparse_attention(inp, idx, list(sample))
+    t_att = time.perf_counter() - t0
+    est = t_idx * n_vis.sum() / n_vis[sample].sum() + \
+        t_att * np.minimum(n_vis, inp.topk).sum() / np.minimum(n_vis[sample], inp.topk).sum()
+    return {"value": round(inp.T / est, 4), "unit": "query-tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(sample)} random rows of the 8192 (indexer, top-k and attention), extrapolated to all "
+                      "rows by their visible keys and selected rows",
+            "extrapolated": True, "seconds": round(t_idx + t_att, 2)}
 
 
 def ragged_config(args, dev, K):
@@ -865,28 +875,34 @@ def ragged_config(args, dev, K):
                       "launch": f"pipelined over {n_pipe} steps on one input set (the next step's copy waits for "
                                 "the previous read-back)"}
     if not args.no_cpu_baseline:
-        import oracle as O
-        picks = list(range(0, inp.B, 2))
-        t0 = time.perf_counter()
-        pr = O.indexer_prolog(p)
-        t_pro = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        idx_h = np.full((inp.T, inp.topk), -1, np.int64)
-        for t in picks:
-            n = int(inp.pos[t]) + 1
-            rows = O.logical_rows(inp, t, n)
-            sc = O.indexer_scores_token(pr["q"][t], pr["q_scale"][t], pr["w"][t], inp.k_cache[rows],
-                                        inp.k_scale[rows], n - 1)
-            idx_h[t] = O.topk_indices(sc, n, inp.topk)
-        O.sparse_attention(inp, idx_h, picks)
-        t_rest = time.perf_counter() - t0
-        lens = inp.seq_len.astype(np.float64)
-        est = t_pro + t_rest * lens.sum() / lens[picks].sum()
-        res["cpu_baseline"] = {"value": round(inp.T / est, 4), "unit": "query-tok/s", "cores": os.cpu_count(),
-                               "kind": "oracle", "sample": f"the prolog of all 32 tokens, then indexer, top-k and "
-                               f"attention of {len(picks)} of the 32 sequences, extrapolated by their key counts",
-                               "extrapolated": True, "seconds": round(t_pro + t_rest, 2)}
+        res["cpu_baseline"] = ragged_cpu_baseline(inp, p)
     return res
+
+
+def ragged_cpu_baseline(inp, p):
+    """The oracle's prolog of all 32 tokens, then indexer, top-k and
+    attention of every other sequence, extrapolated by the key counts."""
+    import oracle as O
+    picks = list(range(0, inp.B, 2))
+    t0 = time.perf_counter()
+    pr = O.indexer_prolog(p)
+    t_pro = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    idx_h = np.full((inp.T, inp.topk), -1, np.int64)
+    for t in picks:
+        n = int(inp.pos[t]) + 1
+        rows = O.logical_rows(inp, t, n)
+        sc = O.indexer_scores_token(pr["q"][t], pr["q_scale"][t], pr["w"][t], inp.k_cache[rows],
+                                    inp.k_scale[rows], n - 1)
+        idx_h[t] = O.topk_indices(sc, n, inp.topk)
+    O.sparse_attention(inp, idx_h, picks)
+    t_rest = time.perf_counter() - t0
+    lens = inp.seq_len.astype(np.float64)
+    est = t_pro + t_rest * lens.sum() / lens[picks].sum()
+    return {"value": round(inp.T / est, 4), "unit": "query-tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"the prolog of all 32 tokens, then indexer, top-k and attention of {len(picks)} of the 32 "
+                      "sequences, extrapolated by their key counts",
+            "extrapolated": True, "seconds": round(t_pro + t_rest, 2)}
 
 
 EXTRA_CONFIGS = {"prolog": prolog_config, "prefill": prefill_config, "ragged": ragged_config}
