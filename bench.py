@@ -23,6 +23,7 @@ bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -905,7 +906,138 @@ def ragged_cpu_baseline(inp, p):
             "extrapolated": True, "seconds": round(t_pro + t_rest, 2)}
 
 
-EXTRA_CONFIGS = {"prolog": prolog_config, "prefill": prefill_config, "ragged": ragged_config}
+def mla_bytes(mp) -> int:
+    """Algorithmic HBM bytes of one MLA Prolog call: its weights (w_dq, w_dkv,
+    w_uq + scales, w_uk, gammas) read once, x read, q_lora, q and the latent
+    rows written."""
+    T, H, K_q, D_x = mp.T, mp.H, mp.K_q, mp.D_x
+    weights = K_q * D_x * 2 + 576 * D_x * 2 + H * 192 * K_q + H * 192 * 2 + H * 128 * 512 * 2 + (K_q + 512) * 4
+    return int(weights + T * D_x * 2 + T * K_q + T * 2 + T * H * 576 * 2 + T * 576 * 2)
+
+
+def dia_config(args, dev, K):
+    """One decode step of DeepSeek Indexer Attention at B=4, MTP1, 64K:
+    MLA Prolog -> Indexer Prolog -> Lightning Indexer + top-k -> sparse
+    attention, the attention's query and latent rows coming from the MLA
+    Prolog.  Four input sets (caches and weights, 1.8 GB) rotate."""
+    from sparse_attention_prolog_gb300 import binding as B
+    from sparse_attention_prolog_gb300.pipeline import DiaBuffers
+    dia = W.dia_decode()
+    S = 4
+    sets = [DiaBuffers(dia, dev) for _ in range(S)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for st in sets:
+                st.run(stream)
+    stream.synchronize()
+    if B.device_error() != 0:
+        raise RuntimeError("device-side error in the DIA warm-up")
+    graphs = [capture(st.run, stream) for st in sets]
+    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    fns = [[("mla_prolog", st.mla.run), ("indexer_prolog", st.pro.run), ("indexer+topk", st.buf.run_topk),
+            ("attention+combine", st.buf.run_attn)] for st in sets]
+    reps = min(max(K, 5), 50)
+    st_ms, stage_timing = stage_times_in_graph(fns, stream, lambda: None, reps)
+    if st_ms is None:
+        st_ms, stage_timing = stage_times_separate(fns, stream, lambda: None, reps)
+    inp = dia.decode
+    idx = sets[0].buf.topk_idx.cpu().numpy()
+    alg = {"mla_prolog": mla_bytes(dia.mla), "indexer_prolog": prolog_bytes(dia.prolog),
+           "indexer+topk": indexer_bytes(inp) + topk_bytes(inp), "attention+combine": attention_bytes(inp, idx)}
+    peak, peak_kind = measured_peaks()
+    dom = max(alg, key=lambda k: st_ms[k])
+    achieved = alg[dom] / (st_ms[dom] / 1e3) / 1e9
+    step_bytes = sum(alg.values())
+
+    def dev_inputs(st):
+        return {"x": st.mla.x, "pos_mla": st.mla.pos, "slot_mla": st.mla.slot, "pos_prolog": st.pro.pos,
+                "slot_prolog": st.pro.slot, "pos": st.buf.pos}
+
+    pinned = {k: v.detach().cpu().pin_memory() for k, v in dev_inputs(sets[0]).items()}
+    outs = [torch.empty(sets[0].buf.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(S)]
+
+    def io_of(k):
+        st = sets[k]
+        dst = dev_inputs(st)
+
+        def copy_in(s_):
+            for n, t in dst.items():
+                t.copy_(pinned[n], non_blocking=True)
+
+        def read_out(s_):
+            outs[k].copy_(st.buf.out, non_blocking=True)
+        return copy_in, st.run, read_out
+
+    n_pipe = max(min(K, 2000), 8 * S)
+    e2e_s = pipelined_e2e(dev, stream, [io_of(k) for k in range(S)], n_pipe)
+    res = {
+        "metric": "DIA decode query-tok/s (MLA prolog+indexer prolog+indexer+topk+sparse attn), B=4 MTP1 64K; "
+                  "% roofline",
+        "value": round(inp.T / (ms / 1e3), 1), "unit": "query-tok/s", "n_gpus": 1, "steps": K,
+        "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "dtype": "bf16 / int8 prologs, int8 indexer (exact f16 MMA), bf16 attention, fp32 accumulate",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "DIA decode B=4 x MTP1 (T=8), KV 65536 per sequence: MLA Prolog (H=128, K_q=1536, "
+                               "D_x=7168) -> Indexer Prolog (its q_lora and x) -> indexer H_I=64 d_I=128 int8, "
+                               "top-2048 -> sparse MLA attention over the latent cache with the new rows",
+                   "l2": f"{S} rotating input sets ({S * 0.44:.1f} GB), no flush"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes": alg[dom], "traffic": None},
+        "step_roofline": {"algorithmic_bytes": step_bytes, "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
+                          "frac": round(step_bytes / (peak * 1e9) / (ms / 1e3), 4)},
+        "stages_ms": {k: round(v, 5) for k, v in st_ms.items()}, "stages_timing": stage_timing,
+        "gpu_launches": 8 * K, "clocks": clocks,
+    }
+    if e2e_s is not None:
+        res["e2e"] = {"value": round(inp.T / e2e_s, 1), "unit": "query-tok/s",
+                      "h2d_bytes_per_step": nbytes(*pinned.values()), "d2h_bytes_per_step": nbytes(outs[0]),
+                      "ms_per_step": round(e2e_s * 1e3, 4),
+                      "launch": f"pipelined over {n_pipe} steps (copy stream, compute stream, read-back stream)"}
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = dia_cpu_baseline(dia)
+    return res
+
+
+def dia_cpu_baseline(dia):
+    """The oracle's whole DIA step (MLA Prolog, Indexer Prolog on its
+    q_lora, indexer, top-k and attention of all 8 tokens with its query and
+    latent rows), repeated for ~5 s."""
+    import oracle as O
+    inp, mp, pp = dia.decode, dia.mla, dia.prolog
+
+    def one():
+        m = O.mla_prolog(mp)
+        p2 = dataclasses.replace(pp, q_lora=m["q_lora"], q_lora_scale=m["q_lora_scale"])
+        pr = O.indexer_prolog(p2)
+        kc_rows = {int(s): (pr["k"][i], pr["k_scale"][i]) for i, s in enumerate(pp.slot)}
+        idx = np.full((inp.T, inp.topk), -1, np.int64)
+        for t in range(inp.T):
+            b, n = int(inp.seq_of_token[t]), int(inp.pos[t]) + 1
+            rows = O.logical_rows(inp, b, n)
+            keys, ks = inp.k_cache[rows].copy(), inp.k_scale[rows].copy()
+            for j, r in enumerate(rows[-2:]):
+                if int(r) in kc_rows:
+                    keys[n - 2 + j], ks[n - 2 + j] = kc_rows[int(r)]
+            sc = O.indexer_scores_token(pr["q"][t], pr["q_scale"][t], pr["w"][t], keys, ks, n - 1)
+            idx[t] = O.topk_indices(sc, n, inp.topk)
+        q_bits = W.f32_to_bf16_bits(m["q"].astype(np.float32))
+        kv = inp.kv_cache.copy()
+        kv[mp.slot] = W.f32_to_bf16_bits(m["kv"].astype(np.float32))
+        O.sparse_attention(dataclasses.replace(inp, q_attn=q_bits, kv_cache=kv), idx)
+
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < 5.0 and reps < 50:
+        one()
+        reps += 1
+    el = time.perf_counter() - t0
+    return {"value": round(reps * inp.T / el, 4), "unit": "query-tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} full DIA step(s) of the same workload (8 query tokens each), numpy float64",
+            "seconds": round(el, 2)}
+
+
+EXTRA_CONFIGS = {"prolog": prolog_config, "prefill": prefill_config, "ragged": ragged_config, "dia": dia_config}
 
 
 # ---------------------------------------------------------------- oracle
@@ -1205,7 +1337,7 @@ def main():
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="keep each step's inputs out of L2 by rotating input copies, or by flushing")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated with --l2 rotate")
-    ap.add_argument("--config", choices=["decode", "prolog", "prefill", "ragged"], default="decode",
+    ap.add_argument("--config", choices=["decode", "prolog", "prefill", "ragged", "dia"], default="decode",
                     help="the workload of the step: the headline decode (default; its line also carries the other "
                          "three under 'configs'), the Indexer Prolog alone, the causal prefill, the ragged paged "
                          "decode")
@@ -1222,7 +1354,7 @@ def main():
                "mla_prolog": run_mla}[args.op]
         print(json.dumps(run(args)), flush=True)
         return
-    extra_steps = {"prolog": 500, "prefill": 10, "ragged": 100}
+    extra_steps = {"prolog": 500, "prefill": 10, "ragged": 100, "dia": 500}
     if args.config != "decode":
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)

@@ -24,16 +24,19 @@ def to_dev(a: np.ndarray, device, kind: str = None) -> torch.Tensor:
 
 
 class PrologBuffers:
-    """Device copies of a workloads.PrologInputs plus its outputs."""
+    """Device copies of a workloads.PrologInputs plus its outputs.  q_lora,
+    q_lora_scale and x may be given as device tensors (another kernel's
+    outputs or inputs, e.g. the MLA Prolog's)."""
 
-    def __init__(self, p, device, k_cache: torch.Tensor = None, k_scale_cache: torch.Tensor = None):
+    def __init__(self, p, device, k_cache: torch.Tensor = None, k_scale_cache: torch.Tensor = None,
+                 q_lora: torch.Tensor = None, q_lora_scale: torch.Tensor = None, x: torch.Tensor = None):
         self.p = p
         d = device
-        self.q_lora = to_dev(p.q_lora, d)
-        self.q_lora_scale = to_dev(p.q_lora_scale, d)
+        self.q_lora = to_dev(p.q_lora, d) if q_lora is None else q_lora
+        self.q_lora_scale = to_dev(p.q_lora_scale, d) if q_lora_scale is None else q_lora_scale
         self.w_qb = to_dev(p.w_qb, d)
         self.w_qb_scale = to_dev(p.w_qb_scale, d)
-        self.x = to_dev(p.x, d, "bf16")
+        self.x = to_dev(p.x, d, "bf16") if x is None else x
         self.w_k = to_dev(p.w_k, d, "bf16")
         self.ln_gamma = to_dev(p.ln_gamma, d)
         self.ln_beta = to_dev(p.ln_beta, d)
@@ -64,7 +67,7 @@ class MlaBuffers:
     """Device copies of a workloads.MlaInputs plus the MLA Prolog's outputs
     (q_lora, q_lora_scale, q) and a latent cache of ``cache_rows`` rows."""
 
-    def __init__(self, p, device, cache_rows: int, kv_fill: float = 0.0):
+    def __init__(self, p, device, cache_rows: int, kv_fill: float = 0.0, kv_cache: torch.Tensor = None):
         self.p = p
         d = device
         self.x = to_dev(p.x, d, "bf16")
@@ -82,7 +85,8 @@ class MlaBuffers:
         self.q_lora = torch.zeros(p.T, p.K_q, dtype=torch.int8, device=d)
         self.q_lora_scale = torch.zeros(p.T, dtype=torch.float16, device=d)
         self.q = torch.zeros(p.T, p.H, 576, dtype=torch.bfloat16, device=d)
-        self.kv_cache = torch.full((cache_rows, 576), kv_fill, dtype=torch.bfloat16, device=d)
+        self.kv_cache = (torch.full((cache_rows, 576), kv_fill, dtype=torch.bfloat16, device=d) if kv_cache is None
+                         else kv_cache)
         self.args = B.mla_args(self.x, self.w_dq, self.gamma_q, self.w_dkv, self.gamma_kv, p.rms_eps, self.w_uq,
                                self.w_uq_scale, self.w_uk, self.pos, self.rope_cos, self.rope_sin,
                                p.rope_interleaved, self.q_lora, self.q_lora_scale, self.q, self.kv_cache, self.slot)
@@ -106,7 +110,7 @@ class DecodeBuffers:
     (seq_of_token) when the batch is not uniform, or when ``seq_map``."""
 
     def __init__(self, inp, device, q_idx=None, q_idx_scale=None, w_idx=None, k_cache=None, k_scale=None,
-                 with_attention=True, keep_scores=False, seq_map=False):
+                 with_attention=True, keep_scores=False, seq_map=False, q_attn=None, kv=None):
         self.inp = inp
         d = device
         self.q_idx = q_idx if q_idx is not None else to_dev(inp.q_idx, d)
@@ -127,8 +131,8 @@ class DecodeBuffers:
         self.tws = torch.zeros(max(B.workspace_bytes("topk", self.targs), 256), dtype=torch.uint8, device=d)
         self.with_attention = with_attention
         if with_attention:
-            self.q_attn = to_dev(inp.q_attn, d, "bf16")
-            self.kv = to_dev(inp.kv_cache, d, "bf16")
+            self.q_attn = to_dev(inp.q_attn, d, "bf16") if q_attn is None else q_attn
+            self.kv = to_dev(inp.kv_cache, d, "bf16") if kv is None else kv
             self.out = torch.zeros(T, inp.H, inp.d_v, dtype=torch.bfloat16, device=d)
             self.lse = torch.zeros(T, inp.H, dtype=torch.float32, device=d)
             self.aargs = B.attn_args(T, inp.B, n_q, inp.H, inp.topk, inp.max_L, inp.scale, self.q_attn,
@@ -146,3 +150,31 @@ class DecodeBuffers:
         self.run_topk(stream)
         if self.with_attention:
             self.run_attn(stream)
+
+
+class DiaBuffers:
+    """One decode step of DeepSeek Indexer Attention on the device: the MLA
+    Prolog (query latent q_lora, attention query q, latent KV rows into the
+    latent cache) -> the Indexer Prolog (fed the MLA Prolog's q_lora and the
+    same hidden states x; new keys into the key cache) -> Lightning Indexer
+    + top-k -> sparse attention (the MLA Prolog's q over the latent cache).
+    `dia` is a workloads.DiaInputs."""
+
+    def __init__(self, dia, device, keep_scores=False):
+        d = device
+        inp = dia.decode
+        self.dia = dia
+        self.k_cache = to_dev(inp.k_cache, d)
+        self.k_scale = to_dev(inp.k_scale, d)
+        self.kv = to_dev(inp.kv_cache, d, "bf16")
+        self.mla = MlaBuffers(dia.mla, d, self.kv.shape[0], kv_cache=self.kv)
+        self.pro = PrologBuffers(dia.prolog, d, self.k_cache, self.k_scale, q_lora=self.mla.q_lora,
+                                 q_lora_scale=self.mla.q_lora_scale, x=self.mla.x)
+        self.buf = DecodeBuffers(inp, d, q_idx=self.pro.q_out, q_idx_scale=self.pro.q_scale_out, w_idx=self.pro.w_out,
+                                 k_cache=self.k_cache, k_scale=self.k_scale, keep_scores=keep_scores,
+                                 q_attn=self.mla.q, kv=self.kv)
+
+    def run(self, stream=None):
+        self.mla.run(stream)
+        self.pro.run(stream)
+        self.buf.run(stream)

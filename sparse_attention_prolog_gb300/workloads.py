@@ -307,3 +307,33 @@ def ragged_paged_decode(seed=1005, B=32, lo=4096, hi=131072, block_size=64,
     return make_decode_inputs(B=B, n_q=1, seq_lens=lens, H_I=64, d_I=128, topk=2048,
                               H=128, seed=seed, w_sigma=1.0 / 8.0, block_size=block_size,
                               max_L=hi, with_attention=with_attention)
+
+
+# ----------------------------------------------------------------------------
+# One decode step of DeepSeek Indexer Attention (MLA Prolog + Indexer Prolog
+# + Lightning Indexer + sparse attention)
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class DiaInputs:
+    """The decode batch and the two prologs' inputs of one DIA step.  The
+    Indexer Prolog takes the MLA Prolog's hidden states x (prolog.x is
+    mla.x) and, at run time, the MLA Prolog's q_lora / q_lora_scale (the
+    prolog's own q_lora fields are placeholders of the right shape); the
+    attention takes the MLA Prolog's query and the latent cache its KV rows
+    go to (decode.q_attn is unused)."""
+    decode: DecodeInputs
+    mla: MlaInputs
+    prolog: PrologInputs
+
+
+def dia_decode(B=4, n_q=2, L=65536, seed=3002, H=128, K_q=1536, D_x=7168):
+    """The DIA step at the headline decode shape: B=4 sequences of L keys,
+    MTP1 (2 query tokens each at L-2, L-1), whose new keys and latent rows go
+    to those two positions of each sequence."""
+    inp = make_decode_inputs(B=B, n_q=n_q, seq_lens=[L] * B, H_I=64, d_I=128, topk=2048, H=H, seed=seed,
+                             w_sigma=1.0 / 8.0)
+    slot = (inp.seq_of_token.astype(np.int64) * inp.max_L + inp.pos).astype(np.int64)
+    mla = make_mla_inputs(inp.T, inp.pos, slot, seed=seed + 1, H=H, K_q=K_q, D_x=D_x, max_pos=L)
+    pro = make_prolog_inputs(T=inp.T, pos=inp.pos, slot=slot, seed=seed + 2, K_q=K_q, D_x=D_x, max_pos=L)
+    pro.x = mla.x
+    return DiaInputs(decode=inp, mla=mla, prolog=pro)
