@@ -1215,6 +1215,75 @@ def run_int8_gemm(args):
     return res
 
 
+def run_int8_gemm_tc(args):
+    """The int8 GEMM on the tensor cores at M=4096 activation rows, N=8192,
+    K=1536 (the Indexer Prolog's q GEMM over a prefill block): 103 GFLOP per
+    call against the dense tensor peak (f16 operands run at the bf16 rate;
+    the burst figure, the kernel being timed alone).  Three input sets
+    (258 MB, larger than L2) rotate."""
+    from sparse_attention_prolog_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, N, K = 4096, 8192, 1536
+    gen = torch.Generator(device=dev).manual_seed(78)
+    sets = []
+    for _ in range(3):
+        a = torch.randint(-128, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+        b = torch.randint(-128, 128, (N, K), dtype=torch.int8, device=dev, generator=gen)
+        sa = torch.full((M,), 1.0 / 128, dtype=torch.float32, device=dev)
+        sb = torch.full((N,), 1.0 / (128 * K ** 0.5), dtype=torch.float32, device=dev)
+        c = torch.empty((M, N), dtype=torch.float16, device=dev)
+        sets.append((a, sa, b, sb, c))
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            B.dsa_int8_gemm(*sets[i % 3], stream)
+    stream.synchronize()
+    assert B.device_error(stream) == 0
+    K_steps = min(args.steps, 1000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    with ClockSampler(device_uuid(dev)) as clk:
+        with torch.cuda.stream(stream):
+            for i, (e0, e1) in enumerate(evs):
+                e0.record(stream)
+                B.dsa_int8_gemm(*sets[i % 3], stream)
+                e1.record(stream)
+        stream.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    flops = 2.0 * M * N * K
+    tf = flops / (ms * 1e-3) / 1e12
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak, peak_kind = 1900.0, "fallback bf16 dense burst"
+    if os.path.exists(path):
+        with open(path) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured bf16 dense burst (cuBLAS)"
+    res = {"metric": "int8_gemm TFLOP/s (a int8 [4096,1536] x b int8 [8192,1536] -> fp16, tensor cores)",
+           "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K_steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 5), "higher_is_better": True,
+           "dtype": "int8 in (exact f16 MMA), fp32 / int32 accumulate, fp16 out", "data": "synthetic (seeded)",
+           "config": {"workload": "int8_gemm M=4096 N=8192 K=1536", "l2": "3 rotating input sets (258 MB)"},
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(tf / peak, 4), "peak_kind": peak_kind, "algorithmic_flops": flops,
+                        "traffic": profiled_traffic([("gemm.cu", "int8_gemm_tc_4096x8192x1536.txt")])},
+           "gpu_launches": K_steps, "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = int8_gemm_tc_cpu_baseline(sets[0])
+    return res
+
+
+def int8_gemm_tc_cpu_baseline(s0):
+    """The oracle on 256 rows of a against all of b, scaled to the call."""
+    import oracle as O
+    a, sa, b, sb, _ = s0
+    an, bn = a[:256].cpu().numpy(), b.cpu().numpy()
+    t0 = time.perf_counter()
+    O.int8_gemm(an, sa[:256].cpu().numpy(), bn, sb.cpu().numpy())
+    dt = time.perf_counter() - t0
+    flops = 2.0 * 256 * bn.shape[0] * bn.shape[1]
+    return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "256 rows of a against all of b, numpy float64 (BLAS threads up to the core count)"}
+
+
 def run_mhc(args):
     """The mHC mappings for 2^20 tokens with 4 streams (96 bytes in and 96
     out per token, 201 MB: larger than L2), timed launch by launch."""
@@ -1343,15 +1412,16 @@ def main():
                          "decode")
     ap.add_argument("--no-extra-configs", action="store_true",
                     help="do not add the prolog, prefill and ragged lines to the decode line")
-    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm", "mhc", "mla_prolog"], default="step",
+    ap.add_argument("--op", choices=["step", "act_quant", "int8_gemm", "int8_gemm_tc", "mhc", "mla_prolog"],
+                    default="step",
                     help="the decode step (default), or a standalone export: the activation quantiser, the int8 "
                          "GEMM, the mHC mappings, the MLA Prolog")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op != "step":
-        run = {"act_quant": run_act_quant, "int8_gemm": run_int8_gemm, "mhc": run_mhc,
-               "mla_prolog": run_mla}[args.op]
+        run = {"act_quant": run_act_quant, "int8_gemm": run_int8_gemm, "int8_gemm_tc": run_int8_gemm_tc,
+               "mhc": run_mhc, "mla_prolog": run_mla}[args.op]
         print(json.dumps(run(args)), flush=True)
         return
     extra_steps = {"prolog": 500, "prefill": 10, "ragged": 100, "dia": 500}

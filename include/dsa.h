@@ -6,7 +6,7 @@
  *   dsa_indexer_topk    : Lightning Indexer scores + per-query top-k
  *   dsa_sparse_attn     : Sparse (MLA) flash attention over the top-k rows
  *   dsa_act_quant       : standalone activation quantisation (int8, per row)
- *   dsa_int8_gemm       : standalone int8 GEMM + dequant to fp16 (M <= 32)
+ *   dsa_int8_gemm       : standalone int8 GEMM + dequant to fp16
  *   dsa_mhc             : manifold-constrained hyper-connection mappings
  *   dsa_mla_prolog      : MLA Prolog (q_lora, absorbed query, latent KV rows)
  *
@@ -335,17 +335,19 @@ int dsa_act_quant(const dsa_act_quant_args* args, void* stream);
 
 /* ------------------------------------------------------------------------
  * Int8 GEMM  [V4-TileLang §Int8 General Matrix Multiplication, steps 1-4]
- * - a standalone export for activation rows of decode size.
+ * - a standalone export.
  *
  *   c[m,n] = fp16( (sum_k a[m,k] * b[n,k]) * a_scale[m] * b_scale[n] )
  *
  * The int32 sum is exact; the dequantisation is fp32 (the product in the
- * order written), rounded once to fp16.
+ * order written), rounded once to fp16.  M <= 32 rows (decode tokens) run as
+ * a weight stream on dp4a; more rows on the tensor cores (int8 converted
+ * exactly to f16, fp32 sums of at most 1024 products, added in int32), with
+ * the same results.
  * Shapes: a int8 [M, K]; b int8 [N, K] (K-major, row n = output column n);
  * a_scale fp32 [M]; b_scale fp32 [N]; c fp16 [M, N].  a and b 16-byte
- * aligned.  Supported: 1 <= M <= 32 (the weight-streaming regime of decode
- * tokens), N >= 1, K a multiple of 16 up to 65536.  No workspace.  M = 0 or
- * N = 0 is a no-op.
+ * aligned.  Supported: 1 <= M <= 8388608, N >= 1, K a multiple of 16 up to
+ * 65536.  No workspace.  M = 0 or N = 0 is a no-op.
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t M, N, K;

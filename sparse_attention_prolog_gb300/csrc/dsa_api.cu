@@ -341,12 +341,15 @@ int dsa_act_quant(const dsa_act_quant_args* a, void* stream) {
 
 int dsa_int8_gemm(const dsa_int8_gemm_args* a, void* stream) {
   if (!a || a->M < 0 || a->N < 0 || a->K < 0) return DSA_ERR_INVALID_ARG;
-  if (a->M > 32 || a->K < 16 || a->K % 16 != 0 || a->K > 65536) return DSA_ERR_UNSUPPORTED;
+  if (a->K < 16 || a->K % 16 != 0 || a->K > 65536 || a->M > 8388608) return DSA_ERR_UNSUPPORTED;
   if (a->M == 0 || a->N == 0) return DSA_OK;
   if (bad_ptr(a->a, 16) || bad_ptr(a->b, 16) || bad_ptr(a->a_scale, 4) || bad_ptr(a->b_scale, 4) ||
       bad_ptr(a->c, 2))
     return DSA_ERR_INVALID_ARG;
-  return launch_int8_gemm(*a, static_cast<cudaStream_t>(stream));
+  // up to 32 activation rows the GEMM is a weight stream (dp4a against the
+  // rows held in shared memory); beyond, a tensor-core GEMM
+  if (a->M <= 32) return launch_int8_gemm(*a, static_cast<cudaStream_t>(stream));
+  return launch_int8_gemm_tc(*a, static_cast<cudaStream_t>(stream));
 }
 
 int dsa_mhc(const dsa_mhc_args* a, void* stream) {

@@ -141,8 +141,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_act_quant(ctypes.byref(aq), null) == 1                  # x not 16-byte aligned
     aq.M = 0
     assert lib.dsa_act_quant(ctypes.byref(aq), null) == 0                  # empty: no-op
-    g = B.Int8GemmArgs(33, 64, 128, 1 << 20, 1 << 21, 1 << 22, 1 << 23, 1 << 24)
-    assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 2                   # M > 32
+    g = B.Int8GemmArgs(8388609, 64, 128, 1 << 20, 1 << 21, 1 << 22, 1 << 23, 1 << 24)
+    assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 2                   # M > 2^23
     g.M, g.K = 8, 100
     assert lib.dsa_int8_gemm(ctypes.byref(g), null) == 2                   # K % 16
     g.K, g.b = 128, (1 << 22) + 4

@@ -39,7 +39,15 @@ def test_act_quant_bit_exact(M, N, round_scale, cuda_lib):
     assert np.array_equal(y.cpu().numpy(), ry), "codes differ"
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 8192, 1536), (1, 100, 16), (5, 300, 1008), (32, 256, 7168), (17, 129, 64)])
+@pytest.mark.parametrize("M,N,K", [
+    (8, 8192, 1536), (1, 100, 16), (5, 300, 1008), (32, 256, 7168), (17, 129, 64),  # weight-stream path
+    (33, 300, 1008),     # tensor cores: one ragged M tile, an N tail that is not a multiple of 8, K past a 64 stage
+    (64, 8192, 1536),    # half an M tile, two 1024-K chunks
+    (512, 8192, 1536),
+    (4096, 8192, 1536),  # 2048 output tiles
+    (130, 136, 4096),    # two M tiles, four chunks
+    (64, 256, 65536),    # the longest K: 64 chunks through both accumulators
+])
 def test_int8_gemm_matches_oracle(M, N, K, cuda_lib):
     """Exact int32 sums, so the fp16 outputs agree to the last place up to
     the fp32 rounding of the dequantisation (at most one fp16 ulp)."""
@@ -58,3 +66,33 @@ def test_int8_gemm_matches_oracle(M, N, K, cuda_lib):
     ulp = np.maximum(np.abs(ref) * 2.0 ** -10, 2.0 ** -24)
     assert np.isfinite(got).all()
     assert (np.abs(got - ref) <= ulp).all(), f"max excess {np.max(np.abs(got - ref) / ulp):.2f} ulp"
+
+
+@pytest.mark.parametrize("M", [8, 130])
+def test_int8_gemm_sums_are_exact_past_fp32_precision(M, cuda_lib):
+    """Rows of +-127 against b = 127 whose running sums pass 2^24 (where an
+    fp32 accumulator can no longer add 16129 exactly) and end at small
+    integers: with unit scales c is the int32 sum itself, so both paths must
+    give it exactly (the tensor-core path adds exact 1024-product chunks)."""
+    K, N = 4096, 136
+    r = np.random.default_rng(M)
+    a = np.empty((M, K), np.int8)
+    for i in range(M):
+        row = np.concatenate([np.full(K // 2, 127), np.full(K // 2, -127)]).astype(np.int64)
+        row[-1 - (i % 7)] += 1 + i % 5  # a small remainder
+        if i % 2:
+            row = row[r.permutation(K)]
+        a[i] = row.astype(np.int8)
+    b = np.full((N, K), 127, np.int8)
+    b[1::3, -1] = 126
+    sa = np.ones(M, np.float32)
+    sb = np.ones(N, np.float32)
+    c = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    B.dsa_int8_gemm(torch.from_numpy(a).to(DEV), torch.from_numpy(sa).to(DEV), torch.from_numpy(b).to(DEV),
+                    torch.from_numpy(sb).to(DEV), c)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    exact = a.astype(np.int64) @ b.astype(np.int64).T
+    assert np.abs(exact).max() < 2048  # exactly representable in fp16
+    assert (np.abs(np.cumsum(a[0].astype(np.int64) * 127)) > 2 ** 24).any()  # the running sum passes 2^24
+    np.testing.assert_array_equal(c.cpu().numpy().astype(np.int64), exact)

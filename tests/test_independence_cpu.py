@@ -61,7 +61,8 @@ def test_cuda_sources_do_not_mention_the_oracle():
 def test_bench_and_entry_reach_the_oracle_only_from_their_baseline_code():
     allowed = {
         "bench.py": {"oracle_step", "run_act_quant", "run_int8_gemm", "run_mhc", "run_mla", "prolog_cpu_baseline",
-                     "prefill_cpu_baseline", "ragged_cpu_baseline", "dia_cpu_baseline"},
+                     "prefill_cpu_baseline", "ragged_cpu_baseline", "dia_cpu_baseline",
+                     "int8_gemm_tc_cpu_baseline"},
         "__graft_entry__.py": {"smoke"},
     }
     for name, fns in allowed.items():
