@@ -48,6 +48,7 @@ WORKLOAD = ("decode B=4 x MTP1 (T=8 query tokens), KV 65536 per sequence; indexe
             "top-2048; sparse MLA attention 128 heads d_qk=576 d_v=512 bf16; prolog T=8 K_q=1536 D_x=7168")
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+SOAK_MS = (150.0, 60.0)  # untimed replays before / after the timed steps (the clock window)
 
 
 def measured_peaks():
@@ -300,7 +301,8 @@ def time_replays(graphs, K, stream, prep, dev):
         b.record(stream)
     stream.synchronize()
     est_ms = max(a.elapsed_time(b) / (2 * len(graphs)), 1e-3)
-    soak_pre, soak_post = int(150.0 / est_ms) + 1, int(60.0 / est_ms) + 1
+    soak_pre = int(SOAK_MS[0] / est_ms) + 1 if SOAK_MS[0] > 0 else 0
+    soak_post = int(SOAK_MS[1] / est_ms) + 1 if SOAK_MS[1] > 0 else 0
 
     def soak(n):
         with torch.cuda.stream(stream):
@@ -746,7 +748,9 @@ def prefill_config(args, dev, K):
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(stage[dom], 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(stage[dom] / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_flops": idx_ops if dom == "indexer+topk" else att_flop,
-                     "traffic": None},
+                     "traffic": profiled_traffic([("indexer.cu", "indexer_prefill8192.txt"),
+                                                  ("topk.cu", "topk_prefill8192.txt")] if dom == "indexer+topk"
+                                                 else [("attention.cu", "attention_prefill8192.txt")])},
         "stage_roofline": {k: {"achieved_tflops": round(v, 1), "frac": round(v / peak, 4)} for k, v in stage.items()},
         "step_roofline": {"algorithmic_flops": idx_ops + att_flop, "achieved_tflops": round(step_tf, 1),
                           "frac": round(step_tf / peak, 4)},
@@ -863,7 +867,12 @@ def ragged_config(args, dev, K):
                          "one set, no flush"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                     "algorithmic_bytes": alg[dom], "traffic": None},
+                     "algorithmic_bytes": alg[dom],
+                     "traffic": profiled_traffic({
+                         "prolog": [("prolog.cu", "prolog_ragged32.txt")],
+                         "indexer+topk": [("indexer.cu", "indexer_ragged32.txt"), ("topk.cu", "topk_ragged32.txt")],
+                         "attention+combine": [("attention.cu", "attention_ragged32.txt"),
+                                               ("attention.cu", "combine_ragged32.txt")]}[dom])},
         "step_roofline": {"algorithmic_bytes": step_bytes, "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
                           "frac": round(step_bytes / (peak * 1e9) / (ms / 1e3), 4)},
         "stages_ms": {k: round(v, 5) for k, v in st_ms.items()}, "stages_timing": stage_timing,
@@ -984,7 +993,14 @@ def dia_config(args, dev, K):
                    "l2": f"{S} rotating input sets ({S * 0.44:.1f} GB), no flush"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                     "algorithmic_bytes": alg[dom], "traffic": None},
+                     "algorithmic_bytes": alg[dom],
+                     "traffic": profiled_traffic({
+                         "mla_prolog": [("mla.cu", "mla_down_decode_T8.txt"), ("mla.cu", "mla_up_decode_T8.txt"),
+                                        ("mla.cu", "mla_absorb_decode_T8.txt")],
+                         "indexer_prolog": [("prolog.cu", "prolog_decode64k.txt")],
+                         "indexer+topk": [("indexer.cu", "indexer_decode64k.txt"), ("topk.cu", "topk_decode64k.txt")],
+                         "attention+combine": [("attention.cu", "attention_decode64k.txt"),
+                                               ("attention.cu", "combine_decode64k.txt")]}[dom])},
         "step_roofline": {"algorithmic_bytes": step_bytes, "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
                           "frac": round(step_bytes / (peak * 1e9) / (ms / 1e3), 4)},
         "stages_ms": {k: round(v, 5) for k, v in st_ms.items()}, "stages_timing": stage_timing,
@@ -1379,7 +1395,9 @@ def run_mla(args):
                       "bytes_per_call": nbytes},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                        "traffic": profiled_traffic([("mla.cu", "mla_prolog_decode_T8.txt")])},
+                        "traffic": profiled_traffic([("mla.cu", "mla_down_decode_T8.txt"),
+                                                     ("mla.cu", "mla_up_decode_T8.txt"),
+                                                     ("mla.cu", "mla_absorb_decode_T8.txt")])},
            "gpu_launches": 3 * K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -1416,7 +1434,12 @@ def main():
                     default="step",
                     help="the decode step (default), or a standalone export: the activation quantiser, the int8 "
                          "GEMM, the mHC mappings, the MLA Prolog")
+    ap.add_argument("--soak-ms", type=float, default=150.0,
+                    help="untimed replays of the step before the timed steps (and 40%% of it after), so that the "
+                         "clock samples cover a loaded window; 0 for none (profiling runs)")
     args = ap.parse_args()
+    global SOAK_MS
+    SOAK_MS = (args.soak_ms, 0.4 * args.soak_ms)
     if args.warmup < 3:
         args.warmup = 3
     if args.op != "step":
