@@ -171,6 +171,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // between the lanes of a warp.
 constexpr int kMhcTokens = 128;
 
+// The hardware reciprocal (one multi-function-unit instruction, relative
+// error below 2^-22) for the Sinkhorn normalisations: each pass divides by
+// a row or column sum, and the correctly rounded reciprocal costs several
+// instructions more per division in a kernel bound by instruction issue.
+__device__ __forceinline__ float rcp_fast(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int HC>
 __global__ void __launch_bounds__(kMhcTokens) mhc_kernel(const float* __restrict__ mixes, const float* __restrict__ hc_scale,
                                                          const float* __restrict__ hc_base, float* __restrict__ pre,
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(kMhcTokens) mhc_kernel(const float* __restrict
       float sum = 0.f;
 #pragma unroll
       for (int i = 0; i < HC; ++i) sum += c[i][j];
-      const float inv = 1.f / (sum + eps);
+      const float inv = rcp_fast(sum + eps);
 #pragma unroll
       for (int i = 0; i < HC; ++i) c[i][j] *= inv;
     }
@@ -235,7 +245,7 @@ __global__ void __launch_bounds__(kMhcTokens) mhc_kernel(const float* __restrict
       float sum = 0.f;
 #pragma unroll
       for (int j = 0; j < HC; ++j) sum += c[i][j];
-      const float inv = 1.f / (sum + eps);
+      const float inv = rcp_fast(sum + eps);
 #pragma unroll
       for (int j = 0; j < HC; ++j) c[i][j] *= inv;
     }
