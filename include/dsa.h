@@ -85,12 +85,13 @@ int dsa_get_device_error(void* stream);
  * kernels on the current device (nanoseconds; 0 restores the default of 4 s;
  * at most 60 s, else DSA_ERR_INVALID_ARG).  A wait that runs out records
  * DSA_ERR_DEVICE_TIMEOUT (see dsa_get_device_error) and its CTA leaves its
- * loops.  The Indexer Prolog first lets its own bulk copies and tensor-core
- * operations finish (up to 4 s), so after a timeout its next call is safe
- * once its workspace is zeroed again; the other kernels leave at once, so
- * shorten the limit only for the Indexer Prolog.  Synchronous: it takes
- * effect for kernels launched after it returns; call it while none of this
- * library's kernels runs.  No counterpart on the pages: a test hook. */
+ * loops, after letting the bulk copies and tensor-core operations it issued
+ * finish (each such drain bounded by 4 s).  After a timed-out call, zero the
+ * call's workspace again before the next one.  Limits below 20 us are
+ * counted in SM clock cycles (two per nanosecond), longer ones on the global
+ * timer.  Synchronous: it takes effect for kernels launched after it
+ * returns; call it while none of this library's kernels runs.  No
+ * counterpart on the pages: a test hook. */
 int dsa_set_wait_limit_ns(uint64_t ns);
 
 /* ------------------------------------------------------------------------
@@ -224,7 +225,7 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * fp32 score rows live there when scores_out is NULL, and, for H_I >= 64
  * with at most 512 tokens and max_L <= 131072, per-token score histograms);
  * it must be zero-filled once before its first use (the library leaves it
- * zeroed).
+ * zeroed; after a call that ended in DSA_ERR_DEVICE_TIMEOUT, zero it again).
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t T, B, n_q, H_I, d_I, topk, max_L;

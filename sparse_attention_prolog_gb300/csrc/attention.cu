@@ -87,6 +87,7 @@ struct __align__(8) Bars {
   uint64_t ready[2], odone, ffull;              // CTA 1 correction / MMA
   uint64_t alldone;                             // CTA 1: every PV MMA complete
   uint64_t qready;                              // CTA 0: q is in TMEM
+  uint64_t mdrain;                              // the MMA thread's last commit
 };
 
 __device__ __forceinline__ int64_t kv_row(const AttnParams& P, int b, int s) {
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.alldone, 1);
     mbar_init(&bars.ffull, 1);
     mbar_init(&bars.qready, 4);
+    mbar_init(&bars.mdrain, 1);
     abort_flag = 0;
     fence_mbar_init();
     if (rank == 1) {
@@ -393,6 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++st == kStagesK) { st = 0; ph ^= 1; }
             if (++sb == 2) { sb = 0; phs ^= 1; }
           }
+          // every MMA issued has completed before the tensor memory is freed
+          mma_commit(&bars.mdrain);
+          mbar_drain(&bars.mdrain, 0);
         }
       } else if (warp == kMmaWarp) {
         // ------------------------------------------------- PV MMA (CTA 1)
@@ -423,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++st == kStagesV) { st = 0; ph ^= 1; }
             if (j + 1 == n_tiles) mma_commit(&bars.alldone);
           }
+          mma_commit(&bars.mdrain);
+          mbar_drain(&bars.mdrain, 0);
         }
       } else if (warp == kRelayWarp && rank == 1) {
         // ----------------------------------- relay: P slot consumed -> CTA 0

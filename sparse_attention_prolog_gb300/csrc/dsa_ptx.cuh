@@ -55,17 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
   return ok != 0;
 }
-// Probe without a suspend hint: ~15 cycles on a completed phase, against
-// ~50 with the hint; the bounded wait below probes this way first.
-__device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity,
                                                       uint32_t hint_ns = kSuspendHintNs) {
   uint32_t ok;
@@ -77,12 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// The cluster-scope probe without a suspend hint.
-__device__ __forceinline__ bool mbar_probe_cluster(uint64_t* bar, uint32_t parity) {
+// Non-blocking tests of a phase (mbarrier.test_wait never suspends the
+// thread; try_wait without a hint may sleep until the phase completes).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
       "selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
@@ -95,9 +94,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // The wait limit in force on this device: a uint64 kWaitLimitOffset bytes
-// past the error word (dsa_set_wait_limit_ns writes it between calls).
+// past the error word.  dsa_set_wait_limit_ns writes it only while none of
+// this library's kernels runs, so a cached read is exact.
 __device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* err) {
-  return *reinterpret_cast<const volatile uint64_t*>(reinterpret_cast<const uint8_t*>(err) + kWaitLimitOffset);
+  return __ldg(reinterpret_cast<const unsigned long long*>(reinterpret_cast<const uint8_t*>(err) + kWaitLimitOffset));
 }
 
 // Bounded wait on one phase of an mbarrier.  After the device's wait limit
@@ -106,21 +106,31 @@ __device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* err) {
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err,
                                                   volatile int* abort_flag) {
-  if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_probe(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  // a completed phase costs one non-blocking test
+  if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
   const uint64_t limit = wait_limit_ns(err);
-  // A limit below the suspend hint spins on the probe and reads the clock
-  // on every pass: a suspended try_wait may sleep until the phase completes.
-  const bool spin = limit < kSuspendHintNs;
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < (spin ? 1 : 4); ++i) {
-      if (spin) {
-        if (kCluster ? mbar_probe_cluster(bar, parity) : mbar_probe(bar, parity)) return true;
-      } else if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) {
-        return true;
+  if (limit < kSuspendHintNs) {
+    // A short limit spins on the probe (a suspended try_wait may sleep until
+    // the phase completes) and counts SM clock cycles, two per nanosecond
+    // (the limit only grows when the clock runs below 2 GHz): the global
+    // timer may advance in steps longer than such a limit.
+    const long long c0 = clock64();
+    const long long cycles = static_cast<long long>(limit) * 2;
+    while (true) {
+      if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (clock64() - c0 > cycles) {
+        atomicOr(err, kErrTimeout);
+        *abort_flag = 1;
+        return false;
       }
     }
+  }
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i)
+      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit) {
       atomicOr(err, kErrTimeout);

@@ -53,6 +53,7 @@ constexpr uint32_t kTmemCols = 512;                   // 2 accumulators + 3 A st
 
 struct __align__(8) TcBars {
   uint64_t full8[kS8], empty8[kS8], full16[kS16], empty16[kS16], tfull[2], tempty[2];
+  uint64_t mdrain;  // the MMA thread's last commit
 };
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < kS8; ++i) { mbar_init(&bars.full8[i], 1); mbar_init(&bars.empty8[i], 4); }
     for (int i = 0; i < kS16; ++i) { mbar_init(&bars.full16[i], 4); mbar_init(&bars.empty16[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&bars.tfull[i], 1); mbar_init(&bars.tempty[i], 4); }
+    mbar_init(&bars.mdrain, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_load_2d(dst + kTile8, &tm_b, k * kBK, n0, &bars.full8[st]);
         }
       }
+      // if a wait gave up, the last stages' copies land before the CTA leaves
+      for (int i = s > kS8 ? s - kS8 : 0; i < s; ++i) mbar_drain(&bars.full8[i % kS8], (i / kS8) & 1);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
@@ -147,6 +151,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      // every MMA issued has completed before the tensor memory is freed
+      mma_commit(&bars.mdrain);
+      mbar_drain(&bars.mdrain, 0);
     }
   } else if (warp < 6) {
     // ---------------------------------------------------------- converters
@@ -241,7 +248,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.tempty[buf]);
       }
-      if (!ok || *abort_v) break;
+      // the four epilogue warps leave together (a warp that gave up must not
+      // leave the others waiting at the named barrier of the next tile)
+      uint32_t all_ok;
+      asm volatile("{\n.reg .pred p, q;\nsetp.ne.b32 p, %1, 0;\nbar.red.and.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}"
+                   : "=r"(all_ok) : "r"(static_cast<uint32_t>(ok && !*abort_v)) : "memory");
+      if (!all_ok) break;
       if (m < M) {
         const float sa = __ldg(a_scale + m);
         __half* crow = c + static_cast<size_t>(m) * N + n0;

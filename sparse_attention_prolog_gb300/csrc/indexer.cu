@@ -224,6 +224,7 @@ struct __align__(8) Bars {
   uint64_t qfull, qempty;
   uint64_t tfull[3], tempty[3];
   uint64_t epsync;  // barrier of the 8 epilogue warps (bounded wait)
+  uint64_t mdrain;  // the MMA thread's last commit: every MMA done before TMEM is freed
 };
 
 template <int HI, int DI>
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.qempty, 1);
     for (int i = 0; i < 3; ++i) { mbar_init(&bars.tfull[i], 1); mbar_init(&bars.tempty[i], 8); }
     mbar_init(&bars.epsync, 256);
+    mbar_init(&bars.mdrain, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -355,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (w0.left > 0) set_group(w0.g);
       griddep_wait();  // the key cache holds rows the previous kernel wrote
+      int issued = 0;  // stages loaded, in order
       Walker w = w0;
       for (bool more = w.left > 0; more; more = walk_next(tiles_prefix, ngroups, w)) {
         const int g = w.g, j = w.j;
@@ -367,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars.full8[st], static_cast<uint32_t>(kTileKeys * (DI + 2)));
           tma_load_2d(dst, &tmap, 0, static_cast<int>(row), &bars.full8[st]);
           bulk_g2s(&ks_s[st][0], P.k_scale + row, static_cast<uint32_t>(kTileKeys * 2), &bars.full8[st]);
+          ++issued;
           if (++st == kStages8) { st = 0; ph ^= 1; }
           continue;
         }
@@ -386,8 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // box start at a multiple of 8, k_scale is 16-byte aligned).
           bulk_g2s(&ks_s[st][c * bh], P.k_scale + row, static_cast<uint32_t>(bh * 2), &bars.full8[st]);
         }
+        ++issued;
         if (++st == kStages8) { st = 0; ph ^= 1; }
       }
+      // If a wait gave up, the last stages' copies may still be in flight:
+      // let them land before the CTA leaves (stage i % 8, phase i / 8; a
+      // stage consumed already has completed that phase).
+      for (int i = issued > kStages8 ? issued - kStages8 : 0; i < issued; ++i)
+        mbar_drain(&bars.full8[i % kStages8], (i / kStages8) & 1);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- converters
@@ -503,6 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++st16 == n16) { st16 = 0; ph16 ^= 1; }
         if (++acc == n_acc) { acc = 0; aph ^= 1; }
       }
+      // every MMA issued has completed before the tensor memory is freed
+      mma_commit(&bars.mdrain);
+      mbar_drain(&bars.mdrain, 0);
     }
   } else if (warp < 4 || (warp >= 8 && warp < 12)) {
     // ---------------------------------------------------------- epilogue

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   if (tid == 0) {
     // producer: atom i of this slice into stage i % kDownStages, once the
     // MMAs that read the stage's previous atom have completed
+    int issued = 0;
     for (int i = 0; i < na; ++i) {
       const int s = i % kDownStages;
       if (i >= kDownStages && !mbar_wait(&empty[s], ((i / kDownStages) - 1) & 1, P.err, &abort_flag)) break;
@@ -109,7 +110,11 @@ __global__ void __launch_bounds__(kDownThreads, 1)
       mbar_arrive_expect_tx(&full[s], kStage);
       tma_load_2d(st, tw, xc, wrow, &full[s]);  // rows past the weight read as zero
       tma_load_2d(st + kDownAtomW, &tm_x, xc, 0, &full[s]);  // tokens past T read as zero
+      issued = i + 1;
     }
+    // if a wait gave up, the last stages' copies land before the CTA leaves
+    for (int i = issued > kDownStages ? issued - kDownStages : 0; i < issued; ++i)
+      mbar_drain(&full[i % kDownStages], (i / kDownStages) & 1);
   } else if (tid == 32) {
     // MMA issuer: D (+)= W_atom [128 x 64] . X_atom^T [64 x NX], K = 16 per MMA
     const uint32_t idesc = idesc_f16(128, NX, kFmtBF16, 0, 0);
@@ -127,8 +132,11 @@ __global__ void __launch_bounds__(kDownThreads, 1)
     mma_commit(&mdone);
   }
   __syncwarp();
-  // a CTA whose tiles never arrived adds nothing (its error is recorded)
-  const bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag) && !*static_cast<volatile int*>(&abort_flag);
+  // a CTA whose tiles never arrived adds nothing (its error is recorded); a
+  // wait that gave up still lets the MMAs finish before TMEM is read or freed
+  bool ok = mbar_wait(&mdone, 0, P.err, &abort_flag);
+  if (!ok) mbar_drain(&mdone, 0);
+  ok = ok && !*static_cast<volatile int*>(&abort_flag);
   __syncwarp();
   tc_fence_after();
   uint32_t v[32];
@@ -294,7 +302,8 @@ __global__ void __launch_bounds__(kUpThreads, TM <= 8 ? 2 : 1)
   const int ch = tid % kUpCh, tg = tid / kUpCh;
   const int n = blockIdx.x * kUpCh + ch;
   const float sb = __half2float(__ldg(P.w_uq_scale + n));
-  const bool ok = mbar_wait(&bar, 0, P.err, &abort_flag);
+  bool ok = mbar_wait(&bar, 0, P.err, &abort_flag);
+  if (!ok) mbar_drain(&bar, 0);  // the slab's copies land before it is read or the CTA leaves
   __syncthreads();  // codes and scales of every token are in shared memory
   int acc[TPT];
 #pragma unroll
@@ -399,7 +408,8 @@ __global__ void __launch_bounds__(kAbsThreads, TM <= 16 ? 2 : 1) mla_absorb_kern
     const int t = i / kDn;
     sQ[i] = t < P.T ? __ldcg(P.nope + (static_cast<size_t>(t) * P.H + h) * kDn + i % kDn) : 0.f;
   }
-  const bool ok = mbar_wait(&bar, 0, P.err, &abort_flag);
+  bool ok = mbar_wait(&bar, 0, P.err, &abort_flag);
+  if (!ok) mbar_drain(&bar, 0);  // the slab's copies land before it is read or the CTA leaves
   __syncthreads();
   // thread: column pair cp of this half, no-position dims [64 nh, 64 nh + 64)
   const int cp = tid & 127, nh = tid >> 7;

@@ -128,7 +128,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t csw = static_cast<uint32_t>(ch & 7);
   for (int chunk = 0; chunk < nchunks; ++chunk) {
     const int s = chunk & 1;
-    if (!mbar_wait(&full[s], (chunk >> 1) & 1, err, &abort_flag)) break;
+    // every thread takes the same decision (the loop ends with a barrier)
+    if (!__syncthreads_and(mbar_wait(&full[s], (chunk >> 1) & 1, err, &abort_flag))) {
+      // chunks `chunk` and `chunk + 1` may still be in flight: let them
+      // land before the CTA leaves
+      if (tid == 0)
+        for (int j = chunk; j < nchunks && j < chunk + 2; ++j) mbar_drain(&full[j & 1], (j >> 1) & 1);
+      break;
+    }
     const uint8_t* w = stage_w(s);
     const uint8_t* x = w + kGemmStageW;
 #pragma unroll 2

@@ -19,11 +19,12 @@ DSA_ERR_DEVICE_DATA = 6
 
 
 def _prolog(rows=64, large=False):
-    """The decode step's prolog (8 tokens), or with large=True the largest
-    supported one: 32 tokens, K_q = 2048, D_x = 12288 (each CTA's copies
-    take longest)."""
+    """The decode step's prolog (8 tokens), or with large=True one token
+    against the largest weights (K_q = 2048, D_x = 12288): each CTA's weight
+    copies take microseconds from a cold L2, while the work before its first
+    wait (one token's RoPE row) is a single round trip."""
     if large:
-        T = 32
+        T = 1
         p = W.make_prolog_inputs(T=T, pos=np.arange(1000, 1000 + T), slot=np.arange(T), seed=71, K_q=2048,
                                  D_x=12288, max_pos=2048)
     else:
@@ -49,7 +50,7 @@ def _check_against_oracle(p, buf, tokens, rows=64):
 
 
 def test_wait_limit_runs_out_then_next_call_passes(cuda_lib):
-    """With a 1 ns limit every prolog CTA gives up waiting for its weight
+    """With a 1 ns limit the prolog CTAs give up waiting for their weight
     copies (L2 is flushed first, so they come from HBM and take microseconds):
     the call reports a device timeout.  The CTAs let their copies and MMAs
     finish before leaving, so with the default limit restored the next call on
@@ -105,3 +106,82 @@ def test_prolog_position_outside_the_rope_table(cuda_lib):
     torch.cuda.synchronize()
     assert B.device_error() == 0
     _check_against_oracle(p, buf, np.arange(p.T))
+
+
+def test_wait_limit_runs_out_in_the_decode_step_then_next_step_passes(cuda_lib):
+    """The decode step (prolog, indexer + top-k, attention + combine) with a
+    1 ns limit after an L2 flush: the waits of the prolog, the indexer and
+    the attention give up, each CTA lets its copies and MMAs finish before it
+    leaves, and the step reports a device timeout.  With the default limit
+    and zeroed workspaces the next step on the same buffers matches the
+    oracle (stage by stage on its own upstream outputs)."""
+    from parity_utils import check_attention, check_topk_set, oracle_scores_row
+    from sparse_attention_prolog_gb300.pipeline import DecodeBuffers
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[8192, 6000], H_I=64, d_I=128, topk=512, H=128, seed=81)
+    buf = DecodeBuffers(inp, DEV, keep_scores=True)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=DEV)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    B.set_wait_limit_ns(1)
+    try:
+        flush.zero_()
+        buf.run()
+        torch.cuda.synchronize()
+        assert B.device_error() == DSA_ERR_DEVICE_TIMEOUT
+    finally:
+        B.set_wait_limit_ns(0)
+    buf.tws.zero_()
+    buf.aws.zero_()
+    buf.run()
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    idx = buf.topk_idx.cpu().numpy()
+    sc = buf.scores.cpu().numpy()
+    for t in range(inp.T):
+        ref = oracle_scores_row(inp, t)
+        n = int(inp.pos[t]) + 1
+        assert np.abs(sc[t, :n] - ref).max() <= 2e-6 * max(np.abs(ref).max(), 1e-30)
+        check_topk_set(idx[t], ref, n, inp.topk, f"t={t}")
+    ref_o, ref_l = O.sparse_attention(inp, idx)
+    check_attention(buf.out.float().cpu().numpy(), ref_o, buf.lse.cpu().numpy(), ref_l, "attention")
+
+
+def test_wait_limit_runs_out_in_the_mla_prolog_and_the_int8_gemm(cuda_lib):
+    """The MLA Prolog and the tensor-core int8 GEMM with a 1 ns limit report
+    a device timeout; with the default limit the next calls give the oracle's
+    q_lora codes and the exact GEMM."""
+    from sparse_attention_prolog_gb300.pipeline import MlaBuffers
+    T = 8
+    p = W.make_mla_inputs(T, np.arange(T) * 5, np.arange(T, dtype=np.int64), seed=82, max_pos=64)
+    mla = MlaBuffers(p, DEV, 16)
+    M, N, K = 512, 2048, 3072
+    r = np.random.default_rng(83)
+    a = r.integers(-128, 128, (M, K)).astype(np.int8)
+    b = r.integers(-128, 128, (N, K)).astype(np.int8)
+    sa = np.full(M, 1.0 / 128, np.float32)
+    sb = np.full(N, 1.0 / (128 * K ** 0.5), np.float32)
+    ta, tb = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    tsa, tsb = torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV)
+    c = torch.zeros((M, N), dtype=torch.float16, device=DEV)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=DEV)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    for run in (lambda: mla.run(), lambda: B.dsa_int8_gemm(ta, tsa, tb, tsb, c)):
+        B.set_wait_limit_ns(1)
+        try:
+            flush.zero_()
+            run()
+            torch.cuda.synchronize()
+            assert B.device_error() == DSA_ERR_DEVICE_TIMEOUT
+        finally:
+            B.set_wait_limit_ns(0)
+    mla.ws.zero_()
+    mla.run()
+    B.dsa_int8_gemm(ta, tsa, tb, tsb, c)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    ref = O.mla_prolog(p)
+    check_codes(mla.q_lora.cpu().numpy(), mla.q_lora_scale.cpu().numpy(), ref["q_lora"], ref["q_lora_scale"], "q_lora")
+    want = O.int8_gemm(a, sa.astype(np.float64), b, sb.astype(np.float64)).astype(np.float64)
+    got = c.cpu().numpy().astype(np.float64)
+    assert (np.abs(got - want) <= np.maximum(np.abs(want) * 2.0 ** -10, 2.0 ** -24)).all()
