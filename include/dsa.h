@@ -39,9 +39,10 @@
  *     stream is still running, and waits for that kernel to complete before
  *     it reads anything the kernel may have written.  The exceptions are
  *     inputs that a decode step never produces in the kernel right before
- *     the call, which are read as soon as the kernel starts: pos and
- *     seq_of_token of dsa_indexer_topk / dsa_indexer_scores, and q and
- *     seq_of_token of dsa_sparse_attn.  The
+ *     the call, which are read as soon as the kernel starts: the weights
+ *     w_qb, w_k and w_proj of dsa_indexer_prolog, pos and seq_of_token of
+ *     dsa_indexer_topk / dsa_indexer_scores, and q and seq_of_token of
+ *     dsa_sparse_attn.  The
  *     kernel enqueued just before such a call must not write them (an event
  *     or a memcpy in between lifts the rule).
  */

@@ -230,13 +230,18 @@ __device__ void q_stream(const PrologParams& P, uint8_t* smem, Pre& pre) {
   }
   __syncthreads();
   griddep_launch_dependents();
-  griddep_wait();
+  // The weight slab is never written by the previous kernel: its copies go
+  // out before the wait for that kernel (programmatic launch), the
+  // activation rows after it.
   if (warp == 0) {
     const uint32_t bytes = static_cast<uint32_t>((D + T) * kchunk);
     if (lane == 0) mbar_arrive_expect_tx(&bar, bytes);
     __syncwarp();
     const int8_t* wsrc = P.w_qb + static_cast<size_t>(head) * D * P.K_q + rank * kchunk;
     for (int r = lane; r < D; r += 32) bulk_g2s(sW + r * wstride, wsrc + static_cast<size_t>(r) * P.K_q, kchunk, &bar);
+  }
+  griddep_wait();  // q_lora and its scales may come from the previous kernel
+  if (warp == 0) {
     const int8_t* qsrc = P.q_lora + rank * kchunk;
     for (int t = lane; t < T; t += 32) bulk_g2s(sQ + t * kchunk, qsrc + static_cast<size_t>(t) * P.K_q, kchunk, &bar);
   }
@@ -348,16 +353,18 @@ __device__ void kw_stream(const PrologParams& P, const CUtensorMap* tm_wk, const
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   griddep_launch_dependents();
-  griddep_wait();
+  // the weight tiles before the wait for the previous kernel, x after it
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nb) * ((has_w ? 2u : 1u) * kKwAtom + kAtomX));
     for (int a = 0; a < nb; ++a) {
       const int xc = x0 + a * 64;  // atoms past D_x read as zero
       tma_load_2d(sA0 + a * kKwAtom, tm_wk, xc, 0, &bar);
       if (has_w) tma_load_2d(sA1 + a * kKwAtom, tm_wp, xc, 0, &bar);
-      tma_load_2d(sB + a * kAtomX, tm_x, xc, 0, &bar);
     }
   }
+  griddep_wait();
+  if (tid == 0)
+    for (int a = 0; a < nb; ++a) tma_load_2d(sB + a * kAtomX, tm_x, x0 + a * 64, 0, &bar);
   // inputs of the last CTA's epilogue
   if (tid < D) {
     pre.gamma[tid] = __ldg(P.ln_gamma + tid);
@@ -559,17 +566,19 @@ int launch_prolog(const dsa_prolog_args& a, void* ws, cudaStream_t stream) {
   }
   const int grid = P.n_q_ctas + static_cast<int>(round_up(P.n_kw_ctas, kQSplit));
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kQSplit;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e;
   auto go = [&](auto kern) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
