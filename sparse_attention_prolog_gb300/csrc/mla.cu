@@ -14,25 +14,30 @@
 //               (128-byte swizzle), multiplies on the tensor core (bf16,
 //               M = 128 channels, N = tokens padded to 16 or 32, fp32 in
 //               tensor memory) and adds its partial sums into the fp32
-//               workspace.  The last CTA (atomic ticket) normalises the
-//               query latent (RMSNorm), quantises it per token, normalises
-//               the KV latent, rotates its rotary part, writes q_lora and the
-//               latent-cache rows, and clears the workspace.
-//   mla_up      q_lora . w_uq^T as exact int32 dp4a sums, dequantised.  A
-//               CTA takes 64 channels, so it holds either 64 no-position
-//               dims of one head (fp32, to the workspace) or that head's 64
-//               rotary dims (rotated, to q[:, h, 512:576] in bf16).
+//               workspace.
+//   mla_up      q_lora . w_uq^T as exact int32 dp4a sums on the weight-
+//               stream layout (w8stream.cuh): one CTA per SM over a
+//               contiguous range of w_uq's rows.  Each CTA normalises the
+//               query latent (RMSNorm) and quantises it per token from the
+//               sums (CTA 0 also writes q_lora), dequantises its rows' sums
+//               into the workspace, and writes the latent-cache rows of
+//               some tokens (RMSNorm of the KV latent, rotated rotary part).
 //   mla_absorb  q[:, h, c] = sum_n u_nope[:, h, n] w_uk[h, n, c]: one CTA per
 //               (head, half of the 512 latent dims), whose 64 KB of w_uk
-//               arrive by bulk copies issued before it waits for mla_up.
+//               arrive by bulk copies issued before it waits for mla_up; the
+//               second half also rotates the head's rotary dims into
+//               q[:, h, 512:576]; the CTAs clear mla_down's sums for the
+//               next call.
 // mla_up and mla_absorb start early (programmatic dependent launch) and
 // fetch their weights while the kernel before them finishes.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
+#include "w8stream.cuh"
 
 namespace dsa {
 namespace {
@@ -155,24 +160,23 @@ __global__ void __launch_bounds__(kDownThreads, 1)
 }
 
 // -------------------------------------------------------------------- up
-constexpr int kUpThreads = 256, kUpCh = 64;
-constexpr uint32_t kUpBoxW = kUpCh * 128;  // [64 channels][128 int8]
-constexpr int kMaxQv = 2048 / 128;         // float4 per lane of a query-latent row
+constexpr int kMaxQv = 2048 / 128;  // float4 per lane of a query-latent row
 
 struct UpParams {
-  int T, H, K_q, interleaved, max_pos;
+  int T, H, K_q, max_pos;
+  int interleaved;
   float eps;
   const float* sums;  // workspace: [T, K_q + 576] from mla_down
   const float* gamma_q;
   const float* gamma_kv;
+  const int8_t* w_uq;  // [H * 192, K_q]
   const __half* w_uq_scale;
   const int32_t* pos;
   const float* rope_cos;
   const float* rope_sin;
   int8_t* q_lora;
   __half* q_lora_scale;
-  __nv_bfloat16* q;  // [T, H, 576]
-  float* nope;       // workspace: [T, H, 128] fp32
+  float* up;  // workspace: [T, H * 192] dequantised q_lora . w_uq^T
   __nv_bfloat16* kv_cache;
   const int64_t* slot;
   int64_t cache_rows;
@@ -180,13 +184,10 @@ struct UpParams {
 };
 
 // One warp, token t: c_q = RMSNorm(sums[t, :K_q]) * gamma_q, quantised per
-// token.  The codes go to the A slab (128-byte swizzled rows of 128 codes,
-// the layout the dot loop reads) and, in CTA 0, to q_lora; returns the
-// fp16 scale as fp32.  Every CTA computes the same codes: the arithmetic
-// is the same sequence of fp32 operations on the same sums.
-template <int TM>
-__device__ __forceinline__ float quant_latent(const UpParams& P, int t, int lane, uint8_t* sA, bool write_out) {
-  constexpr uint32_t kBoxA = TM * 128;
+// token.  The codes go to sA (row t, K_q bytes) and, in CTA 0, to q_lora;
+// returns the fp16 scale as fp32.  Every CTA computes the same codes: the
+// arithmetic is the same sequence of fp32 operations on the same sums.
+__device__ __forceinline__ float quant_latent(const UpParams& P, int t, int lane, int8_t* sA, bool write_out) {
   const float* row = P.sums + static_cast<size_t>(t) * (P.K_q + kDkv);
   const int nj = P.K_q / 128;
   float4 v[kMaxQv];
@@ -219,8 +220,7 @@ __device__ __forceinline__ float quant_latent(const UpParams& P, int t, int lane
   for (int j = 0; j < kMaxQv; ++j) {
     if (j < nj) {
       const uint32_t w4 = code(v[j].x) | (code(v[j].y) << 8) | (code(v[j].z) << 16) | (code(v[j].w) << 24);
-      // byte column 4 lane of box j: 16-byte chunk lane / 4, swizzled by the row
-      *reinterpret_cast<uint32_t*>(sA + j * kBoxA + t * 128 + (((lane >> 2) ^ (t & 7)) << 4) + 4 * (lane & 3)) = w4;
+      *reinterpret_cast<uint32_t*>(sA + static_cast<size_t>(t) * P.K_q + 128 * j + 4 * lane) = w4;
       if (write_out) *reinterpret_cast<uint32_t*>(P.q_lora + static_cast<size_t>(t) * P.K_q + 128 * j + 4 * lane) = w4;
     }
   }
@@ -266,101 +266,57 @@ __device__ __forceinline__ void kv_row(const UpParams& P, int t, int lane) {
   out[kDc + ib] = __float2bfloat16_rn(b * cs + a * sn);
 }
 
-template <int TM>
-__global__ void __launch_bounds__(kUpThreads, TM <= 8 ? 2 : 1)
-    mla_up_kernel(const __grid_constant__ UpParams P, const __grid_constant__ CUtensorMap tm_w) {
-  constexpr uint32_t kBoxA = TM * 128;  // [TM tokens][128 int8]
-  constexpr int TPT = TM / 4;           // tokens per thread: t = tg, tg + 4, ...
+// q_lora . w_uq^T on the weight-stream layout (w8stream.cuh): one CTA per
+// SM over a contiguous range of w_uq's H * 192 rows, the producer warp
+// streaming it from the kernel's start (the weights do not depend on
+// mla_down), the consumer warps waiting for mla_down's sums, quantising the
+// query latent of every token into shared memory and loading their chunks
+// of it into registers.  The sums are dequantised into the workspace `up`;
+// mla_absorb reads the no-position dims and rotates the rotary ones.
+template <int MT, int KW>
+__global__ void __launch_bounds__(kW8Threads, 1) mla_up_kernel(const __grid_constant__ UpParams P, const W8Plan p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t full[kW8MaxStages], empty[kW8MaxStages];
   __shared__ int abort_flag;
-  __shared__ float rbuf[TM][kUpCh];
-  __shared__ float s_sa[TM];
+  __shared__ float s_sa[MT];
+  const size_t ring = static_cast<size_t>(p.ns) * p.stage_bytes;
+  const W8Ring R{smem, full, empty, reinterpret_cast<int*>(smem + ring)};
+  int8_t* sA = reinterpret_cast<int8_t*>(smem + ring + 2 * static_cast<size_t>(p.sr) * MT * 4);  // [T][K_q] codes
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nbox = P.K_q / 128;
-  uint8_t* sW = smem;                     // [nbox][64][128]
-  uint8_t* sA = smem + nbox * kUpBoxW;    // [nbox][TM][128]
-  const int h = blockIdx.x / 3, part = blockIdx.x % 3;  // part 0, 1: no-position dims; 2: rotary dims
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    for (int i = 0; i < p.ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kW8Consumers);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < TM) s_sa[tid] = 0.f;  // tokens past T: rows the dot loop reads but nothing keeps
+  for (int i = tid; i < 2 * p.sr * MT; i += kW8Threads) R.red[i] = 0;
   __syncthreads();
   griddep_launch_dependents();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nbox) * kUpBoxW);
-    for (int q = 0; q < nbox; ++q) tma_load_2d(sW + q * kUpBoxW, &tm_w, q * 128, blockIdx.x * kUpCh, &bar);
+  const int N = P.H * kDh;
+  int r0, r1;
+  w8_rows(N, blockIdx.x, gridDim.x, r0, r1);
+  if (warp == kW8Consumers) {
+    if (lane == 0) w8_produce(p, R, P.w_uq, P.K_q, r0, r1, P.err, &abort_flag);
+    return;
   }
   griddep_wait();  // the sums come from mla_down
-  for (int t = warp; t < P.T; t += kUpThreads / 32) {
-    const float sdiv = quant_latent<TM>(P, t, lane, sA, blockIdx.x == 0);
+  for (int t = warp; t < P.T; t += kW8Consumers) {
+    const float sdiv = quant_latent(P, t, lane, sA, blockIdx.x == 0);
     if (lane == 0) s_sa[t] = sdiv;
   }
-  const int ch = tid % kUpCh, tg = tid / kUpCh;
-  const int n = blockIdx.x * kUpCh + ch;
-  const float sb = __half2float(__ldg(P.w_uq_scale + n));
-  bool ok = mbar_wait(&bar, 0, P.err, &abort_flag);
-  if (!ok) mbar_drain(&bar, 0);  // the slab's copies land before it is read or the CTA leaves
-  __syncthreads();  // codes and scales of every token are in shared memory
-  int acc[TPT];
-#pragma unroll
-  for (int i = 0; i < TPT; ++i) acc[i] = 0;
-  const uint32_t csw = static_cast<uint32_t>(ch & 7);
-  if (ok) {
-    for (int q = 0; q < nbox; ++q) {
-      const uint8_t* w = sW + q * kUpBoxW + ch * 128;
-      const uint8_t* x = sA + q * kBoxA;
-#pragma unroll 2
-      for (int j = 0; j < 8; ++j) {
-        const int4 wv = *reinterpret_cast<const int4*>(w + ((j ^ csw) << 4));
-#pragma unroll
-        for (int i = 0; i < TPT; ++i) {
-          const int t = tg + 4 * i;  // one token row per warp: broadcast reads
-          const int4 av = *reinterpret_cast<const int4*>(x + t * 128 + ((j ^ (t & 7)) << 4));
-          acc[i] = __dp4a(wv.x, av.x, acc[i]);
-          acc[i] = __dp4a(wv.y, av.y, acc[i]);
-          acc[i] = __dp4a(wv.z, av.z, acc[i]);
-          acc[i] = __dp4a(wv.w, av.w, acc[i]);
-        }
-      }
-    }
-  }
-  if (part < 2) {
-    if (ok) {
-#pragma unroll
-      for (int i = 0; i < TPT; ++i) {
-        const int t = tg + 4 * i;
-        if (t < P.T)
-          P.nope[(static_cast<size_t>(t) * P.H + h) * kDn + part * kUpCh + ch] =
-              static_cast<float>(acc[i]) * s_sa[t] * sb;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) rbuf[tg + 4 * i][ch] = static_cast<float>(acc[i]) * s_sa[tg + 4 * i] * sb;
-    __syncthreads();
-    if (ok) {
-      for (int idx = tid; idx < P.T * (kDr / 2); idx += kUpThreads) {
-        const int t = idx / (kDr / 2), l = idx % (kDr / 2);
-        const int p = __ldg(P.pos + t);
-        if (p < 0 || p >= P.max_pos) {
-          atomicOr(P.err, kErrBadIndex);
-          continue;
-        }
-        const int ia = P.interleaved ? 2 * l : l, ib = P.interleaved ? 2 * l + 1 : l + kDr / 2;
-        const float cs = __ldg(P.rope_cos + static_cast<size_t>(p) * (kDr / 2) + l);
-        const float sn = __ldg(P.rope_sin + static_cast<size_t>(p) * (kDr / 2) + l);
-        const float a = rbuf[t][ia], b = rbuf[t][ib];
-        __nv_bfloat16* out = P.q + (static_cast<size_t>(t) * P.H + h) * kDkv + kDc;
-        out[ia] = __float2bfloat16_rn(a * cs - b * sn);
-        out[ib] = __float2bfloat16_rn(b * cs + a * sn);
-      }
-    }
-  }
-  // latent KV rows: token t by warp 0 of CTA t (mod the grid)
+  asm volatile("bar.sync 1, 256;" ::: "memory");  // every token's codes and scale are in shared memory
+  const int nck = P.K_q / 16, cpw = (nck + p.wk - 1) / p.wk;
+  const int c0 = (warp % p.wk) * cpw, c1 = min(nck, c0 + cpw);
+  int4 areg[KW][MT];
+  w8_load_a<MT, KW>(areg, sA, P.K_q, P.T, c0, c1, lane);
+  auto epi = [&](int t, int n, int v) {
+    P.up[static_cast<size_t>(t) * N + n] = static_cast<float>(v) * s_sa[t] * __half2float(__ldg(P.w_uq_scale + n));
+  };
+  w8_consume<MT, KW, 1>(p, R, areg, P.K_q, P.T, r0, r1, c0, c1, epi, P.err, &abort_flag);
+  // latent KV rows: token t by consumer warp 0 of CTA t (mod the grid)
   if (warp == 0)
     for (int t = blockIdx.x; t < P.T; t += gridDim.x) kv_row(P, t, lane);
 }
@@ -370,10 +326,13 @@ constexpr int kAbsThreads = 256;
 constexpr uint32_t kAbsW = kDn * (kDc / 2) * 2;  // [128 n][256 c] bf16 = 64 KB
 
 struct AbsParams {
-  int T, H, n_sums;
+  int T, H, n_sums, max_pos, interleaved;
   const __nv_bfloat16* w_uk;  // [H, 128, 512]
-  const float* nope;          // workspace: [T, H, 128]
+  const float* up;            // workspace: [T, H, 192] from mla_up
   float* sums;                // workspace: mla_down's sums, cleared here for the next call
+  const int32_t* pos;
+  const float* rope_cos;
+  const float* rope_sin;
   __nv_bfloat16* q;           // [T, H, 576]
   uint32_t* err;
 };
@@ -406,7 +365,26 @@ __global__ void __launch_bounds__(kAbsThreads, TM <= 16 ? 2 : 1) mla_absorb_kern
   for (int i = blockIdx.x * kAbsThreads + tid; i < P.n_sums; i += gridDim.x * kAbsThreads) P.sums[i] = 0.f;
   for (int i = tid; i < TM * kDn; i += kAbsThreads) {
     const int t = i / kDn;
-    sQ[i] = t < P.T ? __ldcg(P.nope + (static_cast<size_t>(t) * P.H + h) * kDn + i % kDn) : 0.f;
+    sQ[i] = t < P.T ? __ldcg(P.up + (static_cast<size_t>(t) * P.H + h) * kDh + i % kDn) : 0.f;
+  }
+  if (half == 1) {
+    // the head's rotary dims: q[:, h, 512:576] = RoPE(up[:, h, 128:192])
+    for (int idx = tid; idx < P.T * (kDr / 2); idx += kAbsThreads) {
+      const int t = idx / (kDr / 2), l = idx % (kDr / 2);
+      const int p = __ldg(P.pos + t);
+      if (p < 0 || p >= P.max_pos) {
+        if (h == 0) atomicOr(P.err, kErrBadIndex);
+        continue;
+      }
+      const int ia = P.interleaved ? 2 * l : l, ib = P.interleaved ? 2 * l + 1 : l + kDr / 2;
+      const float cs = __ldg(P.rope_cos + static_cast<size_t>(p) * (kDr / 2) + l);
+      const float sn = __ldg(P.rope_sin + static_cast<size_t>(p) * (kDr / 2) + l);
+      const float* r = P.up + (static_cast<size_t>(t) * P.H + h) * kDh + kDn;
+      const float a = __ldcg(r + ia), b = __ldcg(r + ib);
+      __nv_bfloat16* out = P.q + (static_cast<size_t>(t) * P.H + h) * kDkv + kDc;
+      out[ia] = __float2bfloat16_rn(a * cs - b * sn);
+      out[ib] = __float2bfloat16_rn(b * cs + a * sn);
+    }
   }
   bool ok = mbar_wait(&bar, 0, P.err, &abort_flag);
   if (!ok) mbar_drain(&bar, 0);  // the slab's copies land before it is read or the CTA leaves
@@ -451,9 +429,9 @@ size_t down_sums_bytes(const dsa_mla_prolog_args& a) {
 }  // namespace
 
 // Workspace: [T, K_q + 576] fp32 sums of mla_down (zero between calls), then
-// [T, H, 128] fp32 no-position query dims of mla_up.
+// [T, H, 192] fp32 up-projected query dims of mla_up.
 size_t mla_workspace(const dsa_mla_prolog_args& a) {
-  return down_sums_bytes(a) + round_up(static_cast<size_t>(a.T) * a.H * kDn * sizeof(float), 256);
+  return down_sums_bytes(a) + round_up(static_cast<size_t>(a.T) * a.H * kDh * sizeof(float), 256);
 }
 
 int launch_mla(const dsa_mla_prolog_args& a, void* ws, cudaStream_t stream) {
@@ -461,7 +439,7 @@ int launch_mla(const dsa_mla_prolog_args& a, void* ws, cudaStream_t stream) {
   if (!err) return DSA_ERR_CUDA;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* sums = reinterpret_cast<float*>(wsb);
-  float* nope = reinterpret_cast<float*>(wsb + down_sums_bytes(a));
+  float* up = reinterpret_cast<float*>(wsb + down_sums_bytes(a));
 
   // ---- down: row blocks x slices of D_x, as many slices as fill the SMs
   DownParams D{};
@@ -509,39 +487,49 @@ int launch_mla(const dsa_mla_prolog_args& a, void* ws, cudaStream_t stream) {
   U.T = a.T; U.H = a.H; U.K_q = a.K_q; U.interleaved = a.rope_interleaved; U.max_pos = a.rope_max_pos;
   U.eps = a.rms_eps;
   U.sums = sums; U.gamma_q = a.gamma_q; U.gamma_kv = a.gamma_kv;
+  U.w_uq = a.w_uq;
   U.w_uq_scale = reinterpret_cast<const __half*>(a.w_uq_scale);
   U.pos = a.pos; U.rope_cos = a.rope_cos; U.rope_sin = a.rope_sin;
   U.q_lora = a.q_lora; U.q_lora_scale = reinterpret_cast<__half*>(a.q_lora_scale);
-  U.q = reinterpret_cast<__nv_bfloat16*>(a.q); U.nope = nope;
+  U.up = up;
   U.kv_cache = reinterpret_cast<__nv_bfloat16*>(a.kv_cache); U.slot = a.slot; U.cache_rows = a.cache_rows;
   U.err = err;
-  alignas(64) CUtensorMap tm_w;
-  {
-    const uint64_t st[1] = {static_cast<uint64_t>(a.K_q)};
-    const uint64_t dw[2] = {static_cast<uint64_t>(a.K_q), static_cast<uint64_t>(a.H) * kDh};
-    const uint32_t bw[2] = {128, kUpCh};
-    if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_uq, dw, st, bw, 128)) return DSA_ERR_CUDA;
-  }
-  const size_t smem_up = 1024 + static_cast<size_t>(a.K_q / 128) * (kUpBoxW + static_cast<size_t>(tm) * 128);
+  // the ring takes what the codes of every token and the cross-warp sums
+  // leave of shared memory
+  const size_t codes = static_cast<size_t>(tm) * a.K_q;
+  const uint32_t ring_max =
+      static_cast<uint32_t>(220 * 1024 - 1024 - codes - 2 * static_cast<size_t>(kW8MaxStageRows) * tm * 4);
+  // a's chunks of a lane in up to 128 registers: at K_q = 1536 and 8 tokens
+  // the warps need not split K, so no stage waits for a cross-warp sum
+  const W8Plan wp = w8_plan(a.K_q, tm, 128, ring_max < kW8RingBytes ? ring_max : kW8RingBytes);
+  if (wp.kw == 0) return DSA_ERR_UNSUPPORTED;
+  const size_t smem_up = w8_smem(wp, tm) + codes;
   cudaLaunchConfig_t cu = {};
-  cu.gridDim = dim3(3 * a.H);
-  cu.blockDim = dim3(kUpThreads);
+  cu.gridDim = dim3(std::min(a.H * kDh, sm_count()));
+  cu.blockDim = dim3(kW8Threads);
   cu.dynamicSmemBytes = smem_up;
   cu.stream = stream;
   cu.attrs = pdl;
   cu.numAttrs = 1;
   auto go_up = [&](auto kern) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_up));
-    if (r == cudaSuccess)  // two CTAs per SM where they fit
-      r = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    return r == cudaSuccess ? cudaLaunchKernelEx(&cu, kern, U, tm_w) : r;
+    return r == cudaSuccess ? cudaLaunchKernelEx(&cu, kern, U, wp) : r;
   };
-  e = tm == 8 ? go_up(mla_up_kernel<8>) : (tm == 16 ? go_up(mla_up_kernel<16>) : go_up(mla_up_kernel<32>));
+  if (tm == 8) {
+    e = wp.kw == 1 ? go_up(mla_up_kernel<8, 1>) : wp.kw == 2 ? go_up(mla_up_kernel<8, 2>)
+      : wp.kw == 3 ? go_up(mla_up_kernel<8, 3>) : go_up(mla_up_kernel<8, 4>);
+  } else if (tm == 16) {
+    e = wp.kw == 1 ? go_up(mla_up_kernel<16, 1>) : go_up(mla_up_kernel<16, 2>);
+  } else {
+    e = go_up(mla_up_kernel<32, 1>);
+  }
   if (e != cudaSuccess) return DSA_ERR_CUDA;
 
   AbsParams A{};
   A.T = a.T; A.H = a.H; A.n_sums = a.T * (a.K_q + kDkv);
-  A.w_uk = reinterpret_cast<const __nv_bfloat16*>(a.w_uk); A.nope = nope; A.sums = sums;
+  A.w_uk = reinterpret_cast<const __nv_bfloat16*>(a.w_uk); A.up = up; A.sums = sums;
+  A.pos = a.pos; A.rope_cos = a.rope_cos; A.rope_sin = a.rope_sin;
+  A.max_pos = a.rope_max_pos; A.interleaved = a.rope_interleaved;
   A.q = reinterpret_cast<__nv_bfloat16*>(a.q); A.err = err;
   const size_t smem_abs = kAbsW + static_cast<size_t>(tm) * (kDn + kDc / 2) * sizeof(float);
   cudaLaunchConfig_t ca = cu;

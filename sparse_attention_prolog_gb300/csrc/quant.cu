@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
+#include "w8stream.cuh"
 
 namespace dsa {
 namespace {
@@ -74,96 +75,49 @@ __global__ void __launch_bounds__(kQThreads) act_quant_kernel(const uint16_t* __
 
 // ---------------------------------------------------------------- int8 GEMM
 // [V4-TileLang §Int8 General Matrix Multiplication] steps 1-4 for the
-// decode regime (M <= 32 activation rows): c[m, n] = fp16(sum_k a[m,k]
+// decode regime (M <= 8 activation rows): c[m, n] = fp16(sum_k a[m,k]
 // b[n,k] * a_scale[m] * b_scale[n]).  With so few rows every weight byte is
-// used at most 32 times, so the product is a weight stream (as the prolog's
-// q stream): a CTA owns 128 output channels, streams their rows of b and
-// the rows of a through a two-stage ring of 512-column chunks (2-D TMA
-// tiles of 128 bytes x rows, 128-byte swizzle, so the 16-byte reads of a
-// warp hit distinct banks), and accumulates exact int32 dp4a sums.
-constexpr int kGemmThreads = 256, kGemmCh = 128, kGemmKc = 512;
-constexpr uint32_t kGemmStageW = (kGemmKc / 128) * kGemmCh * 128;  // 64 KB
-constexpr uint32_t kGemmStageA = (kGemmKc / 128) * 32 * 128;       // 16 KB
+// used at most 8 times, so the product is a weight stream: the shared
+// weight-stream layout (w8stream.cuh), one CTA per SM over a contiguous
+// range of b's rows, a's rows in registers, exact int32 dp4a sums.
+// Two rows per warp at once; a's chunks of a lane in at most 64 registers.
+constexpr int kGemmRowsPerWarp = 2, kGemmARegs = 64;
 
-template <int TM>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    int8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                     const float* __restrict__ a_scale, const float* __restrict__ b_scale, __half* __restrict__ c,
-                     int M, int N, int K, uint32_t* err) {
+template <int MT, int KW>
+__global__ void __launch_bounds__(kW8Threads, 1)
+    int8_gemm_kernel(const W8Plan p, const int8_t* __restrict__ a, const float* __restrict__ a_scale,
+                     const int8_t* __restrict__ b, const float* __restrict__ b_scale, __half* __restrict__ c, int M,
+                     int N, int K, uint32_t* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[2];
+  __shared__ __align__(8) uint64_t full[kW8MaxStages], empty[kW8MaxStages];
   __shared__ int abort_flag;
-  constexpr int TPT = TM / 2;  // tokens per thread: t = half, half + 2, ...
-  const int tid = threadIdx.x;
-  const int ch = tid % kGemmCh, half = tid / kGemmCh;
-  const int n0 = blockIdx.x * kGemmCh;
-  const int nchunks = (K + kGemmKc - 1) / kGemmKc;
+  const W8Ring R{smem, full, empty, reinterpret_cast<int*>(smem + static_cast<size_t>(p.ns) * p.stage_bytes)};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int i = 0; i < p.ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kW8Consumers);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
+  for (int i = tid; i < 2 * p.sr * MT; i += kW8Threads) R.red[i] = 0;
   __syncthreads();
-  auto stage_w = [&](int s) { return smem + s * (kGemmStageW + kGemmStageA); };
-  auto issue = [&](int chunk) {  // columns past K and rows past M / N read as zero
-    const int s = chunk & 1;
-    uint8_t* w = stage_w(s);
-    uint8_t* x = w + kGemmStageW;
-    mbar_arrive_expect_tx(&full[s], kGemmStageW + kGemmStageA);
-#pragma unroll
-    for (int q = 0; q < kGemmKc / 128; ++q) {
-      tma_load_2d(w + q * (kGemmCh * 128), &tm_b, chunk * kGemmKc + q * 128, n0, &full[s]);
-      tma_load_2d(x + q * (32 * 128), &tm_a, chunk * kGemmKc + q * 128, 0, &full[s]);
-    }
+  int r0, r1;
+  w8_rows(N, blockIdx.x, gridDim.x, r0, r1);
+  if (warp == kW8Consumers) {
+    if (lane == 0) w8_produce(p, R, b, K, r0, r1, err, &abort_flag);
+    return;
+  }
+  const int nck = K / 16, cpw = (nck + p.wk - 1) / p.wk;
+  const int c0 = (warp % p.wk) * cpw, c1 = min(nck, c0 + cpw);
+  int4 areg[KW][MT];
+  w8_load_a<MT, KW>(areg, a, K, M, c0, c1, lane);
+  auto epi = [&](int t, int n, int v) {
+    c[static_cast<size_t>(t) * N + n] = __float2half_rn(static_cast<float>(v) * __ldg(a_scale + t) * __ldg(b_scale + n));
   };
-  if (tid == 0) {
-    issue(0);
-    if (nchunks > 1) issue(1);
-  }
-  int acc[TPT];
-#pragma unroll
-  for (int i = 0; i < TPT; ++i) acc[i] = 0;
-  const uint32_t csw = static_cast<uint32_t>(ch & 7);
-  for (int chunk = 0; chunk < nchunks; ++chunk) {
-    const int s = chunk & 1;
-    // every thread takes the same decision (the loop ends with a barrier)
-    if (!__syncthreads_and(mbar_wait(&full[s], (chunk >> 1) & 1, err, &abort_flag))) {
-      // chunks `chunk` and `chunk + 1` may still be in flight: let them
-      // land before the CTA leaves
-      if (tid == 0)
-        for (int j = chunk; j < nchunks && j < chunk + 2; ++j) mbar_drain(&full[j & 1], (j >> 1) & 1);
-      break;
-    }
-    const uint8_t* w = stage_w(s);
-    const uint8_t* x = w + kGemmStageW;
-#pragma unroll 2
-    for (int kk = 0; kk < kGemmKc / 16; ++kk) {
-      const int q = kk >> 3, j = kk & 7;
-      const int4 wv = *reinterpret_cast<const int4*>(w + q * (kGemmCh * 128) + ch * 128 + ((j ^ csw) << 4));
-#pragma unroll
-      for (int i = 0; i < TPT; ++i) {
-        const int t = half + 2 * i;  // token rows read by the whole warp (broadcast)
-        const int4 av = *reinterpret_cast<const int4*>(x + q * (32 * 128) + t * 128 + ((j ^ (t & 7)) << 4));
-        acc[i] = __dp4a(wv.x, av.x, acc[i]);
-        acc[i] = __dp4a(wv.y, av.y, acc[i]);
-        acc[i] = __dp4a(wv.z, av.z, acc[i]);
-        acc[i] = __dp4a(wv.w, av.w, acc[i]);
-      }
-    }
-    __syncthreads();  // every thread is done with stage s
-    if (tid == 0 && chunk + 2 < nchunks) issue(chunk + 2);
-  }
-  const int n = n0 + ch;
-  if (n < N && !abort_flag) {
-    const float sb = __ldg(b_scale + n);
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-      const int t = half + 2 * i;
-      if (t < M) c[static_cast<size_t>(t) * N + n] = __float2half_rn(static_cast<float>(acc[i]) * __ldg(a_scale + t) * sb);
-    }
-  }
+  w8_consume<MT, KW, kGemmRowsPerWarp>(p, R, areg, K, M, r0, r1, c0, c1, epi, err, &abort_flag);
 }
 
 // ---------------------------------------------------------------------- mHC
@@ -286,28 +240,25 @@ int launch_mhc(const dsa_mhc_args& a, cudaStream_t s) {
   return cuda_status(cudaGetLastError());
 }
 
+bool int8_gemm_stream_fits(int M, int K) { return M <= 8 && w8_plan(K, 8, kGemmARegs).kw > 0; }
+
 int launch_int8_gemm(const dsa_int8_gemm_args& a, cudaStream_t s) {
   uint32_t* err = error_word();
   if (!err) return DSA_ERR_CUDA;
-  alignas(64) CUtensorMap tm_a, tm_b;
-  const uint64_t da[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
-  const uint64_t db[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.N)};
-  const uint64_t st[1] = {static_cast<uint64_t>(a.K)};
-  const uint32_t ba[2] = {128, 32}, bb[2] = {128, static_cast<uint32_t>(kGemmCh)};
-  if (!encode_tmap(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.a, da, st, ba, 128) ||
-      !encode_tmap(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.b, db, st, bb, 128))
-    return DSA_ERR_CUDA;
-  const size_t smem = 1024 + 2 * static_cast<size_t>(kGemmStageW + kGemmStageA);
-  const dim3 grid((a.N + kGemmCh - 1) / kGemmCh);
+  constexpr int MT = 8;
+  const W8Plan p = w8_plan(a.K, MT, kGemmARegs);
+  if (p.kw == 0 || a.M > MT) return DSA_ERR_UNSUPPORTED;
+  const size_t smem = w8_smem(p, MT);
+  const int grid = a.N < sm_count() ? a.N : sm_count();
   auto go = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kGemmThreads, smem, s>>>(tm_a, tm_b, a.a_scale, a.b_scale, reinterpret_cast<__half*>(a.c), a.M, a.N,
-                                          a.K, err);
+    kern<<<grid, kW8Threads, smem, s>>>(p, a.a, a.a_scale, a.b, a.b_scale, reinterpret_cast<__half*>(a.c), a.M, a.N,
+                                         a.K, err);
     return cudaGetLastError();
   };
-  const cudaError_t e = a.M <= 8 ? go(int8_gemm_kernel<8>) : a.M <= 16 ? go(int8_gemm_kernel<16>)
-                                                                         : go(int8_gemm_kernel<32>);
+  cudaError_t e = cudaErrorInvalidValue;
+  e = p.kw == 1 ? go(int8_gemm_kernel<MT, 1>) : go(int8_gemm_kernel<MT, 2>);
   return cuda_status(e);
 }
 

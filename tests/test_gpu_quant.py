@@ -40,7 +40,13 @@ def test_act_quant_bit_exact(M, N, round_scale, cuda_lib):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (8, 8192, 1536), (1, 100, 16), (5, 300, 1008), (32, 256, 7168), (17, 129, 64),  # weight-stream path
+    (8, 8192, 1536), (1, 100, 16), (5, 300, 1008),  # weight stream: lanes split K, warps split the rows
+    (8, 2000, 8192),     # weight stream at its longest K (eight warps split K, sums meet in shared memory)
+    (6, 24576, 7168),    # the decode-size GEMM: eight warps split K, rows per SM differ by one
+    (3, 24576, 1536),    # the MLA up-projection's shape
+    (8, 300, 8208),      # K past the weight stream's registers: tensor cores
+    (12, 1000, 4096),    # more than 8 rows: tensor cores
+    (32, 256, 7168), (17, 129, 64),
     (33, 300, 1008),     # tensor cores: one ragged M tile, an N tail that is not a multiple of 8, K past a 64 stage
     (64, 8192, 1536),    # half an M tile, two 1024-K chunks
     (512, 8192, 1536),
