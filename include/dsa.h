@@ -88,9 +88,10 @@ int dsa_get_device_error(void* stream);
  * DSA_ERR_DEVICE_TIMEOUT (see dsa_get_device_error) and its CTA leaves its
  * loops, after letting the bulk copies and tensor-core operations it issued
  * finish (each such drain bounded by 4 s).  After a timed-out call, zero the
- * call's workspace again before the next one.  Limits below 20 us are
- * counted in SM clock cycles (two per nanosecond), longer ones on the global
- * timer.  Synchronous: it takes effect for kernels launched after it
+ * call's workspace again before the next one.  Waits are timed on the
+ * global timer, so a limit shorter than its tick (about 1 us) runs out at
+ * the first tick; under a limit below 20 us a wait never blocks in the
+ * hardware.  Synchronous: it takes effect for kernels launched after it
  * returns; call it while none of this library's kernels runs.  No
  * counterpart on the pages: a test hook. */
 int dsa_set_wait_limit_ns(uint64_t ns);
