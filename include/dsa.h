@@ -343,11 +343,12 @@ int dsa_act_quant(const dsa_act_quant_args* args, void* stream);
  *   c[m,n] = fp16( (sum_k a[m,k] * b[n,k]) * a_scale[m] * b_scale[n] )
  *
  * The int32 sum is exact; the dequantisation is fp32 (the product in the
- * order written), rounded once to fp16.  M <= 8 rows (decode tokens) with
- * K <= 8192 run as a weight stream on dp4a (one CTA per SM over a
- * contiguous range of b's rows); other shapes on the tensor cores (int8
- * converted exactly to f16, fp32 sums of at most 1024 products, added in
- * int32), with bit-identical results.
+ * order written), rounded once to fp16.  Both paths run on the tensor
+ * cores (int8 converted exactly to f16, fp32 sums of at most 1024
+ * products, added in int32) and give bit-identical results: up to 32 rows
+ * (decode tokens) a weight stream with b's rows as the MMA's M dimension
+ * and one CTA per SM over a contiguous range of them; more rows, tiles of
+ * 128 x 128.
  * Shapes: a int8 [M, K]; b int8 [N, K] (K-major, row n = output column n);
  * a_scale fp32 [M]; b_scale fp32 [N]; c fp16 [M, N].  a and b 16-byte
  * aligned.  Supported: 1 <= M <= 8388608, N >= 1, K a multiple of 16 up to

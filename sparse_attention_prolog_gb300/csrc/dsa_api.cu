@@ -346,13 +346,12 @@ int dsa_int8_gemm(const dsa_int8_gemm_args* a, void* stream) {
   if (bad_ptr(a->a, 16) || bad_ptr(a->b, 16) || bad_ptr(a->a_scale, 4) || bad_ptr(a->b_scale, 4) ||
       bad_ptr(a->c, 2))
     return DSA_ERR_INVALID_ARG;
-  // Up to 8 activation rows the GEMM is a weight stream (dp4a against the
-  // rows held in registers); beyond, a tensor-core GEMM.  Measured: at
-  // N = 8192, K = 1536 the stream takes 15.0 us for 1 to 8 rows against
-  // 19.1 us on the tensor cores (13 rows); at N = 24576, K = 7168, 84.6 us
-  // against 94.8 us; with 12 rows the stream is no faster than the tensor
-  // cores (19.1 vs 19.1 us; 41.6 vs 29.3 us at N = 24576, K = 1536).
-  if (a->M <= 8 && int8_gemm_stream_fits(a->M, a->K)) return launch_int8_gemm(*a, static_cast<cudaStream_t>(stream));
+  // Up to 32 activation rows the GEMM is a weight stream on the tensor cores
+  // (weights as the MMA's M, the rows of a as its N = 16 or 32); beyond, the
+  // tiled tensor-core GEMM.  Measured, 1 to 16 rows: 15.0 us at N = 8192,
+  // K = 1536 (tiled 19.1 us), 23.2 us at N = 24576, K = 1536 (tiled 29.3),
+  // 70.3 us at N = 24576, K = 7168 (tiled 94.8); 24 rows 17.0 / 25.2 / 76.4.
+  if (a->M <= 32) return launch_int8_gemm_wt(*a, static_cast<cudaStream_t>(stream));
   return launch_int8_gemm_tc(*a, static_cast<cudaStream_t>(stream));
 }
 

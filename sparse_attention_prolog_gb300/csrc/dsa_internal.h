@@ -68,9 +68,8 @@ int launch_topk(const dsa_topk_args& a, const float* scores, int64_t scores_ld, 
 size_t attn_workspace(const dsa_attn_args& a);
 int launch_attn(const dsa_attn_args& a, void* ws, cudaStream_t s);
 int launch_act_quant(const dsa_act_quant_args& a, cudaStream_t s);
-int launch_int8_gemm(const dsa_int8_gemm_args& a, cudaStream_t s);
-// The weight-stream path holds a's rows in registers: M <= 8, K <= 8192.
-bool int8_gemm_stream_fits(int M, int K);
+// The weight stream of the int8 GEMM on the tensor cores (M <= 32).
+int launch_int8_gemm_wt(const dsa_int8_gemm_args& a, cudaStream_t s);
 // The tensor-core path of the int8 GEMM (any M; exact int32 sums).
 int launch_int8_gemm_tc(const dsa_int8_gemm_args& a, cudaStream_t s);
 int launch_mhc(const dsa_mhc_args& a, cudaStream_t s);

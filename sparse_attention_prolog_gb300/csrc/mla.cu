@@ -15,13 +15,13 @@
 //               M = 128 channels, N = tokens padded to 16 or 32, fp32 in
 //               tensor memory) and adds its partial sums into the fp32
 //               workspace.
-//   mla_up      q_lora . w_uq^T as exact int32 dp4a sums on the weight-
-//               stream layout (w8stream.cuh): one CTA per SM over a
-//               contiguous range of w_uq's rows.  Each CTA normalises the
-//               query latent (RMSNorm) and quantises it per token from the
-//               sums (CTA 0 also writes q_lora), dequantises its rows' sums
-//               into the workspace, and writes the latent-cache rows of
-//               some tokens (RMSNorm of the KV latent, rotated rotary part).
+//   mla_up      q_lora . w_uq^T as exact int32 sums on the tensor-core
+//               weight stream (w8tc.cuh): one CTA per SM over a contiguous
+//               range of w_uq's rows.  Each CTA normalises the query latent
+//               (RMSNorm) and quantises it per token from the sums (CTA 0
+//               also writes q_lora), dequantises its rows' sums into the
+//               workspace, and writes the latent-cache rows of some tokens
+//               (RMSNorm of the KV latent, rotated rotary part).
 //   mla_absorb  q[:, h, c] = sum_n u_nope[:, h, n] w_uk[h, n, c]: one CTA per
 //               (head, half of the 512 latent dims), whose 64 KB of w_uk
 //               arrive by bulk copies issued before it waits for mla_up; the
@@ -37,7 +37,7 @@
 #include <cuda_bf16.h>
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
-#include "w8stream.cuh"
+#include "w8tc.cuh"
 
 namespace dsa {
 namespace {
@@ -266,60 +266,48 @@ __device__ __forceinline__ void kv_row(const UpParams& P, int t, int lane) {
   out[kDc + ib] = __float2bfloat16_rn(b * cs + a * sn);
 }
 
-// q_lora . w_uq^T on the weight-stream layout (w8stream.cuh): one CTA per
-// SM over a contiguous range of w_uq's H * 192 rows, the producer warp
-// streaming it from the kernel's start (the weights do not depend on
-// mla_down), the consumer warps waiting for mla_down's sums, quantising the
-// query latent of every token into shared memory and loading their chunks
-// of it into registers.  The sums are dequantised into the workspace `up`;
-// mla_absorb reads the no-position dims and rotates the rotary ones.
-template <int MT, int KW>
-__global__ void __launch_bounds__(kW8Threads, 1) mla_up_kernel(const __grid_constant__ UpParams P, const W8Plan p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kW8MaxStages], empty[kW8MaxStages];
-  __shared__ int abort_flag;
-  __shared__ float s_sa[MT];
-  const size_t ring = static_cast<size_t>(p.ns) * p.stage_bytes;
-  const W8Ring R{smem, full, empty, reinterpret_cast<int*>(smem + ring)};
-  int8_t* sA = reinterpret_cast<int8_t*>(smem + ring + 2 * static_cast<size_t>(p.sr) * MT * 4);  // [T][K_q] codes
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    for (int i = 0; i < p.ns; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kW8Consumers);
-    }
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  for (int i = tid; i < 2 * p.sr * MT; i += kW8Threads) R.red[i] = 0;
-  __syncthreads();
-  griddep_launch_dependents();
-  const int N = P.H * kDh;
-  int r0, r1;
-  w8_rows(N, blockIdx.x, gridDim.x, r0, r1);
-  if (warp == kW8Consumers) {
-    if (lane == 0) w8_produce(p, R, P.w_uq, P.K_q, r0, r1, P.err, &abort_flag);
-    return;
-  }
-  griddep_wait();  // the sums come from mla_down
-  for (int t = warp; t < P.T; t += kW8Consumers) {
-    const float sdiv = quant_latent(P, t, lane, sA, blockIdx.x == 0);
-    if (lane == 0) s_sa[t] = sdiv;
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");  // every token's codes and scale are in shared memory
-  const int nck = P.K_q / 16, cpw = (nck + p.wk - 1) / p.wk;
-  const int c0 = (warp % p.wk) * cpw, c1 = min(nck, c0 + cpw);
-  int4 areg[KW][MT];
-  w8_load_a<MT, KW>(areg, sA, P.K_q, P.T, c0, c1, lane);
-  auto epi = [&](int t, int n, int v) {
-    P.up[static_cast<size_t>(t) * N + n] = static_cast<float>(v) * s_sa[t] * __half2float(__ldg(P.w_uq_scale + n));
-  };
-  w8_consume<MT, KW, 1>(p, R, areg, P.K_q, P.T, r0, r1, c0, c1, epi, P.err, &abort_flag);
-  // latent KV rows: token t by consumer warp 0 of CTA t (mod the grid)
-  if (warp == 0)
-    for (int t = blockIdx.x; t < P.T; t += gridDim.x) kv_row(P, t, lane);
+// q_lora . w_uq^T on the tensor-core weight stream (w8tc.cuh): one CTA per
+// SM over a contiguous range of w_uq's H * 192 rows, whose copies start at
+// the kernel's start (the weights do not depend on mla_down).  The
+// converter warps first wait for mla_down's sums and quantise the query
+// latent of every token into the CTA's resident token tile (CTA 0 also
+// writes q_lora); the epilogue dequantises the sums of its rows into `up`:
+// up[t, n] = s * sa[t] * w_uq_scale[n], the product in that order.  After
+// the stream, warp 0 of CTA t (mod the grid) writes token t's latent row.
+__device__ __forceinline__ float* up_token_scales() {
+  __shared__ float sa[32];
+  return sa;
 }
+
+struct UpWtJob {
+  int M, N, K;
+  uint32_t* err;
+  UpParams P;
+  __device__ __forceinline__ void prologue(int w, int lane, int8_t* tok) const {
+    griddep_wait();  // the sums come from mla_down
+    float* sa = up_token_scales();
+    for (int t = w; t < P.T; t += 8) {
+      const float sdiv = quant_latent(P, t, lane, tok, blockIdx.x == 0);
+      if (lane == 0) sa[t] = sdiv;
+    }
+    // token rows past T are zero (the tile holds 16 or 32 rows)
+    const int nt = P.T <= 16 ? 16 : 32;
+    uint4* z = reinterpret_cast<uint4*>(tok + static_cast<size_t>(P.T) * P.K_q);
+    const int nz = (nt - P.T) * P.K_q / 16;
+    for (int i = w * 32 + lane; i < nz; i += 256) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ __forceinline__ float tok_scale(int t) const { return up_token_scales()[t]; }
+  __device__ __forceinline__ float row_scale(int n) const { return __half2float(__ldg(P.w_uq_scale + n)); }
+  __device__ __forceinline__ void put(int t, int n, int s, float st, float sn) const {
+    P.up[static_cast<size_t>(t) * N + n] = static_cast<float>(s) * st * sn;
+  }
+  __device__ __forceinline__ void tail(int warp, int lane) const {
+    if (warp == 0) {
+      griddep_wait();  // the latent sums come from mla_down
+      for (int t = blockIdx.x; t < P.T; t += gridDim.x) kv_row(P, t, lane);
+    }
+  }
+};
 
 // ---------------------------------------------------------------- absorb
 constexpr int kAbsThreads = 256;
@@ -470,6 +458,9 @@ int launch_mla(const dsa_mla_prolog_args& a, void* ws, cudaStream_t stream) {
   const size_t smem_down = 1024 + kDownStages * (kDownAtomW + static_cast<size_t>(nx) * 128);
   auto go_down = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_down));
+    // the SM keeps its full shared memory, so an mla_up CTA fits beside
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     kern<<<D.n_rb * n_split, kDownThreads, smem_down, stream>>>(D, tm_wdq, tm_wdkv, tm_x);
     return cudaGetLastError();
@@ -494,35 +485,40 @@ int launch_mla(const dsa_mla_prolog_args& a, void* ws, cudaStream_t stream) {
   U.up = up;
   U.kv_cache = reinterpret_cast<__nv_bfloat16*>(a.kv_cache); U.slot = a.slot; U.cache_rows = a.cache_rows;
   U.err = err;
-  // the ring takes what the codes of every token and the cross-warp sums
-  // leave of shared memory
-  const size_t codes = static_cast<size_t>(tm) * a.K_q;
-  const uint32_t ring_max =
-      static_cast<uint32_t>(220 * 1024 - 1024 - codes - 2 * static_cast<size_t>(kW8MaxStageRows) * tm * 4);
-  // a's chunks of a lane in up to 128 registers: at K_q = 1536 and 8 tokens
-  // the warps need not split K, so no stage waits for a cross-warp sum
-  const W8Plan wp = w8_plan(a.K_q, tm, 128, ring_max < kW8RingBytes ? ring_max : kW8RingBytes);
-  if (wp.kw == 0) return DSA_ERR_UNSUPPORTED;
-  const size_t smem_up = w8_smem(wp, tm) + codes;
+  const int nt = a.T <= 16 ? 16 : 32;
+  alignas(64) WtMaps maps;
+  {
+    const uint64_t st[1] = {static_cast<uint64_t>(a.K_q)};
+    const uint64_t dw[2] = {static_cast<uint64_t>(a.K_q), static_cast<uint64_t>(a.H) * kDh};
+    const uint32_t b128[2] = {kWtK, kWtRows}, b16[2] = {kWtK, kWtUnit};
+    if (!encode_tmap(&maps.w128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_uq, dw, st, b128, 128) ||
+        !encode_tmap(&maps.w16, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_uq, dw, st, b16, 128))
+      return DSA_ERR_CUDA;
+    maps.tok = maps.w16;  // unused: the tokens are resident
+  }
+  const UpWtJob job{a.T, a.H * kDh, a.K_q, err, U};
+  const long long units = (static_cast<long long>(a.H) * kDh + kWtUnit - 1) / kWtUnit;
   cudaLaunchConfig_t cu = {};
-  cu.gridDim = dim3(std::min(a.H * kDh, sm_count()));
-  cu.blockDim = dim3(kW8Threads);
-  cu.dynamicSmemBytes = smem_up;
+  cu.gridDim = dim3(static_cast<unsigned>(std::min<long long>(units, sm_count())));
+  cu.blockDim = dim3(kWtThreads);
   cu.stream = stream;
   cu.attrs = pdl;
   cu.numAttrs = 1;
-  auto go_up = [&](auto kern) {
-    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_up));
-    return r == cudaSuccess ? cudaLaunchKernelEx(&cu, kern, U, wp) : r;
+  // A ring small enough that an mla_up CTA fits beside an mla_down CTA on
+  // one SM: the up-projection's weights stream while mla_down runs.
+  const size_t budget = 228 * 1024 - 2048 - smem_down - 4096;
+  auto go_up = [&](auto kern, auto layout) {
+    using L = decltype(layout);
+    const int ns8 = L::stages(a.K_q, budget);
+    cu.dynamicSmemBytes = L::smem(a.K_q, ns8);
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(cu.dynamicSmemBytes));
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    return r == cudaSuccess ? cudaLaunchKernelEx(&cu, kern, maps, job, ns8) : r;
   };
-  if (tm == 8) {
-    e = wp.kw == 1 ? go_up(mla_up_kernel<8, 1>) : wp.kw == 2 ? go_up(mla_up_kernel<8, 2>)
-      : wp.kw == 3 ? go_up(mla_up_kernel<8, 3>) : go_up(mla_up_kernel<8, 4>);
-  } else if (tm == 16) {
-    e = wp.kw == 1 ? go_up(mla_up_kernel<16, 1>) : go_up(mla_up_kernel<16, 2>);
-  } else {
-    e = go_up(mla_up_kernel<32, 1>);
-  }
+  e = nt == 16 ? go_up(wt_kernel<16, true, UpWtJob>, WtLayout<16, true>{})
+               : go_up(wt_kernel<32, true, UpWtJob>, WtLayout<32, true>{});
   if (e != cudaSuccess) return DSA_ERR_CUDA;
 
   AbsParams A{};

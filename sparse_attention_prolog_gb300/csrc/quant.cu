@@ -14,7 +14,7 @@
 #include <cuda_fp16.h>
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
-#include "w8stream.cuh"
+#include "w8tc.cuh"
 
 namespace dsa {
 namespace {
@@ -71,53 +71,6 @@ __global__ void __launch_bounds__(kQThreads) act_quant_kernel(const uint16_t* __
     o.y = quant4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), s);
     __stcs(yr + i, o);
   }
-}
-
-// ---------------------------------------------------------------- int8 GEMM
-// [V4-TileLang §Int8 General Matrix Multiplication] steps 1-4 for the
-// decode regime (M <= 8 activation rows): c[m, n] = fp16(sum_k a[m,k]
-// b[n,k] * a_scale[m] * b_scale[n]).  With so few rows every weight byte is
-// used at most 8 times, so the product is a weight stream: the shared
-// weight-stream layout (w8stream.cuh), one CTA per SM over a contiguous
-// range of b's rows, a's rows in registers, exact int32 dp4a sums.
-// Two rows per warp at once; a's chunks of a lane in at most 64 registers.
-constexpr int kGemmRowsPerWarp = 2, kGemmARegs = 64;
-
-template <int MT, int KW>
-__global__ void __launch_bounds__(kW8Threads, 1)
-    int8_gemm_kernel(const W8Plan p, const int8_t* __restrict__ a, const float* __restrict__ a_scale,
-                     const int8_t* __restrict__ b, const float* __restrict__ b_scale, __half* __restrict__ c, int M,
-                     int N, int K, uint32_t* err) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kW8MaxStages], empty[kW8MaxStages];
-  __shared__ int abort_flag;
-  const W8Ring R{smem, full, empty, reinterpret_cast<int*>(smem + static_cast<size_t>(p.ns) * p.stage_bytes)};
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    for (int i = 0; i < p.ns; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kW8Consumers);
-    }
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  for (int i = tid; i < 2 * p.sr * MT; i += kW8Threads) R.red[i] = 0;
-  __syncthreads();
-  int r0, r1;
-  w8_rows(N, blockIdx.x, gridDim.x, r0, r1);
-  if (warp == kW8Consumers) {
-    if (lane == 0) w8_produce(p, R, b, K, r0, r1, err, &abort_flag);
-    return;
-  }
-  const int nck = K / 16, cpw = (nck + p.wk - 1) / p.wk;
-  const int c0 = (warp % p.wk) * cpw, c1 = min(nck, c0 + cpw);
-  int4 areg[KW][MT];
-  w8_load_a<MT, KW>(areg, a, K, M, c0, c1, lane);
-  auto epi = [&](int t, int n, int v) {
-    c[static_cast<size_t>(t) * N + n] = __float2half_rn(static_cast<float>(v) * __ldg(a_scale + t) * __ldg(b_scale + n));
-  };
-  w8_consume<MT, KW, kGemmRowsPerWarp>(p, R, areg, K, M, r0, r1, c0, c1, epi, err, &abort_flag);
 }
 
 // ---------------------------------------------------------------------- mHC
@@ -240,25 +193,62 @@ int launch_mhc(const dsa_mhc_args& a, cudaStream_t s) {
   return cuda_status(cudaGetLastError());
 }
 
-bool int8_gemm_stream_fits(int M, int K) { return M <= 8 && w8_plan(K, 8, kGemmARegs).kw > 0; }
+// ---------------------------------------------------------------- int8 GEMM
+// [V4-TileLang §Int8 General Matrix Multiplication] steps 1-4 for the
+// decode regime (M <= 32 activation rows): c[m, n] = fp16(sum_k a[m,k]
+// b[n,k] * a_scale[m] * b_scale[n]).  With so few rows every weight byte is
+// used at most 32 times, so the product is a weight stream, run on the
+// tensor cores with the weights as the MMA's M dimension (w8tc.cuh).
 
-int launch_int8_gemm(const dsa_int8_gemm_args& a, cudaStream_t s) {
+// c[t, n] = fp16(s * a_scale[t] * b_scale[n]), the product in that order.
+struct GemmWtJob {
+  int M, N, K;
+  uint32_t* err;
+  const float* a_scale;
+  const float* b_scale;
+  __half* c;
+  __device__ __forceinline__ float tok_scale(int t) const { return __ldg(a_scale + t); }
+  __device__ __forceinline__ float row_scale(int n) const { return __ldg(b_scale + n); }
+  __device__ __forceinline__ void put(int t, int n, int s, float st, float sn) const {
+    c[static_cast<size_t>(t) * N + n] = __float2half_rn(static_cast<float>(s) * st * sn);
+  }
+  __device__ __forceinline__ void prologue(int, int, int8_t*) const {}
+  __device__ __forceinline__ void tail(int, int) const {}
+};
+
+// Shared memory of the weight-stream GEMM: a ring of 8 raw stages with 16
+// tokens (12 stages measured no faster: 71.4 against 69.2 us at M = 8,
+// N = 24576, K = 7168).
+constexpr size_t kWtSmemBudget = 164 * 1024;
+
+int launch_int8_gemm_wt(const dsa_int8_gemm_args& a, cudaStream_t s) {
   uint32_t* err = error_word();
   if (!err) return DSA_ERR_CUDA;
-  constexpr int MT = 8;
-  const W8Plan p = w8_plan(a.K, MT, kGemmARegs);
-  if (p.kw == 0 || a.M > MT) return DSA_ERR_UNSUPPORTED;
-  const size_t smem = w8_smem(p, MT);
-  const int grid = a.N < sm_count() ? a.N : sm_count();
-  auto go = [&](auto kern) {
+  if (a.M > 32) return DSA_ERR_UNSUPPORTED;
+  const int NT = a.M <= 16 ? 16 : 32;
+  alignas(64) WtMaps maps;
+  const uint64_t st[1] = {static_cast<uint64_t>(a.K)};
+  const uint64_t db[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.N)};
+  const uint64_t da[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+  const uint32_t b128[2] = {kWtK, kWtRows}, b16[2] = {kWtK, kWtUnit}, bt[2] = {kWtK, static_cast<uint32_t>(NT)};
+  if (!encode_tmap(&maps.w128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.b, db, st, b128, 128) ||
+      !encode_tmap(&maps.w16, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.b, db, st, b16, 128) ||
+      !encode_tmap(&maps.tok, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.a, da, st, bt, 128))
+    return DSA_ERR_CUDA;
+  const GemmWtJob job{a.M, a.N, a.K, err, a.a_scale, a.b_scale, reinterpret_cast<__half*>(a.c)};
+  const long long units = (static_cast<long long>(a.N) + kWtUnit - 1) / kWtUnit;
+  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  auto go = [&](auto kern, auto layout) {
+    using L = decltype(layout);
+    const int ns8 = L::stages(a.K, kWtSmemBudget);
+    const size_t smem = L::smem(a.K, ns8);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kW8Threads, smem, s>>>(p, a.a, a.a_scale, a.b, a.b_scale, reinterpret_cast<__half*>(a.c), a.M, a.N,
-                                         a.K, err);
+    kern<<<grid, kWtThreads, smem, s>>>(maps, job, ns8);
     return cudaGetLastError();
   };
-  cudaError_t e = cudaErrorInvalidValue;
-  e = p.kw == 1 ? go(int8_gemm_kernel<MT, 1>) : go(int8_gemm_kernel<MT, 2>);
+  const cudaError_t e = NT == 16 ? go(wt_kernel<16, false, GemmWtJob>, WtLayout<16, false>{})
+                                 : go(wt_kernel<32, false, GemmWtJob>, WtLayout<32, false>{});
   return cuda_status(e);
 }
 

@@ -147,9 +147,10 @@ def test_wait_limit_runs_out_in_the_decode_step_then_next_step_passes(cuda_lib):
 
 
 def test_wait_limit_runs_out_in_the_mla_prolog_and_the_int8_gemm(cuda_lib):
-    """The MLA Prolog and the tensor-core int8 GEMM with a 1 ns limit report
-    a device timeout; with the default limit the next calls give the oracle's
-    q_lora codes and the exact GEMM."""
+    """The MLA Prolog and both int8 GEMM paths (512 rows: tiled; 8 rows: the
+    weight stream) with a 1 ns limit report a device timeout; with the
+    default limit the next calls give the oracle's q_lora codes and the
+    exact GEMMs."""
     from sparse_attention_prolog_gb300.pipeline import MlaBuffers
     T = 8
     p = W.make_mla_inputs(T, np.arange(T) * 5, np.arange(T, dtype=np.int64), seed=82, max_pos=64)
@@ -163,10 +164,12 @@ def test_wait_limit_runs_out_in_the_mla_prolog_and_the_int8_gemm(cuda_lib):
     ta, tb = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
     tsa, tsb = torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV)
     c = torch.zeros((M, N), dtype=torch.float16, device=DEV)
+    c8 = torch.zeros((8, N), dtype=torch.float16, device=DEV)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=DEV)
     torch.cuda.synchronize()
     assert B.device_error() == 0
-    for run in (lambda: mla.run(), lambda: B.dsa_int8_gemm(ta, tsa, tb, tsb, c)):
+    for run in (lambda: mla.run(), lambda: B.dsa_int8_gemm(ta, tsa, tb, tsb, c),
+                lambda: B.dsa_int8_gemm(ta[:8], tsa[:8], tb, tsb, c8)):
         B.set_wait_limit_ns(1)
         try:
             flush.zero_()
@@ -178,6 +181,7 @@ def test_wait_limit_runs_out_in_the_mla_prolog_and_the_int8_gemm(cuda_lib):
     mla.ws.zero_()
     mla.run()
     B.dsa_int8_gemm(ta, tsa, tb, tsb, c)
+    B.dsa_int8_gemm(ta[:8], tsa[:8], tb, tsb, c8)
     torch.cuda.synchronize()
     assert B.device_error() == 0
     ref = O.mla_prolog(p)
@@ -185,3 +189,4 @@ def test_wait_limit_runs_out_in_the_mla_prolog_and_the_int8_gemm(cuda_lib):
     want = O.int8_gemm(a, sa.astype(np.float64), b, sb.astype(np.float64)).astype(np.float64)
     got = c.cpu().numpy().astype(np.float64)
     assert (np.abs(got - want) <= np.maximum(np.abs(want) * 2.0 ** -10, 2.0 ** -24)).all()
+    np.testing.assert_array_equal(c8.cpu().numpy(), c.cpu().numpy()[:8])  # the two paths agree bit for bit

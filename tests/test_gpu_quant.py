@@ -40,13 +40,14 @@ def test_act_quant_bit_exact(M, N, round_scale, cuda_lib):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (8, 8192, 1536), (1, 100, 16), (5, 300, 1008),  # weight stream: lanes split K, warps split the rows
-    (8, 2000, 8192),     # weight stream at its longest K (eight warps split K, sums meet in shared memory)
-    (6, 24576, 7168),    # the decode-size GEMM: eight warps split K, rows per SM differ by one
+    (8, 8192, 1536),     # weight stream: 64 rows of 128 per SM (rows per SM differ by one 16-row unit)
+    (1, 100, 16),        # weight stream: a partial block only, one 16-column stage, columns past K zero
+    (5, 300, 1008),      # weight stream: K not a multiple of the 128-column stage
+    (8, 2000, 8208),     # weight stream: 65 stages, a 1024-K chunk left partial
+    (6, 24576, 7168),    # the decode-size GEMM: full and partial blocks per SM
     (3, 24576, 1536),    # the MLA up-projection's shape
-    (8, 300, 8208),      # K past the weight stream's registers: tensor cores
-    (12, 1000, 4096),    # more than 8 rows: tensor cores
-    (32, 256, 7168), (17, 129, 64),
+    (12, 1000, 4096), (16, 999, 512),  # 16 token rows: all of the MMA's N used
+    (32, 256, 7168), (17, 129, 64),    # 32 token rows (N = 32)
     (33, 300, 1008),     # tensor cores: one ragged M tile, an N tail that is not a multiple of 8, K past a 64 stage
     (64, 8192, 1536),    # half an M tile, two 1024-K chunks
     (512, 8192, 1536),
