@@ -488,13 +488,8 @@ int launch_mla(const dsa_mla_prolog_args& a, void* ws, cudaStream_t stream) {
   const int nt = a.T <= 16 ? 16 : 32;
   alignas(64) WtMaps maps;
   {
-    const uint64_t st[1] = {static_cast<uint64_t>(a.K_q)};
-    const uint64_t dw[2] = {static_cast<uint64_t>(a.K_q), static_cast<uint64_t>(a.H) * kDh};
-    const uint32_t b128[2] = {kWtK, kWtRows}, b16[2] = {kWtK, kWtUnit};
-    if (!encode_tmap(&maps.w128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_uq, dw, st, b128, 128) ||
-        !encode_tmap(&maps.w16, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_uq, dw, st, b16, 128))
-      return DSA_ERR_CUDA;
-    maps.tok = maps.w16;  // unused: the tokens are resident
+    if (!wt_encode_weights(maps, a.w_uq, a.H * kDh, a.K_q)) return DSA_ERR_CUDA;
+    maps.tok = maps.w[0];  // unused: the tokens are resident
   }
   const UpWtJob job{a.T, a.H * kDh, a.K_q, err, U};
   const long long units = (static_cast<long long>(a.H) * kDh + kWtUnit - 1) / kWtUnit;
