@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_tiles; ++j) {
         const long long row = row_next;
         if (j + 1 < n_tiles) row_next = gather_row(P, idx_row, b, slot_begin + (j + 1) * kRows, warp - 4, lane);
-        if (!mbar_wait(&bars.kempty[st], ph ^ 1, P.err, abort_v)) break;
+        if (!mbar_wait_polling<false>(&bars.kempty[st], ph ^ 1, P.err, abort_v)) break;
         gather_tile(P, row, sK + st * kStageK, kAtomsK, warp - 4, lane);
         // the stage's barrier counts this thread once its copies have landed
         cp_async_mbar_arrive(&bars.kfull[st]);
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_tiles; ++j) {
         const long long row = row_next;
         if (j + 1 < n_tiles) row_next = gather_row(P, idx_row, b, slot_begin + (j + 1) * kRows, warp - 4, lane);
-        if (!mbar_wait(&bars.vempty[st], ph ^ 1, P.err, abort_v)) break;
+        if (!mbar_wait_polling<false>(&bars.vempty[st], ph ^ 1, P.err, abort_v)) break;
         gather_tile(P, row, sV + st * kStageV, kAtomsV, warp - 4, lane);
         // the stage's barrier counts this thread once its copies have landed
         cp_async_mbar_arrive(&bars.vfull[st]);
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int s_lo = nx_lo, s_hi = nx_hi;
           if (j + 1 < n_tiles) load_idx(j + 1, nx_lo, nx_hi);
-          if (!mbar_wait(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
+          if (!mbar_wait_polling<false>(&bars.sfull[sb], phs, P.err, abort_v)) { ok = false; break; }
           const uint32_t v_lo = __ballot_sync(0xffffffffu, s_lo >= 0 && s_lo < P.max_L);
           const uint32_t v_hi = __ballot_sync(0xffffffffu, s_hi >= 0 && s_hi < P.max_L);
           tc_fence_after();
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           l_sum += lt;
           const int ps = j & 1;
-          if (!mbar_wait_cluster(&bars.pfree[ps], ((j >> 1) & 1) ^ 1, P.err, abort_v)) { ok = false; break; }
+          if (!mbar_wait_polling<true>(&bars.pfree[ps], ((j >> 1) & 1) ^ 1, P.err, abort_v)) { ok = false; break; }
           const uint32_t prow = remote_p + ps * kPSlot;
   #pragma unroll
           for (int c = 0; c < 8; ++c)
@@ -339,13 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int consumed = 0;  // odone phases observed
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int ps = j & 1;
-          if (!mbar_wait_cluster(&bars.pfull[ps], (j >> 1) & 1, P.err, abort_v)) { ok = false; break; }
+          if (!mbar_wait_polling<true>(&bars.pfull[ps], (j >> 1) & 1, P.err, abort_v)) { ok = false; break; }
           const float alpha = sAlpha[ps * 128 + hrow];
           const bool need = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
           if (need) {
             // O must hold PV of tile j-1 before it is rescaled.
             while (consumed < j) {
-              if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
+              if (!mbar_wait_polling<false>(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
               ++consumed;
             }
             if (!ok) break;
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&bars.ready[ps]);
           // keep at most one PV completion unobserved
           while (consumed < j) {
-            if (!mbar_wait(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
+            if (!mbar_wait_polling<false>(&bars.odone, consumed & 1, P.err, abort_v)) { ok = false; break; }
             ++consumed;
           }
         }
@@ -379,10 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
           int st = 0, sb = 0;
           uint32_t ph = 0, phs = 0;
-          if (n_tiles > 0 && mbar_wait(&bars.qready, 0, P.err, abort_v)) tc_fence_after();
+          if (n_tiles > 0 && mbar_wait_polling<false>(&bars.qready, 0, P.err, abort_v)) tc_fence_after();
           for (int j = 0; j < n_tiles; ++j) {
-            if (!mbar_wait(&bars.kfull[st], ph, P.err, abort_v)) break;
-            if (!mbar_wait(&bars.sempty[sb], phs ^ 1, P.err, abort_v)) break;
+            if (!mbar_wait_polling<false>(&bars.kfull[st], ph, P.err, abort_v)) break;
+            if (!mbar_wait_polling<false>(&bars.sempty[sb], phs ^ 1, P.err, abort_v)) break;
             fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
             tc_fence_after();
             const uint32_t base = smem_u32(sK + st * kStageK);
@@ -407,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ph = 0;
           for (int j = 0; j < n_tiles; ++j) {
             const int ps = j & 1;
-            if (!mbar_wait(&bars.vfull[st], ph, P.err, abort_v)) break;
-            if (!mbar_wait(&bars.ready[ps], (j >> 1) & 1, P.err, abort_v)) break;
+            if (!mbar_wait_polling<false>(&bars.vfull[st], ph, P.err, abort_v)) break;
+            if (!mbar_wait_polling<false>(&bars.ready[ps], (j >> 1) & 1, P.err, abort_v)) break;
             fence_proxy_async_smem();  // cp.async / st.async data -> tensor core reads
             tc_fence_after();
             const uint32_t pbase = smem_u32(sP + ps * kPSlot);
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t remote_pfree[2] = {mapa(smem_u32(&bars.pfree[0]), 0), mapa(smem_u32(&bars.pfree[1]), 0)};
           for (int j = 0; j + 2 < n_tiles; ++j) {
             const int ps = j & 1;
-            if (!mbar_wait(&bars.pcons[ps], (j >> 1) & 1, P.err, abort_v)) break;
+            if (!mbar_wait_polling<false>(&bars.pcons[ps], (j >> 1) & 1, P.err, abort_v)) break;
             mbar_arrive_expect_tx(&bars.pfull[ps], kPBytes);  // arm the slot's next use
             mbar_arrive_remote(remote_pfree[ps]);
           }
@@ -450,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // arrived: normalise, convert to bf16 into a swizzled staging tile (the
       // free V stages) and write it with TMA stores, 64 columns x 128 heads
       // per box (heads past H are clipped by the tensor map).
-      if (ok && n_tiles > 0) ok = mbar_wait(&bars.alldone, 0, P.err, abort_v);
-      if (ok) ok = mbar_wait_cluster(&bars.ffull, 0, P.err, abort_v);
+      if (ok && n_tiles > 0) ok = mbar_wait_polling<false>(&bars.alldone, 0, P.err, abort_v);
+      if (ok) ok = mbar_wait_polling<true>(&bars.ffull, 0, P.err, abort_v);
       tc_fence_after();
       const int hrow = (warp & 3) * 32 + lane;
       const int half = warp < 4 ? 0 : 1;  // columns [256 half, 256 half + 256)
