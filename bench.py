@@ -205,9 +205,11 @@ def src_hash(*names) -> str:
 
 
 def profiled_traffic(parts):
-    """Sum over (kernel source, summary) pairs of the dram read+write bytes
+    """Sum over (kernel sources, summary) pairs of the dram read+write bytes
     per launch in each committed ncu summary; None unless every summary
-    exists and was taken on the current source of its kernel."""
+    exists and was taken on the current sources of its kernel (a kernel's
+    sources are its .cu file and the headers it takes device code from,
+    joined by '+')."""
     total = 0.0
     for kernel_file, summary in parts:
         path = os.path.join(ROOT, "profiles", summary)
@@ -218,7 +220,7 @@ def profiled_traffic(parts):
             if ":" in line:
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-        if vals.get("source_sha256_16") != src_hash(kernel_file):
+        if vals.get("source_sha256_16") != src_hash(*kernel_file.split("+")):
             return None
         try:
             total += float(vals["traffic_bytes_per_launch"].split()[0])
@@ -467,9 +469,9 @@ def run_ours(args, rank, world, local):
     alg = {"prolog": prolog_bytes(p), "indexer+topk": indexer_bytes(inp) + topk_bytes(inp),
            "attention+combine": attention_bytes(inp, idx)}
     dom = max(alg, key=lambda k: st_ms[k])
-    kfile = {"prolog": [("prolog.cu", "prolog_decode64k.txt")],
-             "indexer+topk": [("indexer.cu", "indexer_decode64k.txt"), ("topk.cu", "topk_decode64k.txt")],
-             "attention+combine": [("attention.cu", "attention_decode64k.txt"), ("attention.cu", "combine_decode64k.txt")]}[dom]
+    kfile = {"prolog": [("prolog.cu+dsa_ptx.cuh", "prolog_decode64k.txt")],
+             "indexer+topk": [("indexer.cu+dsa_ptx.cuh", "indexer_decode64k.txt"), ("topk.cu+dsa_ptx.cuh", "topk_decode64k.txt")],
+             "attention+combine": [("attention.cu+dsa_ptx.cuh", "attention_decode64k.txt"), ("attention.cu+dsa_ptx.cuh", "combine_decode64k.txt")]}[dom]
     achieved = alg[dom] / (st_ms[dom] / 1e3) / 1e9
     step_bytes = sum(alg.values())
 
@@ -668,7 +670,7 @@ def prolog_config(args, dev, K):
         "roofline": {"bound": "hbm", "kernel": "prolog_kernel", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes": alg,
-                     "traffic": profiled_traffic([("prolog.cu", "prolog_alone_T8.txt")])},
+                     "traffic": profiled_traffic([("prolog.cu+dsa_ptx.cuh", "prolog_alone_T8.txt")])},
         "gpu_launches": K, "clocks": clocks,
     }
     if e2e_s is not None:
@@ -748,9 +750,9 @@ def prefill_config(args, dev, K):
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(stage[dom], 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(stage[dom] / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_flops": idx_ops if dom == "indexer+topk" else att_flop,
-                     "traffic": profiled_traffic([("indexer.cu", "indexer_prefill8192.txt"),
-                                                  ("topk.cu", "topk_prefill8192.txt")] if dom == "indexer+topk"
-                                                 else [("attention.cu", "attention_prefill8192.txt")])},
+                     "traffic": profiled_traffic([("indexer.cu+dsa_ptx.cuh", "indexer_prefill8192.txt"),
+                                                  ("topk.cu+dsa_ptx.cuh", "topk_prefill8192.txt")] if dom == "indexer+topk"
+                                                 else [("attention.cu+dsa_ptx.cuh", "attention_prefill8192.txt")])},
         "stage_roofline": {k: {"achieved_tflops": round(v, 1), "frac": round(v / peak, 4)} for k, v in stage.items()},
         "step_roofline": {"algorithmic_flops": idx_ops + att_flop, "achieved_tflops": round(step_tf, 1),
                           "frac": round(step_tf / peak, 4)},
@@ -869,10 +871,10 @@ def ragged_config(args, dev, K):
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes": alg[dom],
                      "traffic": profiled_traffic({
-                         "prolog": [("prolog.cu", "prolog_ragged32.txt")],
-                         "indexer+topk": [("indexer.cu", "indexer_ragged32.txt"), ("topk.cu", "topk_ragged32.txt")],
-                         "attention+combine": [("attention.cu", "attention_ragged32.txt"),
-                                               ("attention.cu", "combine_ragged32.txt")]}[dom])},
+                         "prolog": [("prolog.cu+dsa_ptx.cuh", "prolog_ragged32.txt")],
+                         "indexer+topk": [("indexer.cu+dsa_ptx.cuh", "indexer_ragged32.txt"), ("topk.cu+dsa_ptx.cuh", "topk_ragged32.txt")],
+                         "attention+combine": [("attention.cu+dsa_ptx.cuh", "attention_ragged32.txt"),
+                                               ("attention.cu+dsa_ptx.cuh", "combine_ragged32.txt")]}[dom])},
         "step_roofline": {"algorithmic_bytes": step_bytes, "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
                           "frac": round(step_bytes / (peak * 1e9) / (ms / 1e3), 4)},
         "stages_ms": {k: round(v, 5) for k, v in st_ms.items()}, "stages_timing": stage_timing,
@@ -995,12 +997,12 @@ def dia_config(args, dev, K):
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes": alg[dom],
                      "traffic": profiled_traffic({
-                         "mla_prolog": [("mla.cu", "mla_down_decode_T8.txt"), ("mla.cu", "mla_up_decode_T8.txt"),
-                                        ("mla.cu", "mla_absorb_decode_T8.txt")],
-                         "indexer_prolog": [("prolog.cu", "prolog_decode64k.txt")],
-                         "indexer+topk": [("indexer.cu", "indexer_decode64k.txt"), ("topk.cu", "topk_decode64k.txt")],
-                         "attention+combine": [("attention.cu", "attention_decode64k.txt"),
-                                               ("attention.cu", "combine_decode64k.txt")]}[dom])},
+                         "mla_prolog": [("mla.cu+w8tc.cuh+dsa_ptx.cuh", "mla_down_decode_T8.txt"), ("mla.cu+w8tc.cuh+dsa_ptx.cuh", "mla_up_decode_T8.txt"),
+                                        ("mla.cu+w8tc.cuh+dsa_ptx.cuh", "mla_absorb_decode_T8.txt")],
+                         "indexer_prolog": [("prolog.cu+dsa_ptx.cuh", "prolog_decode64k.txt")],
+                         "indexer+topk": [("indexer.cu+dsa_ptx.cuh", "indexer_decode64k.txt"), ("topk.cu+dsa_ptx.cuh", "topk_decode64k.txt")],
+                         "attention+combine": [("attention.cu+dsa_ptx.cuh", "attention_decode64k.txt"),
+                                               ("attention.cu+dsa_ptx.cuh", "combine_decode64k.txt")]}[dom])},
         "step_roofline": {"algorithmic_bytes": step_bytes, "roofline_us": round(step_bytes / (peak * 1e9) * 1e6, 3),
                           "frac": round(step_bytes / (peak * 1e9) / (ms / 1e3), 4)},
         "stages_ms": {k: round(v, 5) for k, v in st_ms.items()}, "stages_timing": stage_timing,
@@ -1166,7 +1168,7 @@ def run_act_quant(args):
                       "l2": "inputs larger than L2 (235 MB read per launch)"},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                        "traffic": profiled_traffic([("quant.cu", "act_quant_16384x7168.txt")])},
+                        "traffic": profiled_traffic([("quant.cu+w8tc.cuh+dsa_ptx.cuh", "act_quant_16384x7168.txt")])},
            "gpu_launches": K, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -1218,7 +1220,7 @@ def run_int8_gemm(args):
                                                    "l2": "weight larger than L2 (176 MB per launch)"},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                        "traffic": profiled_traffic([("quant.cu", "int8_gemm_8x24576x7168.txt")])},
+                        "traffic": profiled_traffic([("quant.cu+w8tc.cuh+dsa_ptx.cuh", "int8_gemm_8x24576x7168.txt")])},
            "gpu_launches": K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -1280,7 +1282,7 @@ def run_int8_gemm_tc(args):
            "config": {"workload": "int8_gemm M=4096 N=8192 K=1536", "l2": "3 rotating input sets (258 MB)"},
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
                         "frac": round(tf / peak, 4), "peak_kind": peak_kind, "algorithmic_flops": flops,
-                        "traffic": profiled_traffic([("gemm.cu", "int8_gemm_tc_4096x8192x1536.txt")])},
+                        "traffic": profiled_traffic([("gemm.cu+dsa_ptx.cuh", "int8_gemm_tc_4096x8192x1536.txt")])},
            "gpu_launches": K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = int8_gemm_tc_cpu_baseline(sets[0])
@@ -1338,7 +1340,7 @@ def run_mhc(args):
            "config": {"workload": "mhc n=1048576 hc=4 iters=20", "l2": "inputs larger than L2 (201 MB per launch)"},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                        "traffic": profiled_traffic([("quant.cu", "mhc_1048576x4.txt")])},
+                        "traffic": profiled_traffic([("quant.cu+w8tc.cuh+dsa_ptx.cuh", "mhc_1048576x4.txt")])},
            "gpu_launches": K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
@@ -1395,9 +1397,9 @@ def run_mla(args):
                       "bytes_per_call": nbytes},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                        "traffic": profiled_traffic([("mla.cu", "mla_down_decode_T8.txt"),
-                                                     ("mla.cu", "mla_up_decode_T8.txt"),
-                                                     ("mla.cu", "mla_absorb_decode_T8.txt")])},
+                        "traffic": profiled_traffic([("mla.cu+w8tc.cuh+dsa_ptx.cuh", "mla_down_decode_T8.txt"),
+                                                     ("mla.cu+w8tc.cuh+dsa_ptx.cuh", "mla_up_decode_T8.txt"),
+                                                     ("mla.cu+w8tc.cuh+dsa_ptx.cuh", "mla_absorb_decode_T8.txt")])},
            "gpu_launches": 3 * K_steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
         import oracle as O
