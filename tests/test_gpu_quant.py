@@ -47,6 +47,8 @@ def test_act_quant_bit_exact(M, N, round_scale, cuda_lib):
     (6, 24576, 7168),    # the decode-size GEMM: full and partial blocks per SM
     (3, 24576, 1536),    # the MLA up-projection's shape
     (12, 1000, 4096), (16, 999, 512),  # 16 token rows: all of the MMA's N used
+    (8, 300, 65536),     # weight stream at the longest K: 64 exact 1024-K chunks
+    (2, 40000, 256),     # weight stream: 256 or 272 rows per SM, a full super-block and a 16-row one
     (32, 256, 7168), (17, 129, 64),    # 32 token rows (N = 32)
     (33, 300, 1008),     # tensor cores: one ragged M tile, an N tail that is not a multiple of 8, K past a 64 stage
     (64, 8192, 1536),    # half an M tile, two 1024-K chunks
