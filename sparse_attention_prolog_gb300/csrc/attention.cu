@@ -243,6 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t remote_final = mapa(smem_u32(sFinal), 1);
         const uint32_t remote_pfull[2] = {mapa(smem_u32(&bars.pfull[0]), 1), mapa(smem_u32(&bars.pfull[1]), 1)};
         const uint32_t remote_ffull = mapa(smem_u32(&bars.ffull), 1);
+        // The pairs of the first half of the tokens start first (lowest block
+        // indices); each pulls its slice of the query of token t + T/2 into
+        // L2 for the pairs that may start only when SMs free up.
+        if (P.n_chunks > 1 && t < P.T / 2 && hrow == 0) {
+          const int t2 = t + P.T / 2;
+          const int per = (q_rows + P.n_chunks - 1) / P.n_chunks;
+          const int h0 = chunk * per, nh = min(per, q_rows - h0);
+          if (nh > 0) prefetch_l2(P.q + (static_cast<size_t>(t2) * P.H + hb * 128 + h0) * kDqk, nh * kDqk * 2);
+        }
         // q row of this thread's head: global -> registers -> TMEM columns
         // [0, 288), three atoms (24 independent 16-byte loads) per round.
         {
