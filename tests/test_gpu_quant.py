@@ -105,3 +105,42 @@ def test_int8_gemm_sums_are_exact_past_fp32_precision(M, cuda_lib):
     assert np.abs(exact).max() < 2048  # exactly representable in fp16
     assert (np.abs(np.cumsum(a[0].astype(np.int64) * 127)) > 2 ** 24).any()  # the running sum passes 2^24
     np.testing.assert_array_equal(c.cpu().numpy().astype(np.int64), exact)
+
+
+def test_int8_gemm_random_shapes_and_paths_agree(cuda_lib):
+    """Seeded random shapes on both paths (up to 32 rows the weight stream,
+    above the tiled GEMM): exact sums against the oracle, and the first 32
+    rows of a 33-row call (tiled) equal a 32-row call (weight stream) bit
+    for bit."""
+    r = np.random.default_rng(2024)
+    for _ in range(12):
+        M = int(r.integers(1, 41))
+        N = int(r.integers(1, 3000))
+        K = 16 * int(r.integers(1, 257))
+        a = r.integers(-128, 128, (M, K)).astype(np.int8)
+        b = r.integers(-128, 128, (N, K)).astype(np.int8)
+        sa = r.uniform(0.5, 2.0, M).astype(np.float32) * np.float32(1.0 / 128)
+        sb = r.uniform(0.5, 2.0, N).astype(np.float32) / np.float32(128 * max(K, 64) ** 0.5)
+        c = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+        B.dsa_int8_gemm(torch.from_numpy(a).to(DEV), torch.from_numpy(sa).to(DEV), torch.from_numpy(b).to(DEV),
+                        torch.from_numpy(sb).to(DEV), c)
+        torch.cuda.synchronize()
+        assert B.device_error() == 0
+        ref = O.int8_gemm(a, sa.astype(np.float64), b, sb.astype(np.float64)).astype(np.float64)
+        got = c.cpu().numpy().astype(np.float64)
+        ulp = np.maximum(np.abs(ref) * 2.0 ** -10, 2.0 ** -24)
+        assert (np.abs(got - ref) <= ulp).all(), f"M={M} N={N} K={K}"
+    M, N, K = 33, 777, 1040
+    a = r.integers(-128, 128, (M, K)).astype(np.int8)
+    b = r.integers(-128, 128, (N, K)).astype(np.int8)
+    sa = r.uniform(0.5, 2.0, M).astype(np.float32)
+    sb = r.uniform(0.5, 2.0, N).astype(np.float32) / np.float32(128 * 128)
+    ta, tb = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    tsa, tsb = torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV)
+    c33 = torch.empty((33, N), dtype=torch.float16, device=DEV)
+    c32 = torch.empty((32, N), dtype=torch.float16, device=DEV)
+    B.dsa_int8_gemm(ta, tsa, tb, tsb, c33)
+    B.dsa_int8_gemm(ta[:32].contiguous(), tsa[:32].contiguous(), tb, tsb, c32)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    np.testing.assert_array_equal(c32.cpu().numpy(), c33.cpu().numpy()[:32])
