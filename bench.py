@@ -6,8 +6,9 @@ top-k -> sparse MLA attention, B=4 sequences, MTP1 (2 query tokens each),
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is whole-job query tokens per
-second measured on the device (CUDA events on the launching stream, one CUDA
-graph per step, max over ranks).  By default the steps rotate over 4
+second measured on the device (one CUDA graph per step, K graphs replayed back
+to back between one pair of CUDA events on the launching stream, max over
+ranks).  By default the steps rotate over 4
 independent device copies of every input (caches, weights, queries; about
 1.4 GB), so no step finds its inputs in the 126 MB L2 left by the steps
 before it; `--l2 flush` instead writes 256 MiB before every step (which also
@@ -288,11 +289,14 @@ def stage_times_separate(stage_fns_per_set, stream, prep, reps):
 
 
 def time_replays(graphs, K, stream, prep, dev):
-    """Mean ms of K replays of graphs[k % len(graphs)] (CUDA events on the
-    launching stream around each replay, a barrier and a synchronize on both
-    sides of the timed region), and the clocks of a loaded window around it:
-    untimed replays of the same graphs run just before and after the timed
-    ones, so that the 20 ms clock poll sees the region however short it is."""
+    """ms per step of K replays of graphs[k % len(graphs)], with a barrier and
+    a synchronize on both sides of the timed region, and the clocks of a
+    loaded window around it: untimed replays of the same graphs run just
+    before and after the timed ones, so that the 20 ms clock poll sees the
+    region however short it is.  Without `prep` the K replays run back to
+    back between one pair of CUDA events on the launching stream (total / K);
+    with it (an L2 flush before every step), events around each replay keep
+    the flush outside the timed region and the mean is returned."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -309,7 +313,8 @@ def time_replays(graphs, K, stream, prep, dev):
     def soak(n):
         with torch.cuda.stream(stream):
             for w in range(n):
-                prep()
+                if prep is not None:
+                    prep()
                 graphs[w % len(graphs)].replay()
 
     with ClockSampler(device_uuid(dev)) as clk:
@@ -317,16 +322,25 @@ def time_replays(graphs, K, stream, prep, dev):
         D.barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            for k in range(K):
-                prep()
-                starts[k].record(stream)
-                graphs[k % len(graphs)].replay()
-                ends[k].record(stream)
+            if prep is None:
+                a.record(stream)
+                for k in range(K):
+                    graphs[k % len(graphs)].replay()
+                b.record(stream)
+            else:
+                for k in range(K):
+                    prep()
+                    starts[k].record(stream)
+                    graphs[k % len(graphs)].replay()
+                    ends[k].record(stream)
         torch.cuda.synchronize()
         D.barrier()
         soak(soak_post)
         torch.cuda.synchronize()
-    ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+    if prep is None:
+        ms = a.elapsed_time(b) / K
+    else:
+        ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
     clocks = clk.summary()
     clocks["window"] = (f"the {K} timed steps with {soak_pre} untimed replays of the same step graphs before "
                         f"and {soak_post} after them (one loaded window, sampled every {ClockSampler.PERIOD_MS} ms)")
@@ -450,7 +464,7 @@ def run_ours(args, rank, world, local):
     stream.synchronize()
 
     K = args.steps
-    ms, clocks = time_replays(graphs, K, stream, prep, dev)
+    ms, clocks = time_replays(graphs, K, stream, prep if flush is not None else None, dev)
     ms_max = D.max_over_ranks(ms, dev)
     tokens_total = D.sum_over_ranks(inp.T, dev)
     value = tokens_total / (ms_max / 1e3)
@@ -571,7 +585,9 @@ def run_ours(args, rank, world, local):
                    "l2": (f"inputs larger than L2: {len(sets)} rotating device copies of every input "
                           f"({len(sets) * 0.36:.1f} GB), no flush" if args.l2 == "rotate"
                           else "flushed before every timed step (256 MiB write, outside the events)"),
-                   "timing": "one CUDA graph per step, CUDA events on its stream", "parallelism": f"replicas x{world}"},
+                   "timing": ("one CUDA graph per step, K replays back to back between one pair of CUDA events on its "
+                              "stream" if flush is None else "one CUDA graph per step, CUDA events around each "
+                              "replay (the flush before it outside)"), "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes": alg[dom],
@@ -632,7 +648,7 @@ def prolog_config(args, dev, K):
     if B.device_error() != 0:
         raise RuntimeError("device-side error in the prolog warm-up")
     graphs = [capture(pr.run, stream) for pr in sets]
-    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    ms, clocks = time_replays(graphs, K, stream, None, dev)
     peak, peak_kind = measured_peaks()
     alg = prolog_bytes(p)
     achieved = alg / (ms / 1e3) / 1e9
@@ -712,7 +728,7 @@ def prefill_config(args, dev, K):
     if B.device_error() != 0:
         raise RuntimeError("device-side error in the prefill warm-up")
     graphs = [capture(buf.run, stream)]
-    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    ms, clocks = time_replays(graphs, K, stream, None, dev)
     st_ms, stage_timing = stage_times_in_graph([[("indexer+topk", buf.run_topk), ("attention", buf.run_attn)]],
                                                stream, lambda: None, max(K, 3))
     if st_ms is None:
@@ -828,7 +844,7 @@ def ragged_config(args, dev, K):
     if B.device_error() != 0:
         raise RuntimeError("device-side error in the ragged warm-up")
     graphs = [capture(step, stream)]
-    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    ms, clocks = time_replays(graphs, K, stream, None, dev)
     fns = [[("prolog", pro.run), ("indexer+topk", buf.run_topk), ("attention+combine", buf.run_attn)]]
     st_ms, stage_timing = stage_times_in_graph(fns, stream, lambda: None, min(max(K, 5), 50))
     if st_ms is None:
@@ -945,7 +961,7 @@ def dia_config(args, dev, K):
     if B.device_error() != 0:
         raise RuntimeError("device-side error in the DIA warm-up")
     graphs = [capture(st.run, stream) for st in sets]
-    ms, clocks = time_replays(graphs, K, stream, lambda: None, dev)
+    ms, clocks = time_replays(graphs, K, stream, None, dev)
     fns = [[("mla_prolog", st.mla.run), ("indexer_prolog", st.pro.run), ("indexer+topk", st.buf.run_topk),
             ("attention+combine", st.buf.run_attn)] for st in sets]
     reps = min(max(K, 5), 50)
