@@ -418,22 +418,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_group = false;
         const Group G = group_of(P, grp, g);
         const int rows_real = G.ntok * P.H_I;
-        for (int task = ct; task < N * chunks; task += 128) {
-          const int n = task / chunks, c = task % chunks;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (n < rows_real) {
-            const int8_t* src = P.q + (static_cast<size_t>(G.t0) * P.H_I + n) * d_I + c * 16;
-            v = __ldg(reinterpret_cast<const uint4*>(src));
+        // in batches of 8 chunks per thread, every load of a batch issued
+        // before any is used
+        constexpr int kQBatch = 8;
+        for (int b0 = ct; b0 < N * chunks; b0 += 128 * kQBatch) {
+          uint4 qv[kQBatch];
+#pragma unroll
+          for (int i = 0; i < kQBatch; ++i) {
+            const int task = b0 + i * 128;
+            const int n = task / chunks, c = task % chunks;
+            qv[i] = make_uint4(0, 0, 0, 0);
+            if (task < N * chunks && n < rows_real)
+              qv[i] = __ldg(reinterpret_cast<const uint4*>(P.q + (static_cast<size_t>(G.t0) * P.H_I + n) * d_I + c * 16));
           }
-          uint32_t f[8];
-          i8x4_to_f16x4(v.x, f[0], f[1]);
-          i8x4_to_f16x4(v.y, f[2], f[3]);
-          i8x4_to_f16x4(v.z, f[4], f[5]);
-          i8x4_to_f16x4(v.w, f[6], f[7]);
-          uint8_t* atom = sQ + (c / 4) * (N * 128);
-          const int cc = (c % 4) * 2;
-          *reinterpret_cast<uint4*>(atom + sw128_off(n, cc)) = make_uint4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<uint4*>(atom + sw128_off(n, cc + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+          for (int i = 0; i < kQBatch; ++i) {
+            const int task = b0 + i * 128;
+            if (task >= N * chunks) break;
+            const int n = task / chunks, c = task % chunks;
+            uint32_t f[8];
+            i8x4_to_f16x4(qv[i].x, f[0], f[1]);
+            i8x4_to_f16x4(qv[i].y, f[2], f[3]);
+            i8x4_to_f16x4(qv[i].z, f[4], f[5]);
+            i8x4_to_f16x4(qv[i].w, f[6], f[7]);
+            uint8_t* atom = sQ + (c / 4) * (N * 128);
+            const int cc = (c % 4) * 2;
+            *reinterpret_cast<uint4*>(atom + sw128_off(n, cc)) = make_uint4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<uint4*>(atom + sw128_off(n, cc + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
