@@ -452,9 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
   }
   const uint32_t ub = static_cast<uint32_t>(B);
   const uint32_t cnt0 = mapa(smem_u32(cnt), 0);
-  auto zero_hist_slice = [&]() {  // once every CTA has read the histogram
-    const int h0 = static_cast<int>(rank) * kHB / static_cast<int>(ncta);
-    const int h1 = static_cast<int>(rank + 1) * kHB / static_cast<int>(ncta);
+  // Once every CTA has read the histogram: the CTAs other than CTA 0 clear
+  // it (CTA 0 goes on with the candidates), CTA 0 alone when it has no peer.
+  auto zero_hist_slice = [&]() {
+    const int nz = ncta > 1 ? static_cast<int>(ncta) - 1 : 1;
+    const int z = ncta > 1 ? static_cast<int>(rank) - 1 : 0;
+    if (z < 0) return;
+    const int h0 = z * kHB / nz, h1 = (z + 1) * kHB / nz;
     for (int i = h0 + tid; i < h1; i += kThreads) hist[i] = 0;
   };
   cluster_wait();
