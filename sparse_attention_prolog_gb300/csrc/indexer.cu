@@ -55,6 +55,12 @@ constexpr int kStages16 = 3;  // converted f16 key tiles (in TMEM)
 constexpr int kThreads = 448;  // 14 warps, see the role map above
 constexpr int kMaxG = 32;     // tokens per group
 constexpr int kCoef = 256;    // max query rows (N) of a group
+// Cost of a group change, in tiles, in the split of the work over CTAs: the
+// group's queries are staged and its head weights loaded while no tile is
+// scored (measured on a causal prefill: a group's first tile takes about
+// two tiles' time longer than the others).
+constexpr int kGroupCost = 2;
+constexpr int kGroupCostMinGroups = 64;
 constexpr int kHistBins = 4096;  // leading 12 bits of the score's order key
 
 struct IdxParams {
@@ -107,6 +113,18 @@ __device__ __forceinline__ Group group_of(const IdxParams& P, const uint16_t* gr
   for (int i = 0; i < G.ntok; ++i) m = max(m, __ldg(P.pos + G.t0 + i));
   G.maxpos = min(m, P.max_L - 1);
   return G;
+}
+
+// First token and token count of group g (no global loads).
+__device__ __forceinline__ void group_tokens(const IdxParams& P, const uint16_t* grp, int g, int& t0, int& ntok) {
+  if (grp != nullptr) {
+    t0 = grp[g];
+    ntok = grp[g + 1] - t0;
+  } else {
+    const int b = g / P.groups_per_seq, gj = g % P.groups_per_seq;
+    t0 = b * P.n_q + gj * P.G;
+    ntok = min(P.G, P.n_q - gj * P.G);
+  }
 }
 
 // Work list: the active tiles (tiles holding at least one visible key) of
@@ -240,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [n_groups + 1] tile prefix, then (token map only) the group table
   int* tiles_prefix = reinterpret_cast<int*>(sQ + static_cast<size_t>(N) * DI * 2);
   uint16_t* grp = P.seq != nullptr ? reinterpret_cast<uint16_t*>(tiles_prefix + P.n_groups + 1) : nullptr;
+  // [n_groups + 1] prefix of the work's cost: scratch in the key ring, which
+  // no copy writes before the setup below is done
+  int* cost_prefix = reinterpret_cast<int*>(smem);
   __shared__ Bars bars;
   // fp16 key scales of each ring stage, copied with its key tile.
   __shared__ __align__(16) unsigned short ks_s[kStages8][kTileKeys];
@@ -247,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   __shared__ __align__(16) float coef[kCoef];
   __shared__ int tok_pos[kMaxG];
-  __shared__ int scan_tmp[kThreads / 32];
+  __shared__ int scan_tmp[kThreads / 32], scan_tmp2[kThreads / 32];
   // Per-token histogram of each visible score's leading 12 key bits (groups
   // of at most two tokens, H_I >= 64); flushed to global memory at every
   // group change so the top-k pass can find its threshold digit at once.
@@ -295,33 +316,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The group table of a token map (uniform batches need none), then the
   // per-group tile counts and their exclusive prefix (block-wide scan).
   const int ngroups = grp != nullptr ? build_groups<kThreads>(P, grp, scan_tmp) : P.n_groups;
+  // Group changes weigh in the split only when groups are many and short
+  // (a prefill); a decode's few long groups split by tiles alone.
+  const int group_cost = ngroups > kGroupCostMinGroups ? kGroupCost : 0;
   {
     const int ng = ngroups;
     const int per = (ng + kThreads - 1) / kThreads;
     const int g0 = min(ng, tid * per), g1 = min(ng, g0 + per);
-    int local = 0;
-    for (int g = g0; g < g1; ++g) local += group_tiles(P, grp, g);
-    int incl = local;
+    int local = 0, lcost = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int tg = group_tiles(P, grp, g);
+      local += tg;
+      lcost += tg > 0 ? tg + group_cost : 0;
+    }
+    int incl = local, cincl = lcost;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
+      const int c = __shfl_up_sync(0xffffffffu, cincl, o);
+      if (lane >= o) { incl += n; cincl += c; }
     }
-    if (lane == 31) scan_tmp[warp] = incl;
+    if (lane == 31) { scan_tmp[warp] = incl; scan_tmp2[warp] = cincl; }
     __syncthreads();
-    int woff = 0;
-    for (int w2 = 0; w2 < warp; ++w2) woff += scan_tmp[w2];
-    int run = woff + incl - local;
+    int woff = 0, cwoff = 0;
+    for (int w2 = 0; w2 < warp; ++w2) { woff += scan_tmp[w2]; cwoff += scan_tmp2[w2]; }
+    int run = woff + incl - local, crun = cwoff + cincl - lcost;
     for (int g = g0; g < g1; ++g) {
       tiles_prefix[g] = run;
-      run += group_tiles(P, grp, g);
+      if (group_cost > 0) cost_prefix[g] = crun;
+      const int tg = group_tiles(P, grp, g);
+      run += tg;
+      crun += tg > 0 ? tg + group_cost : 0;
     }
-    if (tid == kThreads - 1) tiles_prefix[ng] = run;
+    if (tid == kThreads - 1) {
+      tiles_prefix[ng] = run;
+      if (group_cost > 0) cost_prefix[ng] = crun;
+    }
     __syncthreads();
   }
-  const int total_items = tiles_prefix[ngroups];
-  const int item_lo = static_cast<int>((static_cast<long long>(total_items) * blockIdx.x) / gridDim.x);
-  const int item_hi = static_cast<int>((static_cast<long long>(total_items) * (blockIdx.x + 1)) / gridDim.x);
+  // Equal shares of the work's cost, as tile ranges: tile j of group g sits
+  // at cost position cost_prefix[g] + group_cost + j, and a CTA takes the
+  // tiles whose positions fall in its share.
+  auto tiles_below = [&](long long u) -> int {  // tiles at positions below u
+    int lo = 0, hi = ngroups;  // largest g with cost_prefix[g] <= u
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cost_prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    const long long in_g = u - cost_prefix[lo] - group_cost;
+    const int tg = tiles_prefix[lo + 1] - tiles_prefix[lo];
+    return tiles_prefix[lo] + static_cast<int>(in_g < 0 ? 0 : (in_g > tg ? tg : in_g));
+  };
+  const long long total_cost = group_cost > 0 ? cost_prefix[ngroups] : tiles_prefix[ngroups];
+  const long long u_lo = total_cost * blockIdx.x / gridDim.x, u_hi = total_cost * (blockIdx.x + 1) / gridDim.x;
+  const int item_lo = group_cost > 0 ? tiles_below(u_lo) : static_cast<int>(u_lo);
+  const int item_hi = group_cost > 0 ? tiles_below(u_hi) : static_cast<int>(u_hi);
   // First (group, tile) of this CTA's share: binary search in the prefix.
   Walker w0{0, 0, item_hi - item_lo};
   {
@@ -450,6 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.qfull);
+        // the next group of this CTA's share: its q rows into L2 now, so that
+        // its staging at the next group change reads L2, not DRAM
+        if (ct == 0 && g + 1 < ngroups && tiles_prefix[g + 1] < item_hi) {
+          int tn, nn;
+          group_tokens(P, grp, g + 1, tn, nn);
+          prefetch_l2(P.q + static_cast<size_t>(tn) * P.H_I * d_I, static_cast<uint32_t>(nn * P.H_I * d_I));
+        }
       }
       if (!mbar_wait(&bars.full8[st8], ph8, P.err, abort_v)) break;
       if (!mbar_wait(&bars.empty16[st16], ph16 ^ 1, P.err, abort_v)) break;
@@ -588,6 +644,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           coef[n] = c;
         }
         for (int gi = et; gi < kMaxG; gi += 256) tok_pos[gi] = (gi < G.ntok) ? __ldg(P.pos + G.t0 + gi) : -1;
+        if (g + 1 < ngroups && tiles_prefix[g + 1] < item_hi) {  // the next group's weights, into L2
+          int tn, nn;
+          group_tokens(P, grp, g + 1, tn, nn);
+          const char* wb = reinterpret_cast<const char*>(P.w + static_cast<size_t>(tn) * P.H_I);
+          const char* sb = reinterpret_cast<const char*>(P.q_scale + static_cast<size_t>(tn) * P.H_I);
+          const int wl = nn * P.H_I * 4, sl = nn * P.H_I * 2;
+          if (et * 128 < wl) prefetch_line_l2(wb + et * 128);
+          if (et * 128 < sl) prefetch_line_l2(sb + et * 128);
+        }
         if (!ep_sync()) return false;
       }
       if (!mbar_wait(&bars.tfull[acc], aph, P.err, abort_v)) return false;
