@@ -115,6 +115,11 @@ __device__ __forceinline__ Group group_of(const IdxParams& P, const uint16_t* gr
   return G;
 }
 
+// Hint: bring the cache line holding `p` into L2.
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // First token and token count of group g (no global loads).
 __device__ __forceinline__ void group_tokens(const IdxParams& P, const uint16_t* grp, int g, int& t0, int& ntok) {
   if (grp != nullptr) {
