@@ -87,6 +87,7 @@ struct __align__(8) Bars {
   uint64_t ready[2], odone, ffull;              // CTA 1 correction / MMA
   uint64_t alldone;                             // CTA 1: every PV MMA complete
   uint64_t qready;                              // CTA 0: q is in TMEM
+  uint64_t tiles;                               // the chunk's tile count is known (gather warps)
   uint64_t mdrain;                              // the MMA thread's last commit
 };
 
@@ -151,7 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int slot_begin = chunk * P.chunk_rows;
   const int rows_here = bad_seq ? 0 : max(0, min(P.chunk_rows, P.topk - slot_begin));
-  const int n_tiles = (rows_here + kRows - 1) / kRows;
+  // The chunk's tiles end at its last valid index (slots past it are masked
+  // and add nothing): the gather warps find it once the index rows are
+  // there and publish the count; every other role waits for it.
+  __shared__ int last_valid, n_tiles_sh;
   const int32_t* idx_row = P.idx + static_cast<size_t>(t) * P.topk;
 
   // CTA 1 layout: V stages, then P slots, alpha, final (m, l)
@@ -172,6 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.alldone, 1);
     mbar_init(&bars.ffull, 1);
     mbar_init(&bars.qready, 4);
+    mbar_init(&bars.tiles, 1);
+    last_valid = -1;
     mbar_init(&bars.mdrain, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -188,6 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base;
   volatile int* abort_v = &abort_flag;
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  auto tile_count = [&]() -> int {  // roles other than the gather warps
+    if (!mbar_wait_polling<false>(&bars.tiles, 0, P.err, abort_v)) return 0;
+    return n_tiles_sh;
+  };
 
   const int q_rows = max(0, min(128, P.H - hb * 128));  // real heads of this block
   cluster_sync();  // both CTAs' barriers are initialised before any remote use
@@ -198,12 +208,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 4 && warp < 4 + kGatherWarps) {
     setmaxnreg_dec<kRegsGather>();
+    griddep_wait();  // the index rows come from the previous kernel
+    // the first tile's rows are looked up together with the chunk's last slot
+    long long row_next = rows_here > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
+    int n_tiles;
+    {
+      // a valid last slot (every decode chunk) ends the chunk at once; else
+      // the gather warps find the last valid slot together
+      const int last = rows_here > 0 ? __ldg(idx_row + slot_begin + rows_here - 1) : -1;
+      if (rows_here == 0 || (last >= 0 && last < P.max_L)) {
+        n_tiles = (rows_here + kRows - 1) / kRows;
+      } else {
+        int mx = -1;
+        for (int i = (warp - 4) * 32 + lane; i < rows_here; i += kGatherWarps * 32) {
+          const int s = __ldg(idx_row + slot_begin + i);
+          if (s >= 0 && s < P.max_L) mx = i;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0 && mx >= 0) atomicMax(&last_valid, mx);
+        asm volatile("bar.sync 1, %0;" ::"n"(kGatherWarps * 32) : "memory");
+        n_tiles = (last_valid + kRows) / kRows;
+      }
+      if (warp == 4 && lane == 0) {
+        n_tiles_sh = n_tiles;
+        mbar_arrive(&bars.tiles);
+      }
+    }
     if (rank == 0) {
       // ------------------------------------------------ gather K (CTA 0)
-      griddep_wait();
       int st = 0;
       uint32_t ph = 0;
-      long long row_next = n_tiles > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
       for (int j = 0; j < n_tiles; ++j) {
         const long long row = row_next;
         if (j + 1 < n_tiles) row_next = gather_row(P, idx_row, b, slot_begin + (j + 1) * kRows, warp - 4, lane);
@@ -216,10 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
       // ------------------------------------------------ gather V (CTA 1)
-      griddep_wait();
       int st = 0;
       uint32_t ph = 0;
-      long long row_next = n_tiles > 0 ? gather_row(P, idx_row, b, slot_begin, warp - 4, lane) : -1;
       for (int j = 0; j < n_tiles; ++j) {
         const long long row = row_next;
         if (j + 1 < n_tiles) row_next = gather_row(P, idx_row, b, slot_begin + (j + 1) * kRows, warp - 4, lane);
@@ -233,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     bool ok = true;
+    int n_tiles = -1;  // set by each role where it first needs it (tile_count)
     if (warp < 4) {
       setmaxnreg_inc<kRegsSoftmax>();
       if (rank == 0) {
@@ -291,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi = (slot0 + 32 + lane < P.topk) ? __ldg(idx_row + slot0 + 32 + lane) : -1;
         };
         int nx_lo = -1, nx_hi = -1;
-        if (n_tiles > 0) load_idx(0, nx_lo, nx_hi);
+        if (rows_here > 0) load_idx(0, nx_lo, nx_hi);  // before the tile count: one round trip
+        n_tiles = tile_count();
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int s_lo = nx_lo, s_hi = nx_hi;
           if (j + 1 < n_tiles) load_idx(j + 1, nx_lo, nx_hi);
@@ -344,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_async_v2(remote_final + hrow * 8, __float_as_uint(m_used), __float_as_uint(l_sum), remote_ffull);
       } else {
         // ----------------------------------------- correction (CTA 1)
+        n_tiles = tile_count();
         const int hrow = warp * 32 + lane;
         int consumed = 0;  // odone phases observed
         for (int j = 0; j < n_tiles && ok; ++j) {
@@ -385,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == kMmaWarp && rank == 0) {
         // ---------------------------------------------- QK^T MMA (CTA 0)
         if (lane == 0) {
+          n_tiles = tile_count();
           const uint32_t idesc = idesc_f16(128, kRows, kFmtBF16, 0, 0);
           int st = 0, sb = 0;
           uint32_t ph = 0, phs = 0;
@@ -411,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (warp == kMmaWarp) {
         // ------------------------------------------------- PV MMA (CTA 1)
         if (lane == 0) {
+          n_tiles = tile_count();
           const uint32_t idesc = idesc_f16(128, 256, kFmtBF16, 0, 1);
           int st = 0;
           uint32_t ph = 0;
@@ -443,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (warp == kRelayWarp && rank == 1) {
         // ----------------------------------- relay: P slot consumed -> CTA 0
         if (lane == 0) {
+          n_tiles = tile_count();
           const uint32_t remote_pfree[2] = {mapa(smem_u32(&bars.pfree[0]), 0), mapa(smem_u32(&bars.pfree[1]), 0)};
           for (int j = 0; j + 2 < n_tiles; ++j) {
             const int ps = j & 1;
@@ -459,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // arrived: normalise, convert to bf16 into a swizzled staging tile (the
       // free V stages) and write it with TMA stores, 64 columns x 128 heads
       // per box (heads past H are clipped by the tensor map).
+      if (n_tiles < 0) n_tiles = tile_count();
+      __syncwarp();
       if (ok && n_tiles > 0) ok = mbar_wait_polling<false>(&bars.alldone, 0, P.err, abort_v);
       if (ok) ok = mbar_wait_polling<true>(&bars.ffull, 0, P.err, abort_v);
       tc_fence_after();
