@@ -115,23 +115,6 @@ __device__ __forceinline__ Group group_of(const IdxParams& P, const uint16_t* gr
   return G;
 }
 
-// Hint: bring the cache line holding `p` into L2.
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
-}
-
-// First token and token count of group g (no global loads).
-__device__ __forceinline__ void group_tokens(const IdxParams& P, const uint16_t* grp, int g, int& t0, int& ntok) {
-  if (grp != nullptr) {
-    t0 = grp[g];
-    ntok = grp[g + 1] - t0;
-  } else {
-    const int b = g / P.groups_per_seq, gj = g % P.groups_per_seq;
-    t0 = b * P.n_q + gj * P.G;
-    ntok = min(P.G, P.n_q - gj * P.G);
-  }
-}
-
 // Work list: the active tiles (tiles holding at least one visible key) of
 // all groups in group-major order.  Every CTA computes the per-group tile
 // counts and their prefix sum, then walks its own contiguous, equal share of
@@ -504,13 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.qfull);
-        // the next group of this CTA's share: its q rows into L2 now, so that
-        // its staging at the next group change reads L2, not DRAM
-        if (ct == 0 && g + 1 < ngroups && tiles_prefix[g + 1] < item_hi) {
-          int tn, nn;
-          group_tokens(P, grp, g + 1, tn, nn);
-          prefetch_l2(P.q + static_cast<size_t>(tn) * P.H_I * d_I, static_cast<uint32_t>(nn * P.H_I * d_I));
-        }
       }
       if (!mbar_wait(&bars.full8[st8], ph8, P.err, abort_v)) break;
       if (!mbar_wait(&bars.empty16[st16], ph16 ^ 1, P.err, abort_v)) break;
@@ -649,15 +625,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           coef[n] = c;
         }
         for (int gi = et; gi < kMaxG; gi += 256) tok_pos[gi] = (gi < G.ntok) ? __ldg(P.pos + G.t0 + gi) : -1;
-        if (g + 1 < ngroups && tiles_prefix[g + 1] < item_hi) {  // the next group's weights, into L2
-          int tn, nn;
-          group_tokens(P, grp, g + 1, tn, nn);
-          const char* wb = reinterpret_cast<const char*>(P.w + static_cast<size_t>(tn) * P.H_I);
-          const char* sb = reinterpret_cast<const char*>(P.q_scale + static_cast<size_t>(tn) * P.H_I);
-          const int wl = nn * P.H_I * 4, sl = nn * P.H_I * 2;
-          if (et * 128 < wl) prefetch_line_l2(wb + et * 128);
-          if (et * 128 < sl) prefetch_line_l2(sb + et * 128);
-        }
         if (!ep_sync()) return false;
       }
       if (!mbar_wait(&bars.tfull[acc], aph, P.err, abort_v)) return false;
