@@ -62,6 +62,27 @@ def test_all_masked_and_duplicates(cuda_lib):
     _attn_with_idx(inp, idx)
 
 
+def test_masked_tails_end_chunks_early(cuda_lib):
+    """Chunks of four 64-row tiles (16 tokens, top-1024) whose index rows end
+    in masked slots: the chunk stops at its last valid slot, found from the
+    chunk's last slot when that is valid and by a scan of the chunk when it
+    is not (valid slots after masked ones included)."""
+    inp = W.make_decode_inputs(B=2, n_q=8, seq_lens=[3000, 2500], H_I=4, d_I=64, topk=1024, H=128, seed=26)
+    rng = np.random.default_rng(26)
+    idx = _random_idx(rng, inp)
+    idx[0, 300:] = -1                  # a valid prefix: chunk 1 keeps one tile, chunks 2-3 none
+    idx[1, 255::256] = -1              # every chunk's last slot masked, the one before valid
+    idx[2] = -1
+    idx[2, ::256] = 11                 # one valid slot at the start of each chunk
+    idx[3] = -1
+    idx[3, 190] = 40                   # one valid slot in chunk 0's third tile
+    idx[4] = -1                        # nothing selected
+    idx[5, rng.random(inp.topk) < 0.3] = -1
+    idx[5, 700:] = -1                  # scattered holes, then a masked tail
+    idx[6, 1000:1023] = -1             # a valid last slot after masked ones
+    _attn_with_idx(inp, idx)
+
+
 def test_large_scores_trigger_rescale(cuda_lib):
     """Scaled-up q and rope dims make later tiles exceed the running max by
     far more than 2^8, exercising the O rescale path; the value dims keep
