@@ -199,10 +199,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
                                           volatile int* abort_flag) {
   return mbar_wait_bounded<false>(bar, parity, err, abort_flag);
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err,
-                                                  volatile int* abort_flag) {
-  return mbar_wait_bounded<true>(bar, parity, err, abort_flag);
-}
 
 // Register reallocation between warpgroups (every thread of the warpgroup
 // executes the same instruction).
@@ -233,12 +229,6 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ int4 ld_cluster_v4(uint32_t addr) {
-  int4 v;
-  asm volatile("ld.shared::cluster.v4.s32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
   return v;
 }
 // Asynchronous store into another CTA's shared memory; completion counts
@@ -277,18 +267,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// Row gather: rows y0..y3 of a 2-D tensor map whose box is {box_x, 1},
-// columns [x, x + box_x), into four consecutive box rows at smem_dst (with
-// the map's swizzle).  Every row must be a valid row of the tensor.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-        "r"(smem_u32(bar))
-      : "memory");
-}
 // 3-D tiled store shared -> global (bulk group completion).
 __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
@@ -310,24 +288,6 @@ __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
 __device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
 __device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
 
-// 3-D tiled load global -> shared (this CTA), mbarrier completion.
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
-// another CTA of the cluster; dst and bar are shared::cluster addresses.
-__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar) : "memory");
-}
-// Copies a 128-row x 256-bit slice of a shared-memory matrix (descriptor)
-// into TMEM lanes 0..127, 8 columns from taddr.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Hint: bring `bytes` (a multiple of 16) at 16-byte aligned `src` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
