@@ -399,6 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
   __shared__ uint32_t lh[2][kLowBins];  // this CTA's counts, passes 1 and 2
   __shared__ uint32_t gh[2][kLowBins];  // CTA 0: the cluster's counts (tie path)
   __shared__ __align__(8) uint32_t cnt[4];  // CTA 0: slots above B, candidates (one u64), emission
+  __shared__ uint2 grp_s[32];               // CTA 0: the k-th key's group when it is small
+  __shared__ uint32_t grp_n;
   const int tid = threadIdx.x;
   const uint32_t rank = cluster_ctarank();
   uint32_t ncta;
@@ -408,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
     lh[0][i] = 0; lh[1][i] = 0; gh[0][i] = 0; gh[1][i] = 0;
   }
   if (tid < 4) cnt[tid] = 0;
+  if (tid == 0) grp_n = 0;
   // CTA 0's counters are zero before any peer's atomics: the arrive is here,
   // the matching wait just before the first remote access, so the barrier
   // overlaps the loads below.
@@ -506,8 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
     if (tid == 0 && n_cand != c_bin) atomicOr(P.err, kErrBadIndex);
     uint32_t prefix = ub << 20, mask = 0xFFF00000u;
     bool whole_bin = false;  // the k-th key's digit group is taken entirely
+    bool small = false;      // or it holds at most 32 keys: one warp ranks them, no second pass
 #pragma unroll 1
-    for (int pass = 0; pass < 2 && !whole_bin; ++pass) {
+    for (int pass = 0; pass < 2 && !whole_bin && !small; ++pass) {
       const int shift = pass == 0 ? 10 : 0;
       for (uint32_t i = tid; i < n_cand; i += kThreads) {
         const uint32_t key = cand[i].x;
@@ -527,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
       mask |= static_cast<uint32_t>(kLowBins - 1) << shift;
       // every key of the found group is needed: the lower bits do not matter
       whole_bin = (cb == need);
+      small = !whole_bin && cb <= 32u;
     }
     // Keys of bin B above the group `prefix/mask` come first; then `need`
     // keys of the group itself (all of it when whole_bin, else the copies of
@@ -539,8 +544,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_hist_kernel(const TopkHistPa
         const uint32_t q = atomicAdd(&cnt[2], 1u);
         if (c_above + q < base_eq) out[c_above + q] = static_cast<int32_t>(c.y);
       } else if (g == prefix) {
-        const uint32_t q = atomicAdd(&cnt[3], 1u);
-        if (q < need) out[base_eq + q] = static_cast<int32_t>(c.y);
+        if (small) {
+          const uint32_t q = atomicAdd(&grp_n, 1u);
+          if (q < 32u) grp_s[q] = c;
+        } else {
+          const uint32_t q = atomicAdd(&cnt[3], 1u);
+          if (q < need) out[base_eq + q] = static_cast<int32_t>(c.y);
+        }
+      }
+    }
+    if (small) {  // the `need` largest keys of the group (equal keys in list order)
+      __syncthreads();
+      if (tid < 32) {
+        const uint32_t n = min(grp_n, 32u);
+        const uint2 me = tid < static_cast<int>(n) ? grp_s[tid] : make_uint2(0u, 0u);
+        uint32_t rank = 0;
+        for (uint32_t m = 0; m < n; ++m) {
+          const uint2 o = grp_s[m];
+          rank += (o.x > me.x || (o.x == me.x && m < static_cast<uint32_t>(tid))) ? 1u : 0u;
+        }
+        if (tid < static_cast<int>(n) && rank < need) out[base_eq + rank] = static_cast<int32_t>(me.y);
       }
     }
     return;
