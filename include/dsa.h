@@ -217,7 +217,12 @@ int dsa_indexer_prolog_noalloc(const dsa_prolog_args* args, void* stream);
  * [n_rows], key s of sequence b at row block_table[b, s / block_size] *
  * block_size + s % block_size, block_table int32 [B, max_blocks],
  * max_L = max_blocks * block_size.  k_cache and k_scale are 16-byte
- * aligned (each tile's scales are copied with its keys in bulk).
+ * aligned (each tile's scales are copied with its keys in bulk).  Every
+ * block_table entry that a visible key reaches must name a page of the
+ * cache (0 <= id and (id + 1) * block_size <= n_rows): n_rows is not an
+ * argument, so the upper bound is the caller's to keep.  A negative entry
+ * is recorded as DSA_ERR_DEVICE_DATA (row 0 is read in its place; the
+ * scores of that page are unspecified).
  * Supported: d_I in {64, 128}; H_I in {4, 8, 16, 32, 64, 128}; topk >= 1;
  * a token-group table that fits shared memory (B * ceil(n_q / G) <= 4096
  * groups for a uniform batch, G = min(n_q, 128 / H_I, 32); about
@@ -291,7 +296,10 @@ int dsa_indexer_dots_debug(const dsa_topk_args* args, int32_t* dots, void* strea
  * Shapes: q bf16 [T, H, d_qk]; kv bf16 contiguous [B, max_L, d_qk] or paged
  * [n_rows, d_qk] through block_table int32 [B, max_blocks] as above;
  * topk_idx int32 [T, topk] with entries in [-1, max_L); out bf16
- * [T, H, d_v]; lse fp32 [T, H] or NULL.
+ * [T, H, d_v]; lse fp32 [T, H] or NULL.  A selected index must lie in a
+ * page of the cache (as for dsa_indexer_topk, the upper bound is not
+ * checked); one whose block_table entry is negative reads a zero row (a
+ * logit of 0 with a zero value) and is not reported.
  * Supported: d_qk = 576, d_v = 512, 1 <= H <= 128, 1 <= topk <= 65536.
  * Workspace: dsa_sparse_attn_workspace() bytes.
  * ---------------------------------------------------------------------- */
