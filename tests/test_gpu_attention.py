@@ -104,6 +104,18 @@ def test_paged_kv(cuda_lib):
     _attn_with_idx(inp, _random_idx(rng, inp))
 
 
+@pytest.mark.parametrize("block_size", [1, 3, 16, 256])
+def test_paged_kv_page_sizes(block_size, cuda_lib):
+    """Pages of one row, of an odd row count (max_L = 2049 = 683 pages of
+    3), of 16 rows and of 256 rows: each selected row is looked up through
+    its own page."""
+    max_L = -(-2048 // block_size) * block_size
+    inp = W.make_decode_inputs(B=3, n_q=1, seq_lens=[700, 2000, 1500], H_I=4, d_I=64, topk=300, H=128,
+                               seed=60 + block_size, block_size=block_size, max_L=max_L)
+    rng = np.random.default_rng(block_size)
+    _attn_with_idx(inp, _random_idx(rng, inp, frac_invalid=0.05))
+
+
 def test_heads_above_128(cuda_lib):
     inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[512], H_I=4, d_I=64, topk=128, H=160, seed=25)
     rng = np.random.default_rng(6)

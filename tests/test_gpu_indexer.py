@@ -57,6 +57,21 @@ def test_paged_decode_indexer(cuda_lib):
     _check_all(inp, buf)
 
 
+@pytest.mark.parametrize("block_size,d_I,H_I", [(8, 128, 64), (16, 64, 32), (32, 128, 16), (128, 128, 64),
+                                                 (256, 64, 128)])
+def test_paged_page_sizes(block_size, d_I, H_I, cuda_lib):
+    """Every supported kind of page: pages smaller than a 128-key tile (8,
+    16, 32 keys: one box per page, the last tile's boxes cut after the last
+    visible key), a page of one tile and pages of two tiles; both key
+    widths, and head counts on both top-k paths (histogram-seeded for
+    H_I >= 64, the general kernel below)."""
+    inp = W.make_decode_inputs(B=3, n_q=2, seq_lens=[700, 2048, 1501], H_I=H_I, d_I=d_I, topk=256, H=8,
+                               seed=40 + block_size, block_size=block_size, max_L=2048, with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
 def test_short_rows_pad_with_minus_one(cuda_lib):
     """Prefill-like causal rows where early tokens see fewer than k keys."""
     inp = W.make_decode_inputs(B=1, n_q=384, seq_lens=[384], H_I=64, d_I=128, topk=200, H=8, seed=13,
