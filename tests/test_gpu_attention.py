@@ -116,6 +116,15 @@ def test_paged_kv_page_sizes(block_size, cuda_lib):
     _attn_with_idx(inp, _random_idx(rng, inp, frac_invalid=0.05))
 
 
+@pytest.mark.parametrize("topk", [1, 8192])
+def test_extreme_selection_sizes(topk, cuda_lib):
+    """One selected row per token, and 8192 rows per token (many split
+    chunks merged by the combine), 128 heads."""
+    inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[9000], H_I=4, d_I=64, topk=topk, H=128, seed=70 + topk)
+    rng = np.random.default_rng(topk + 1)
+    _attn_with_idx(inp, _random_idx(rng, inp))
+
+
 def test_heads_above_128(cuda_lib):
     inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[512], H_I=4, d_I=64, topk=128, H=160, seed=25)
     rng = np.random.default_rng(6)

@@ -72,6 +72,19 @@ def test_paged_page_sizes(block_size, d_I, H_I, cuda_lib):
     _check_all(inp, buf)
 
 
+@pytest.mark.parametrize("topk,H_I", [(1, 64), (7, 64), (4096, 64), (1, 32), (4096, 32)])
+def test_topk_extreme_k(topk, H_I, cuda_lib):
+    """k = 1 (the single largest key), a small odd k, and k = 4096 (twice the
+    decode selection), on the histogram-seeded top-k (H_I = 64) and on the
+    general kernel (H_I = 32); one sequence is shorter than 4096 keys, so
+    that row is padded with -1 when k = 4096."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[3001, 20000], H_I=H_I, d_I=128, topk=topk, H=8,
+                               seed=50 + topk, max_L=20096, with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
 def test_short_rows_pad_with_minus_one(cuda_lib):
     """Prefill-like causal rows where early tokens see fewer than k keys."""
     inp = W.make_decode_inputs(B=1, n_q=384, seq_lens=[384], H_I=64, d_I=128, topk=200, H=8, seed=13,
