@@ -86,6 +86,19 @@ def test_prolog_largest_supported_shape(H_I, d_I, cuda_lib):
     _run_and_check(p, cuda_lib, cache_rows=2 * T)
 
 
+@pytest.mark.parametrize("H_I,d_I,d_rope,interleaved", [(1, 128, 64, 0), (3, 64, 32, 1), (17, 128, 8, 0),
+                                                        (100, 128, 128, 1), (7, 64, 64, 0)])
+def test_prolog_head_counts_and_rotary_widths(H_I, d_I, d_rope, interleaved, cuda_lib):
+    """Head counts that are not powers of two (one q CTA pair, a few, and
+    200 q CTAs in two waves with a weight tile cut at row 100) and rotary
+    widths from 8 dims to the whole head, both pair layouts."""
+    T = 5
+    p = W.make_prolog_inputs(T=T, pos=np.array([0, 3, 77, 500, 1023]), slot=np.array([4, -1, 0, 2, 1]),
+                             seed=95 + H_I, H_I=H_I, d_I=d_I, d_rope=d_rope, K_q=1024, D_x=2048,
+                             max_pos=1024, rope_interleaved=interleaved)
+    _run_and_check(p, cuda_lib, cache_rows=6)
+
+
 def test_prolog_repeated_calls_share_the_workspace(cuda_lib):
     """The k / weight sums accumulate in the workspace and the call leaves
     it zeroed: three calls on one workspace give the same checked result."""
