@@ -125,6 +125,15 @@ def test_extreme_selection_sizes(topk, cuda_lib):
     _attn_with_idx(inp, _random_idx(rng, inp))
 
 
+@pytest.mark.parametrize("H", [1, 64, 100])
+def test_head_counts_below_128(H, cuda_lib):
+    """Head blocks only partly filled (1, 64 and 100 of 128 rows), over
+    several split chunks, with a sink per head for H = 100."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[1500, 3000], H_I=4, d_I=64, topk=600, H=H, seed=80 + H)
+    rng = np.random.default_rng(H + 3)
+    _attn_with_idx(inp, _random_idx(rng, inp, frac_invalid=0.05), sink=_sinks(H, 90) if H == 100 else None)
+
+
 def test_heads_above_128(cuda_lib):
     inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[512], H_I=4, d_I=64, topk=128, H=160, seed=25)
     rng = np.random.default_rng(6)

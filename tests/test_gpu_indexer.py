@@ -85,6 +85,18 @@ def test_topk_extreme_k(topk, H_I, cuda_lib):
     _check_all(inp, buf)
 
 
+@pytest.mark.parametrize("H_I,d_I,n_q", [(8, 64, 16), (4, 128, 40), (16, 128, 3)])
+def test_tokens_per_key_tile(H_I, d_I, n_q, cuda_lib):
+    """The indexer scores G = min(n_q, 128 / H_I, 32) tokens of a sequence
+    against each key tile: 16 tokens at H_I = 8, 32 + 8 at H_I = 4 (a
+    group cut at the 32-token bound), and 3 of the possible 8 at H_I = 16."""
+    inp = W.make_decode_inputs(B=2, n_q=n_q, seq_lens=[3000, 2100], H_I=H_I, d_I=d_I, topk=300, H=8,
+                               seed=20 + n_q, max_L=3072, with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
 def test_short_rows_pad_with_minus_one(cuda_lib):
     """Prefill-like causal rows where early tokens see fewer than k keys."""
     inp = W.make_decode_inputs(B=1, n_q=384, seq_lens=[384], H_I=64, d_I=128, topk=200, H=8, seed=13,
