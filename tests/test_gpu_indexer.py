@@ -117,6 +117,19 @@ def test_fused_topk_row_splits(seq_lens, max_L, cuda_lib):
     _check_all(inp, buf)
 
 
+@pytest.mark.parametrize("L,H_I", [(131072, 64), (200064, 64), (12032, 32)])
+def test_long_rows(L, H_I, cuda_lib):
+    """A full row of 131072 keys, the longest the histogram-seeded top-k
+    takes (8 CTAs of 16 keys per thread); 200064 keys, past it (the general
+    kernel on 8-CTA clusters); 12032 keys on the general kernel's 2-CTA
+    clusters.  The other sequence is short."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[L, 5000], H_I=H_I, d_I=128, topk=2048, H=8, seed=19,
+                               with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    _check_all(inp, buf)
+
+
 def test_fused_topk_all_scores_equal(cuda_lib):
     """Zero queries make every visible score 0: any k distinct visible keys
     are a correct answer."""
