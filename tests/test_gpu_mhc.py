@@ -31,3 +31,27 @@ def test_mhc_matches_oracle(hc, iters, cuda_lib):
     np.testing.assert_allclose(pre.cpu().numpy(), rp, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(post.cpu().numpy(), rq, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(comb.cpu().numpy(), rc, rtol=1e-4, atol=1e-6)
+
+
+@pytest.mark.parametrize("n,iters,eps,mag", [(1, 100, 1e-6, 2.0), (129, 100, 0.0, 2.0), (300, 5, 1e-6, 40.0)])
+def test_mhc_limits(n, iters, eps, mag, cuda_lib):
+    """One token; the largest round count (100) with and without eps; and
+    mixes of magnitude ~40, whose comb logits would overflow exp in fp32
+    without the softmax's max shift and whose sigmoids saturate."""
+    hc = 4
+    r = np.random.default_rng(n + iters)
+    w = hc * (2 + hc)
+    mixes = (r.standard_normal((n, w)) * mag).astype(np.float32)
+    scale = np.array([0.8, 1.3, 1.7], np.float32)
+    base = (r.standard_normal(w) * 0.5).astype(np.float32)
+    d = lambda a: torch.from_numpy(a).to(DEV)
+    pre = torch.empty((n, hc), device=DEV)
+    post = torch.empty((n, hc), device=DEV)
+    comb = torch.empty((n, hc, hc), device=DEV)
+    B.dsa_mhc(d(mixes), d(scale), d(base), hc, iters, eps, pre, post, comb)
+    torch.cuda.synchronize()
+    rp, rq, rc = O.mhc(mixes.astype(np.float64), scale.astype(np.float64), base.astype(np.float64), hc, iters, eps)
+    assert np.isfinite(comb.cpu().numpy()).all()
+    np.testing.assert_allclose(pre.cpu().numpy(), rp, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(post.cpu().numpy(), rq, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(comb.cpu().numpy(), rc, rtol=1e-4, atol=1e-6)
