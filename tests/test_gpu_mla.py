@@ -56,6 +56,9 @@ def _check(p, buf, rows):
     (8, 128, 1536, 7168, 0),  # the decode step (B=4, MTP1)
     (17, 16, 2048, 1024, 1),  # 32-token tiles with a ragged tail, the largest K_q, interleaved pairs
     (32, 8, 128, 64, 0),      # the most tokens, one query row block, one atom in all
+    (1, 1, 128, 64, 1),       # one token, one head: the smallest call
+    (5, 100, 640, 3072, 0),   # a head count that is not a power of two, K_q of five 128-blocks
+    (32, 128, 2048, 16384, 1),  # every bound of the header at once
 ])
 def test_mla_matches_oracle(T, H, K_q, D_x, inter, cuda_lib):
     pos = (np.arange(T) * 97 + 11) % 8192
