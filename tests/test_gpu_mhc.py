@@ -55,3 +55,26 @@ def test_mhc_limits(n, iters, eps, mag, cuda_lib):
     np.testing.assert_allclose(pre.cpu().numpy(), rp, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(post.cpu().numpy(), rq, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(comb.cpu().numpy(), rc, rtol=1e-4, atol=1e-6)
+
+
+def test_mhc_at_the_benchmarked_size_sampled(cuda_lib):
+    """2^20 tokens, 4 streams, 20 rounds (the benchmarked call) in one
+    launch; tokens are independent, so 256 sampled tokens are compared."""
+    n, hc, iters, eps = 1 << 20, 4, 20, 1e-6
+    w = hc * (2 + hc)
+    g = torch.Generator(device="cpu").manual_seed(13)
+    mixes = torch.randn((n, w), generator=g) * 2.0
+    scale = torch.tensor([0.8, 1.3, 1.7])
+    base = torch.randn(w, generator=g) * 0.5
+    pre = torch.empty((n, hc), device=DEV)
+    post = torch.empty((n, hc), device=DEV)
+    comb = torch.empty((n, hc, hc), device=DEV)
+    B.dsa_mhc(mixes.to(DEV), scale.to(DEV), base.to(DEV), hc, iters, eps, pre, post, comb)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(14).choice(n, 256, replace=False))
+    rows[-1] = n - 1
+    mx = mixes.numpy()[rows].astype(np.float64)
+    rp, rq, rc = O.mhc(mx, scale.numpy().astype(np.float64), base.numpy().astype(np.float64), hc, iters, eps)
+    np.testing.assert_allclose(pre.cpu().numpy()[rows], rp, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(post.cpu().numpy()[rows], rq, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(comb.cpu().numpy()[rows], rc, rtol=1e-4, atol=1e-6)

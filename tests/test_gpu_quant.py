@@ -144,3 +144,23 @@ def test_int8_gemm_random_shapes_and_paths_agree(cuda_lib):
     torch.cuda.synchronize()
     assert B.device_error() == 0
     np.testing.assert_array_equal(c32.cpu().numpy(), c33.cpu().numpy()[:32])
+
+
+def test_act_quant_at_the_benchmarked_size_sampled(cuda_lib):
+    """[16384, 7168], the benchmarked size, in one launch; every row is
+    quantised on its own, so 64 sampled rows are compared bit for bit (and
+    no code is left at its fill value)."""
+    M, N = 16384, 7168
+    g = torch.Generator(device="cpu").manual_seed(11)
+    x32 = torch.randn((M, N), generator=g) * torch.exp(torch.empty((M, 1)).uniform_(-20, 20, generator=g))
+    x = x32.to(torch.bfloat16)
+    y = torch.full((M, N), 99, dtype=torch.int8, device=DEV)
+    s = torch.full((M,), -1.0, dtype=torch.float32, device=DEV)
+    B.dsa_act_quant(x.to(DEV), y, s, False)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(12).choice(M, 64, replace=False)
+    bits = x[rows].view(torch.int16).numpy().view(np.uint16)
+    ry, rs = O.act_quant(bits, round_scale=False)
+    assert np.array_equal(s.cpu().numpy()[rows].view(np.uint32), rs.view(np.uint32)), "scales differ"
+    assert np.array_equal(y.cpu().numpy()[rows], ry), "codes differ"
+    assert (s.cpu().numpy() > 0).all()
