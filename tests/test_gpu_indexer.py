@@ -97,6 +97,19 @@ def test_tokens_per_key_tile(H_I, d_I, n_q, cuda_lib):
     _check_all(inp, buf)
 
 
+def test_most_token_groups(cuda_lib):
+    """4096 one-token sequences of 1 to 128 keys: the largest token-group
+    table the indexer takes (4096 groups), on the general top-k kernel
+    (T > 512); 128 sampled tokens, the first and last included."""
+    L = np.random.default_rng(3).integers(1, 129, 4096)
+    inp = W.make_decode_inputs(B=4096, n_q=1, seq_lens=L, H_I=64, d_I=128, topk=32, H=8, seed=33, max_L=128,
+                               with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+    buf.run_topk()
+    tokens = sorted(set(np.random.default_rng(4).choice(4096, 126, replace=False).tolist()) | {0, 4095})
+    _check_all(inp, buf, tokens=tokens)
+
+
 def test_short_rows_pad_with_minus_one(cuda_lib):
     """Prefill-like causal rows where early tokens see fewer than k keys."""
     inp = W.make_decode_inputs(B=1, n_q=384, seq_lens=[384], H_I=64, d_I=128, topk=200, H=8, seed=13,
