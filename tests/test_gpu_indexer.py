@@ -110,6 +110,34 @@ def test_most_token_groups(cuda_lib):
     _check_all(inp, buf, tokens=tokens)
 
 
+@pytest.mark.parametrize("H_I,n_q", [(64, 2), (16, [3, 1])])
+def test_scores_and_selection_as_two_calls(H_I, n_q, cuda_lib):
+    """dsa_indexer_scores then dsa_topk_from_scores: the score rows (-inf
+    past each token's causal limit within its group's columns) and the
+    selection from a copy of them with a row pitch wider than max_L."""
+    inp = W.make_decode_inputs(B=2, n_q=n_q, seq_lens=[3001, 4096], H_I=H_I, d_I=128, topk=512, H=8, seed=25,
+                               with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False)
+    scores = torch.full((inp.T, inp.max_L), float("nan"), dtype=torch.float32, device=DEV)
+    B.dsa_indexer_scores(buf.targs, scores)
+    wide = torch.full((inp.T, inp.max_L + 96), float("nan"), dtype=torch.float32, device=DEV)
+    wide[:, :inp.max_L] = scores
+    B.dsa_topk_from_scores(buf.targs, wide)
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    sc = scores.cpu().numpy()
+    idx = buf.topk_idx.cpu().numpy()
+    for t in range(inp.T):
+        ref = oracle_scores_row(inp, t)
+        n = int(inp.pos[t]) + 1
+        g = sc[t, :n].astype(np.float64)
+        assert np.abs(g - ref).max() <= 2e-6 * max(np.abs(ref).max(), 1e-30), f"t={t}"
+        last = int(inp.pos[inp.seq_of_token == inp.seq_of_token[t]].max())
+        assert np.isneginf(sc[t, n:last + 1]).all(), f"t={t}: columns past pos not -inf"
+        check_topk_set(idx[t], ref, n, inp.topk, f"t={t}")
+        check_topk_exact_on_scores(idx[t], sc[t], n, inp.topk, f"t={t}")
+
+
 def test_short_rows_pad_with_minus_one(cuda_lib):
     """Prefill-like causal rows where early tokens see fewer than k keys."""
     inp = W.make_decode_inputs(B=1, n_q=384, seq_lens=[384], H_I=64, d_I=128, topk=200, H=8, seed=13,
