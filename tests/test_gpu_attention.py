@@ -134,6 +134,24 @@ def test_head_counts_below_128(H, cuda_lib):
     _attn_with_idx(inp, _random_idx(rng, inp, frac_invalid=0.05), sink=_sinks(H, 90) if H == 100 else None)
 
 
+@pytest.mark.parametrize("topk", [64, 1000])
+def test_without_lse_output(topk, cuda_lib):
+    """lse = NULL (the output alone), on one chunk per token and on split
+    chunks merged by the combine."""
+    inp = W.make_decode_inputs(B=2, n_q=2, seq_lens=[3001, 4096], H_I=4, d_I=64, topk=topk, H=128, seed=27)
+    buf = DecodeBuffers(inp, DEV, with_attention=True)
+    idx = _random_idx(np.random.default_rng(topk + 9), inp, frac_invalid=0.1)
+    buf.topk_idx.copy_(torch.from_numpy(idx.astype(np.int32)))
+    buf.aargs.lse = None
+    buf.lse.fill_(7.0)
+    buf.run_attn()
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    ref_o, _ = O.sparse_attention(inp, idx, list(range(inp.T)), None)
+    check_attention(buf.out.float().cpu().numpy(), ref_o, what="attn without lse")
+    assert (buf.lse.cpu().numpy() == 7.0).all()
+
+
 def test_heads_above_128(cuda_lib):
     inp = W.make_decode_inputs(B=1, n_q=2, seq_lens=[512], H_I=4, d_I=64, topk=128, H=160, seed=25)
     rng = np.random.default_rng(6)
