@@ -124,8 +124,9 @@ int dsa_set_wait_limit_ns(uint64_t ns);
  * rows are not written; its w row is); q_out int8
  * [T, H_I, d_I]; q_scale_out fp16 [T, H_I]; k_cache int8 [cache_rows, d_I];
  * k_scale_cache fp16 [cache_rows]; slot int64 [T]: row of k_cache that
- * receives token t's key, -1 = none (slots must not repeat); w_out fp32
- * [T, H_I] (required iff w_proj != NULL).
+ * receives token t's key, -1 = none (slots must not repeat; a slot >=
+ * cache_rows is recorded as DSA_ERR_DEVICE_DATA and that key row is not
+ * written); w_out fp32 [T, H_I] (required iff w_proj != NULL).
  * Supported: 1 <= T <= 32, d_I in {64, 128}, 1 <= H_I <= 128, d_rope even
  * with d_rope <= d_I and (d_rope/2) a multiple of d_I/32, K_q <= 2048 and
  * D_x <= 12288, both multiples of 64; x, w_k and w_proj 16-byte aligned.

@@ -190,3 +190,88 @@ def test_wait_limit_runs_out_in_the_mla_prolog_and_the_int8_gemm(cuda_lib):
     got = c.cpu().numpy().astype(np.float64)
     assert (np.abs(got - want) <= np.maximum(np.abs(want) * 2.0 ** -10, 2.0 ** -24)).all()
     np.testing.assert_array_equal(c8.cpu().numpy(), c.cpu().numpy()[:8])  # the two paths agree bit for bit
+
+
+def test_prolog_slot_past_the_cache(cuda_lib):
+    """A slot equal to cache_rows: recorded as invalid device data and that
+    key row is not written; every other token matches the oracle, and the
+    same buffers with valid slots pass again."""
+    p, buf = _prolog()
+    bad = p.slot.copy()
+    bad[2] = 64  # the cache has 64 rows
+    buf.slot.copy_(torch.from_numpy(bad))
+    buf.run()
+    torch.cuda.synchronize()
+    assert B.device_error() == DSA_ERR_DEVICE_DATA
+    assert (buf.k_cache.cpu().numpy()[p.slot[2]] == 99).all()
+    _check_against_oracle(p, buf, [t for t in range(p.T) if t != 2])
+    buf.slot.copy_(torch.from_numpy(p.slot))
+    buf.run()
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    _check_against_oracle(p, buf, np.arange(p.T))
+
+
+def test_mla_slot_past_the_cache(cuda_lib):
+    """The MLA Prolog with a slot equal to cache_rows: recorded, that latent
+    row not written, the other rows within the bf16 rounding; then a call
+    with valid slots on the same workspace passes."""
+    from sparse_attention_prolog_gb300.pipeline import MlaBuffers
+    T, rows, fill = 4, 8, 5.0
+    p = W.make_mla_inputs(T, np.arange(T) + 10, np.arange(T, dtype=np.int64) * 2, seed=811, H=8, K_q=256, D_x=512,
+                          max_pos=64)
+    buf = MlaBuffers(p, DEV, rows, fill)
+    bad = p.slot.copy()
+    bad[1] = rows
+    buf.slot.copy_(torch.from_numpy(bad))
+    buf.run()
+    torch.cuda.synchronize()
+    assert B.device_error() == DSA_ERR_DEVICE_DATA
+    ref = O.mla_prolog(p)
+
+    def close(tokens):
+        kv = buf.kv_cache.float().cpu().numpy().astype(np.float64)
+        for t in tokens:
+            err = np.abs(kv[p.slot[t]] - ref["kv"][t]) - (8e-3 * np.abs(ref["kv"][t]) + 2e-3)
+            assert err.max() <= 0, f"kv row of token {t}"
+
+    assert (buf.kv_cache.float().cpu().numpy()[p.slot[1]] == fill).all()
+    close([0, 2, 3])
+    buf.slot.copy_(torch.from_numpy(p.slot))
+    buf.run()
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    close(range(T))
+
+
+def test_indexer_negative_page_entry(cuda_lib):
+    """A visible page of sequence 0 unmapped (-1 in its block table):
+    recorded as invalid device data; sequence 1's scores and selection are
+    unaffected, and the restored table passes."""
+    from parity_utils import check_topk_set, oracle_scores_row
+    from sparse_attention_prolog_gb300.pipeline import DecodeBuffers
+    inp = W.make_decode_inputs(B=2, n_q=1, seq_lens=[1000, 1500], H_I=64, d_I=128, topk=256, H=8, seed=45,
+                               block_size=64, max_L=1536, with_attention=False)
+    buf = DecodeBuffers(inp, DEV, with_attention=False, keep_scores=True)
+
+    def check(tokens):
+        sc = buf.scores.cpu().numpy()
+        idx = buf.topk_idx.cpu().numpy()
+        for t in tokens:
+            ref = oracle_scores_row(inp, t)
+            n = int(inp.pos[t]) + 1
+            assert np.abs(sc[t, :n] - ref).max() <= 2e-6 * np.abs(ref).max(), f"t={t}"
+            check_topk_set(idx[t], ref, n, inp.topk, f"t={t}")
+
+    bt = inp.block_table.copy()
+    bt[0, 3] = -1
+    buf.block_table.copy_(torch.from_numpy(bt))
+    buf.run_topk()
+    torch.cuda.synchronize()
+    assert B.device_error() == DSA_ERR_DEVICE_DATA
+    check([1])
+    buf.block_table.copy_(torch.from_numpy(inp.block_table))
+    buf.run_topk()
+    torch.cuda.synchronize()
+    assert B.device_error() == 0
+    check([0, 1])
