@@ -1,7 +1,10 @@
 """Host logic of the benchmark, on fake nvidia-smi output (CPU only)."""
 import datetime
+import os
 
 import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _line(t, idx, uuid, sm, mx, hw="Not Active", thermal="Not Active", swt="Not Active", cap="Not Active"):
@@ -49,3 +52,57 @@ def test_profiled_traffic_needs_the_current_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic([("k.cu", "a.txt"), ("k.cu", "missing.txt")]) is None
     (csrc / "k.cu").write_text("kernel v2")
     assert bench.profiled_traffic([("k.cu", "a.txt")]) is None
+
+
+REF_KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+            "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"}
+
+
+def _json_lines(text):
+    import json
+    return [json.loads(line) for line in text.splitlines() if line.startswith("{")]
+
+
+def _check_reference_line(d, n_gpus):
+    import bench
+    assert REF_KEYS <= set(d)
+    assert d["impl"] == "reference" and d["n_gpus"] == n_gpus
+    assert (d["metric"], d["unit"], d["higher_is_better"]) == (bench.METRIC, bench.UNIT, True)
+    assert d["config"]["workload"] == bench.WORKLOAD
+    assert d["warmup"] >= 3 and d["steps"] == 1 and d["value"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores and
+    prints one line with the headline's metric, unit and workload."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
+                        "--ref-tokens", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 1)
+
+
+def test_reference_arm_under_two_ranks():
+    """Launched as two ranks (gloo on the CPU): rank 0 alone runs and prints
+    the line; the other rank exits 0 without work."""
+    import socket
+    import subprocess
+    import sys
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+                        "--steps", "1", "--warmup", "0", "--ref-tokens", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 2)
