@@ -106,3 +106,20 @@ def test_reference_arm_under_two_ranks():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_reference_line(lines[0], 2)
+
+
+def test_every_profile_summary_names_its_sources_and_command():
+    """Each committed ncu summary gives the command that made it and the
+    kernel sources it was taken on, and those sources are the current ones
+    (a kernel changed after its capture would make the benchmark report
+    its traffic as null)."""
+    import glob
+    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", "*.txt")))
+    assert paths
+    for path in paths:
+        text = open(path).read()
+        vals = dict((k.strip(), v.strip()) for k, v in (line.split(":", 1) for line in text.splitlines()
+                                                         if ":" in line))
+        assert "ncu" in text and "--clock-control none" in text, path
+        srcs = [s.strip() for s in vals["sources"].split(",")]
+        assert vals["source_sha256_16"] == bench.src_hash(*srcs), f"{path}: taken on other sources"
