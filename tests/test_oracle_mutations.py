@@ -55,6 +55,12 @@ MUTANTS = [
      "out = (p @ kv[:, :d_v]) / l", "out = (p @ kv[:, -d_v:]) / l"),
     ("attention sink left out of the denominator",
      "l = l + np.exp(sk[:, None] - m)", "l = l"),
+    ("attention sink term not shifted by the running max",
+     "l = l + np.exp(sk[:, None] - m)", "l = l + np.exp(sk[:, None])"),
+    ("attention lse without the max added back",
+     "return out, (m + np.log(l))[:, 0]", "return out, np.log(l)[:, 0]"),
+    ("attention max ignoring the sink",
+     "m = np.maximum(m, sk[:, None])", "m = m"),
     ("power-of-two scale rounded down",
      "up = np.where(m == 0.5, e - 1, e).astype(np.int32)", "up = (e - 1).astype(np.int32)"),
     ("mHC rounds normalising columns before rows",
@@ -192,6 +198,7 @@ def test_unmutated_copy_passes_every_pin(monkeypatch):
     assert _failing_pin(_module(SRC), monkeypatch) is None
 
 
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")  # a mistaken oracle may overflow
 @pytest.mark.parametrize("what,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_planted_mistake_fails_a_pin(what, old, new, monkeypatch):
     assert SRC.count(old) == 1, f"the oracle text for '{what}' is not unique"

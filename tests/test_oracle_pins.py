@@ -301,6 +301,55 @@ def test_indexer_hand_worked_case():
     np.testing.assert_array_equal(O.topk_indices(I0, 1, 2), g["top2_pos0"])
 
 
+def _golden_value(tok):
+    """A value of the attention golden file: "a/b", "log a/b" or "-inf"."""
+    from fractions import Fraction
+    if tok == "-inf":
+        return -np.inf
+    if tok.startswith("log "):
+        return float(np.log(float(Fraction(tok[4:]))))
+    return float(Fraction(tok))
+
+
+def test_attention_hand_worked_case():
+    g = {}
+    with open(os.path.join(GOLDEN, "attention_hand_case.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(None, 1)
+            if key in ("q", "row"):
+                name, vals = rest.split(None, 1)
+                g.setdefault(key, []).append([float(v) for v in vals.split()])
+            elif key == "scale":
+                g[key] = _golden_value(rest)
+            else:
+                name, val = rest.split(None, 1)
+                g.setdefault(key, []).append(_golden_value(val))
+    q, rows = np.array(g["q"]), np.array(g["row"])
+    out, lse = O.sparse_attention_token(q, rows, g["scale"], 1)
+    np.testing.assert_allclose(out[:, 0], g["out"], rtol=1e-13)
+    np.testing.assert_allclose(lse, g["lse"], rtol=1e-13)
+    out, lse = O.sparse_attention_token(q, rows, g["scale"], 1, sink=np.array(g["sink"]))
+    np.testing.assert_allclose(out[:, 0], g["out_sink"], rtol=1e-13)
+    np.testing.assert_allclose(lse, g["lse_sink"], rtol=1e-13)
+    out, lse = O.sparse_attention_token(q, rows[:0], g["scale"], 1, sink=np.array(g["sink"]))
+    assert (out == 0).all()
+    np.testing.assert_array_equal(lse, g["empty_lse_sink"])
+
+
+def test_attention_sink_far_above_the_logits():
+    """A sink 1000 above every logit takes the whole softmax: the output is
+    0 to within e^-999 and lse equals the sink, without overflow (a
+    softmax shifted by the logits' max alone would divide by infinity)."""
+    q = np.array([[0.0, 1.0]])
+    rows = np.array([[2.0, 0.0], [6.0, 1.0]])
+    out, lse = O.sparse_attention_token(q, rows, 1.0, 1, sink=np.array([1000.0]))
+    assert np.isfinite(out).all() and np.abs(out).max() < 1e-300
+    np.testing.assert_allclose(lse, [1000.0], rtol=1e-15)
+
+
 def test_indexer_scores_brute_force_loops():
     H, D, n = 3, 8, 11
     q = rng.integers(-127, 128, size=(H, D)).astype(np.int8)
