@@ -14,9 +14,11 @@ independent device copies of every input (caches, weights, queries; about
 before it; `--l2 flush` instead writes 256 MiB before every step (which also
 evicts the kernels' code from L2).  `e2e` repeats
 the step through the C ABI with host buffers (pinned H2D of the step's new
-inputs, D2H of the attention output) timed on the host, launched as one CUDA
-graph per step (the copies and calls issued one by one are reported beside
-it as `eager_value`); `roofline` is the
+inputs, D2H of the attention output) timed on the host: step k+1's copies
+in and step k's read-back overlap step k's calls on their own streams, as a
+serving loop runs them; the serial loop (copies, calls and read-back, then a
+synchronize) and the calls issued one by one are reported beside it as
+`serial_value` and `eager_value`; `roofline` is the
 dominant kernel's algorithmic bytes / its event-timed duration against the
 measured HBM copy bandwidth.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload.
